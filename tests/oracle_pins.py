@@ -1,0 +1,408 @@
+"""Pins for the float64 oracle: checks against facts that the pages and the
+mathematics fix, independent of the oracle's own code.
+
+Each pin is a function ``pin_*(lib)`` that raises ``AssertionError`` when the
+oracle library ``lib`` disagrees with the fact.  ``test_oracle_pins.py`` runs
+them against the real oracle; ``test_oracle_mutants.py`` runs them against
+deliberately broken copies of the oracle and requires each copy to fail at
+least one pin.
+
+Facts used (no pin re-types the oracle's formula):
+  * closed forms: uniform logits give logp = -ln V; V = 1 gives 0; V = 2 gives
+    -log1p(exp(x_other - x_id));
+  * brute force in 50-digit decimal arithmetic on rows of V <= 16;
+  * invariants: probabilities sum to one; shifting every logit by a constant
+    changes nothing; a -inf logit is the same as a missing column;
+  * a library routine: scipy's log_softmax in float64;
+  * the metric definitions of the Diagnostics table ("WS2 Cross-Config
+    Logprob Drift Contract", section "Diagnostics") evaluated on hand-built
+    dlogp vectors in decimal arithmetic, percentiles by their counting
+    definition and by numpy's inverted-CDF percentile;
+  * the zero-update expectation (same page, section "Primary Failure Signal"):
+    identical train and rollout inputs give dlogp = 0, ratio0 = 1,
+    approx_kl0 = 0 exactly;
+  * the masking rule (section "Measurement Contract"): inactive rows never
+    influence any aggregate;
+  * item B1 of the roadmap: zero active tokens and worst-token metadata;
+  * the shard rules of the LogProb knobs table ("[WS2] Framework for ablation
+    experiment", rows 3-5 and 8): exact tiling, single-owner gather, merge
+    result independent of the shard split up to rounding.
+"""
+from __future__ import annotations
+
+import math
+from decimal import Decimal, getcontext
+
+import numpy as np
+
+import oracle
+
+getcontext().prec = 50
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest-even) and return the raw bits."""
+    f = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def dec_logp(row_vals, idx) -> Decimal:
+    """log softmax of one row in 50-digit decimal arithmetic."""
+    vals = [Decimal(float(v)) for v in row_vals]
+    total = sum((v.exp() for v in vals), Decimal(0))
+    return vals[idx] - total.ln()
+
+
+def _close(a, b, tol, what=""):
+    assert abs(a - b) <= tol, f"{what}: {a!r} vs {b!r} (|diff| {abs(a - b):.3e} > {tol:.1e})"
+
+
+# --------------------------------------------------------------- logp pins
+
+def pin_uniform_minus_log_v(lib):
+    for vocab in (1, 2, 3, 7, 1000, 151936):
+        for c in (0.0, -3.5, 80.0):
+            row = np.full(vocab, c, dtype=np.float32)
+            lp, st = oracle.row_logp(row, vocab // 2, lib=lib)
+            assert st == 0
+            _close(lp, -math.log(vocab), 1e-13 * max(1.0, abs(c)) + 1e-15, f"uniform V={vocab} c={c}")
+            lpb, _ = oracle.row_logp(bf16_bits(row), vocab - 1, lib=lib)
+            _close(lpb, -math.log(vocab), 1e-13 * max(1.0, abs(c)) + 1e-15, f"uniform bf16 V={vocab}")
+
+
+def pin_single_token_vocab(lib):
+    for c in (0.0, 5.25, -1e30):
+        lp, st = oracle.row_logp(np.array([c], dtype=np.float32), 0, lib=lib)
+        assert st == 0 and lp == 0.0, (c, lp)
+
+
+def pin_two_token_closed_form(lib):
+    rng = np.random.default_rng(11)
+    for _ in range(50):
+        x = rng.normal(0, 4, size=2).astype(np.float32)
+        for i in (0, 1):
+            lp, _ = oracle.row_logp(x, i, lib=lib)
+            other = float(x[1 - i]) - float(x[i])
+            want = -math.log1p(math.exp(other)) if other < 30 else -other - math.log1p(math.exp(-other))
+            _close(lp, want, 1e-14, "V=2")
+
+
+def pin_brute_force_decimal(lib):
+    rng = np.random.default_rng(12)
+    for vocab in (3, 5, 8, 16):
+        for _ in range(6):
+            raw = rng.normal(0, 3, size=vocab).astype(np.float32)
+            for arr in (raw, bf16_bits(raw)):
+                vals = arr if arr.dtype == np.float32 else bf16_to_f32(arr)
+                idx = int(rng.integers(0, vocab))
+                lp, _ = oracle.row_logp(arr, idx, lib=lib)
+                _close(lp, float(dec_logp(vals, idx)), 1e-13, f"decimal V={vocab}")
+
+
+def pin_probabilities_sum_to_one(lib):
+    rng = np.random.default_rng(13)
+    for vocab in (10, 257):
+        x = bf16_bits(rng.normal(0, 3, size=vocab).astype(np.float32))
+        total = math.fsum(math.exp(oracle.row_logp(x, j, lib=lib)[0]) for j in range(vocab))
+        _close(total, 1.0, 1e-12, "sum of probabilities")
+
+
+def pin_shift_invariance(lib):
+    rng = np.random.default_rng(14)
+    x = (rng.integers(-8192, 8192, size=300) / 1024.0).astype(np.float32)  # exact in fp32
+    for c in (64.0, -256.0):
+        xs = (x + np.float32(c)).astype(np.float32)
+        assert np.all(xs.astype(np.float64) == x.astype(np.float64) + c)
+        for idx in (0, 17, 299):
+            a, _ = oracle.row_logp(x, idx, lib=lib)
+            b, _ = oracle.row_logp(xs, idx, lib=lib)
+            _close(a, b, 1e-12, "shift")
+
+
+def pin_library_log_softmax(lib):
+    from scipy.special import log_softmax
+
+    rng = np.random.default_rng(15)
+    x = rng.normal(0, 3, size=(4, 5000)).astype(np.float32)
+    x[1, 123] += 15.0
+    ref = log_softmax(x.astype(np.float64), axis=1)
+    for r in range(4):
+        for idx in (0, 123, 4999):
+            lp, _ = oracle.row_logp(x[r], idx, lib=lib)
+            _close(lp, ref[r, idx], 1e-11, "scipy log_softmax")
+
+
+def pin_neg_inf_is_missing_column(lib):
+    rng = np.random.default_rng(16)
+    x = rng.normal(0, 2, size=40).astype(np.float32)
+    y = x.copy()
+    y[[3, 30]] = -np.inf
+    keep = np.array([j for j in range(40) if j not in (3, 30)])
+    for idx in (0, 20, 39):
+        a, st = oracle.row_logp(y, idx, lib=lib)
+        assert st == 0
+        b, _ = oracle.row_logp(np.ascontiguousarray(x[keep]), int(np.searchsorted(keep, idx)), lib=lib)
+        _close(a, b, 1e-14, "-inf column")
+
+
+def pin_selected_index_and_bf16_widening(lib):
+    # logits 0, 1, 2, ... (exact in bf16): logp(j) differs from logp(0) by exactly j
+    x = np.arange(12, dtype=np.float32)
+    for arr in (x, bf16_bits(x)):
+        base, _ = oracle.row_logp(arr, 0, lib=lib)
+        for j in (1, 5, 11):
+            lp, _ = oracle.row_logp(arr, j, lib=lib)
+            _close(lp - base, float(j), 1e-12, "selected index")
+        _close(base, float(dec_logp(x, 0)), 1e-13, "bf16 widening")
+
+
+# --------------------------------------------------------------- metric pins
+
+def _dec_metrics(d, lo, hi):
+    """The Diagnostics table, evaluated in decimal on the active values."""
+    n = len(d)
+    ds = [Decimal(float(v)) for v in d]
+    ratio = [v.exp() for v in ds]
+    return {
+        "ratio0_mean": float(sum(ratio) / n),
+        "approx_kl0": float(sum(r - 1 - v for r, v in zip(ratio, ds)) / n),
+        "mean_abs_dlogp": float(sum(abs(v) for v in ds) / n),
+        "clipfrac0": sum(1 for r in ratio if r < Decimal(lo) or r > Decimal(hi)) / n,
+    }
+
+
+def _nearest_rank_by_counting(values, p):
+    """Smallest v among the values with #{x <= v} >= p*A/100."""
+    a = len(values)
+    best = None
+    for v in values:
+        if sum(1 for x in values if x <= v) * 100 >= p * a:
+            if best is None or v < best:
+                best = v
+    return best
+
+
+def pin_metrics_decimal(lib):
+    rng = np.random.default_rng(21)
+    for n in (1, 2, 5, 37, 200):
+        d = rng.normal(0, 0.3, size=n) * rng.choice([1e-6, 1e-2, 1.0], size=n)
+        d[0] = 0.9  # ratio above 1.2 -> clipped
+        mask = np.ones(n, dtype=np.uint8)
+        got = oracle.metrics(d, mask, 0.8, 1.2, lib=lib)
+        want = _dec_metrics(d, 0.8, 1.2)
+        for k in ("ratio0_mean", "mean_abs_dlogp"):
+            _close(got[k], want[k], 1e-14, k)
+        _close(got["approx_kl0"], want["approx_kl0"], 1e-13 * max(want["approx_kl0"], 1e-300), "approx_kl0")
+        assert got["clipfrac0"] == want["clipfrac0"], (got["clipfrac0"], want["clipfrac0"])
+        assert got["n_active"] == n
+        # the same values with inactive rows interleaved: only active rows count
+        full = np.concatenate([d, rng.normal(0, 5, size=n)])
+        fmask = np.concatenate([mask, np.zeros(n, np.uint8)])
+        order = rng.permutation(2 * n)
+        got2 = oracle.metrics(full[order], fmask[order], 0.8, 1.2, lib=lib)
+        for k in ("ratio0_mean", "mean_abs_dlogp", "clipfrac0"):
+            _close(got2[k], want[k], 1e-14, "masked " + k)
+        assert got2["n_active"] == n
+
+
+def pin_constant_dlogp(lib):
+    for c in (-0.25, 1e-3, 3e-8, 0.5):
+        d = np.full(9, c)
+        got = oracle.metrics(d, np.ones(9, np.uint8), 0.8, 1.2, lib=lib)
+        dc = Decimal(c)
+        k3 = float(dc.exp() - 1 - dc)
+        # expm1(c) - c in double cancels: the error is a few ulps of c, not of the result
+        _close(got["approx_kl0"], k3, 4 * abs(c) * 2.0**-52 + 1e-15 * k3, "k3(c)")
+        _close(got["ratio0_mean"], float(dc.exp()), 1e-15, "ratio0")
+        assert got["mean_abs_dlogp"] == abs(c)
+        assert got["p95_abs_dlogp"] == got["p99_abs_dlogp"] == got["max_abs_dlogp"] == abs(c)
+
+
+def pin_percentiles_definition(lib):
+    rng = np.random.default_rng(22)
+    for n in list(range(1, 41)) + [97, 100, 101, 199, 200]:
+        d = rng.normal(0, 1, size=n)
+        if n > 4:
+            d[:3] = d[3]  # ties
+        absd = np.abs(d)
+        got = oracle.metrics(d, np.ones(n, np.uint8), 0.8, 1.2, lib=lib)
+        for p, key in ((95, "p95_abs_dlogp"), (99, "p99_abs_dlogp"), (100, "max_abs_dlogp")):
+            want = _nearest_rank_by_counting(list(absd), p)
+            assert got[key] == want, (n, key, got[key], want)
+            assert got[key] == np.percentile(absd, p, method="inverted_cdf")
+
+
+def pin_clipfrac_constructed(lib):
+    # ratios 0.5, 1, 2, 0.9, 1.1, 0.79, 1.21: four are outside [0.8, 1.2]
+    d = np.log(np.array([0.5, 1.0, 2.0, 0.9, 1.1, 0.79, 1.21]))
+    got = oracle.metrics(d, np.ones(7, np.uint8), 0.8, 1.2, lib=lib)
+    assert got["clipfrac0"] == 4 / 7, got["clipfrac0"]
+    # a ratio equal to a bound counts as inside: choose bounds that are exp of the data
+    d2 = np.array([-0.5, 0.0, 0.25])
+    got2 = oracle.metrics(d2, np.ones(3, np.uint8), math.exp(-0.5), math.exp(0.25), lib=lib)
+    assert got2["clipfrac0"] == 0.0, got2["clipfrac0"]
+    got3 = oracle.metrics(d2, np.ones(3, np.uint8), math.exp(-0.5) * (1 + 1e-12), 2.0, lib=lib)
+    assert got3["clipfrac0"] == 1 / 3
+
+
+def pin_argmax_lowest_row(lib):
+    d = np.array([0.1, -0.7, 0.3, 0.7, -0.7, 0.2])
+    mask = np.array([1, 0, 1, 1, 1, 1], np.uint8)
+    got = oracle.metrics(d, mask, 0.8, 1.2, lib=lib)
+    assert got["argmax_row"] == 3 and got["max_abs_dlogp"] == 0.7, got
+    mask[1] = 1
+    assert oracle.metrics(d, mask, 0.8, 1.2, lib=lib)["argmax_row"] == 1
+
+
+def pin_zero_active(lib):
+    got = oracle.metrics(np.array([1.0, -2.0]), np.zeros(2, np.uint8), 0.8, 1.2, lib=lib)
+    assert got["n_active"] == 0 and got["flags"] & oracle.FLAG_NO_ACTIVE and got["argmax_row"] == -1
+    for k in ("ratio0_mean", "clipfrac0", "approx_kl0", "mean_abs_dlogp", "p95_abs_dlogp",
+              "p99_abs_dlogp", "max_abs_dlogp"):
+        assert got[k] == 0.0
+
+
+# ------------------------------------------------------- whole-scoring pins
+
+def _case(n_rows, vocab, seed, dtype="bf16"):
+    rng = np.random.default_rng(seed)
+    t = rng.normal(0, 2, size=(n_rows, vocab)).astype(np.float32)
+    r = t + rng.normal(0, 0.05, size=t.shape).astype(np.float32)
+    if dtype == "bf16":
+        t, r = bf16_bits(t), bf16_bits(r)
+    ids = rng.integers(0, vocab, size=n_rows).astype(np.int32)
+    mask = (rng.random(n_rows) < 0.7).astype(np.uint8)
+    mask[0] = 1
+    return t, r, ids, mask
+
+
+def pin_zero_update_expectation(lib):
+    t, _, ids, mask = _case(30, 50, 31)
+    res = oracle.score(t, t, ids, mask, lib=lib)
+    assert res.status == 0
+    assert np.all(res.dlogp == 0.0)
+    m = res.metrics
+    assert m["ratio0_mean"] == 1.0 and m["approx_kl0"] == 0.0 and m["clipfrac0"] == 0.0
+    assert m["mean_abs_dlogp"] == m["p95_abs_dlogp"] == m["max_abs_dlogp"] == 0.0
+    # bf16 against its exact fp32 upcast is the same input
+    up = np.ascontiguousarray(bf16_to_f32(t))
+    res2 = oracle.score(t, up, ids, mask, lib=lib)
+    assert np.all(res2.dlogp == 0.0)
+
+
+def pin_dlogp_sign_and_values(lib):
+    t, r, ids, mask = _case(12, 9, 32, dtype="f32")
+    res = oracle.score(t, r, ids, mask, lib=lib)
+    for i in np.flatnonzero(mask):
+        lt = float(dec_logp(t[i], ids[i]))
+        lr = float(dec_logp(r[i], ids[i]))
+        _close(res.logp_train[i], lt, 1e-13, "logp_train")
+        _close(res.logp_rollout[i], lr, 1e-13, "logp_rollout")
+        _close(res.dlogp[i], lt - lr, 1e-13, "dlogp = train - rollout")
+    assert np.all(res.dlogp[mask == 0] == 0.0)
+
+
+def pin_masked_rows_never_read(lib):
+    t, r, ids, mask = _case(40, 33, 33, dtype="f32")
+    base = oracle.score(t, r, ids, mask, lib=lib)
+    t2, r2, ids2 = t.copy(), r.copy(), ids.copy()
+    off = mask == 0
+    t2[off] = np.nan
+    r2[off, 0] = np.inf
+    ids2[off] = -5
+    res = oracle.score(t2, r2, ids2, mask, lib=lib)
+    assert res.status == 0
+    assert res.metrics == base.metrics
+    active = mask == 1
+    assert np.array_equal(res.dlogp[active], base.dlogp[active])
+
+
+def pin_active_token_count(lib):
+    t, r, ids, mask = _case(50, 7, 34)
+    res = oracle.score(t, r, ids, mask, lib=lib)
+    assert res.metrics["n_active"] == int(mask.sum())
+
+
+def pin_bad_rows_flagged(lib):
+    t, r, ids, mask = _case(6, 10, 35, dtype="f32")
+    mask[:] = 1
+    ids2 = ids.copy()
+    ids2[2] = 10
+    assert oracle.score(t, r, ids2, mask, lib=lib).status == oracle.STATUS_TOKEN_OOB
+    ids2[2] = -1
+    assert oracle.score(t, r, ids2, mask, lib=lib).status == oracle.STATUS_TOKEN_OOB
+    t2 = t.copy()
+    t2[4, 3] = np.nan
+    assert oracle.score(t2, r, ids, mask, lib=lib).status == oracle.STATUS_NONFINITE
+    t3 = t.copy()
+    t3[1, :] = -np.inf
+    assert oracle.score(t3, r, ids, mask, lib=lib).status == oracle.STATUS_NONFINITE
+
+
+def pin_padded_row_stride(lib):
+    t, r, ids, mask = _case(8, 20, 36, dtype="f32")
+    base = oracle.score(t, r, ids, mask, lib=lib)
+    wide = np.full((8, 27), 99.0, dtype=np.float32)
+    wide[:, :20] = t
+    res = oracle.score(wide[:, :20], r, ids, mask, lib=lib)
+    assert np.array_equal(res.dlogp, base.dlogp)
+
+
+# -------------------------------------------------------------- shard pins
+
+def _split(x, bounds):
+    return [np.ascontiguousarray(x[:, a:b]) for a, b in bounds]
+
+
+def pin_sharded_equals_unsharded(lib):
+    t, r, ids, mask = _case(20, 64, 41)
+    base = oracle.score(t, r, ids, mask, lib=lib)
+    for bounds in ([(0, 64)], [(0, 16), (16, 32), (32, 48), (48, 64)], [(0, 5), (5, 63), (63, 64)]):
+        res = oracle.score_sharded(_split(t, bounds), _split(r, bounds), bounds, ids, mask, lib=lib)
+        assert res.status == 0
+        np.testing.assert_allclose(res.logp_train, base.logp_train, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(res.dlogp, base.dlogp, rtol=0, atol=1e-12)
+        perm = list(range(len(bounds)))[::-1]
+        res2 = oracle.score_sharded(_split(t, bounds), _split(r, bounds), bounds, ids, mask, order=perm, lib=lib)
+        np.testing.assert_allclose(res2.logp_rollout, base.logp_rollout, rtol=0, atol=1e-12)
+
+
+def pin_shard_tiling_rules(lib):
+    assert oracle.check_tiling([(0, 10), (10, 20)], 20, lib=lib)
+    assert oracle.check_tiling([(10, 20), (0, 10)], 20, lib=lib)
+    assert not oracle.check_tiling([(0, 10), (11, 20)], 20, lib=lib)   # gap
+    assert not oracle.check_tiling([(0, 11), (10, 20)], 20, lib=lib)   # overlap
+    assert not oracle.check_tiling([(0, 10), (10, 21)], 20, lib=lib)   # past the vocab
+    assert not oracle.check_tiling([(0, 10)], 20, lib=lib)             # short
+    assert not oracle.check_tiling([(0, 10), (5, 15)], 20, lib=lib)    # overlap hides a gap
+    assert not oracle.check_tiling([], 20, lib=lib)
+
+
+# --------------------------------------------------------------- head pins
+
+def pin_head_logits_matmul(lib):
+    from scipy.special import log_softmax
+
+    rng = np.random.default_rng(51)
+    hidden, vocab = 24, 40
+    h = bf16_bits(rng.normal(0, 1, size=(3, hidden)).astype(np.float32))
+    W = bf16_bits(rng.normal(0, 0.5, size=(vocab, hidden)).astype(np.float32))
+    ref = bf16_to_f32(h).astype(np.float64) @ bf16_to_f32(W).astype(np.float64).T
+    for i in range(3):
+        x = oracle.head_logits(h[i], W, lib=lib)
+        np.testing.assert_allclose(x, ref[i], rtol=1e-13, atol=1e-13)
+    h2 = bf16_bits(bf16_to_f32(h) + rng.normal(0, 0.1, size=h.shape).astype(np.float32))
+    ids = rng.integers(0, vocab, size=3).astype(np.int32)
+    res = oracle.score_head_rows(h, h2, W, ids, [0, 2], lib=lib)
+    ref2 = bf16_to_f32(h2).astype(np.float64) @ bf16_to_f32(W).astype(np.float64).T
+    for k, i in enumerate((0, 2)):
+        _close(res.logp_train[k], log_softmax(ref[i])[ids[i]], 1e-12, "head logp train")
+        _close(res.logp_rollout[k], log_softmax(ref2[i])[ids[i]], 1e-12, "head logp rollout")
+
+
+ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
