@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Benchmark of the selected-token logprob drift scorer on GB300.
+
+One step = the whole scoring path over one batch: stage 1 (active-row
+selection), stage 2 (the streaming row pass over both logits tensors plus the
+per-row finalise) and stage 3 (the drift metrics and the percentile select),
+exactly the kernels lpd_score launches, on one stream.  The default workload
+is the Qwen3-8B-vocab shape: B=8 x T=4096 rows, V=151936, bf16 logits on both
+sides (19.9 GB, far larger than the 129 MB L2, so no L2 flush is needed
+between steps).
+
+Printed (one JSON line, rank 0):
+  value      active tokens scored per second, device-timed (CUDA events)
+  roofline   stage 2's algorithmic bytes / its average duration vs the
+             measured HBM copy bandwidth
+  e2e        the same metric through the C ABI with the inputs copied from
+             pinned host memory every step and the metrics record read back
+  cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
+
+--impl reference times the oracle alone (the reference arm of this build).
+Multi-GPU (torchrun, N>1): every rank scores its own batch (replicas, weak
+scaling, no collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+CONFIGS = {
+    "qwen": dict(workload="qwen3-8b-vocab B=8 T=4096 V=151936 bf16/bf16", vocab=151936),
+    "llama": dict(workload="llama-vocab B=64 T=1024 V=128256 bf16/fp32", vocab=128256),
+    "sharded": dict(workload="vocab-sharded B=1 T=32768 V=151936 (4 shards) bf16/bf16", vocab=151936),
+    "tiny": dict(workload="tiny B=2 T=64 V=1024 bf16/bf16", vocab=1024),
+}
+METRIC = "active tokens/sec scored; achieved HBM GB/s vs GB300 peak (logp+drift pass)"
+UNIT = "active_tokens/s"
+KERNEL_SOURCES = ["logprob_drift_scoring_gb300/csrc/lpd_rows.cu"]
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for rel in KERNEL_SOURCES + ["logprob_drift_scoring_gb300/csrc/lpd_internal.cuh"]:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(config: str):
+    """dram bytes per launch of the row pass from the committed ncu summary, if
+    it was captured on the current kernel source; else None."""
+    p = ROOT / "profiles" / f"row_kernel_{config}.md"
+    if not p.exists():
+        return None
+    text = p.read_text()
+    m_src = re.search(r"kernel_source_sha1:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_uuid():
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- workloads
+
+def make_workload(config: str, device, seed_offset: int = 0, batch=None, seq=None):
+    """The named workload; batch/seq shrink it (used only for small ncu captures)."""
+    from logprob_drift_scoring_gb300 import workloads as W
+
+    if config == "qwen":
+        return W.qwen(seed=1 + seed_offset, device=device, batch=batch or 8, seq=seq or 4096)
+    if config == "llama":
+        return W.llama(seed=2 + seed_offset, device=device, batch=batch or 64, seq=seq or 1024)
+    if config == "sharded":
+        return W.sharded(seed=3 + seed_offset, device=device, seq=seq or 32768)
+    if config == "tiny":
+        return W.tiny(seed=0 + seed_offset, device=device)
+    raise SystemExit(f"unknown config {config}")
+
+
+def bytes_per_active_token(w) -> int:
+    """Algorithmic bytes of the row pass per active token: both logits rows
+    once, the token id, and the three fp32 per-token outputs."""
+    ts = w.train if isinstance(w.train, list) else [w.train]
+    rs = w.rollout if isinstance(w.rollout, list) else [w.rollout]
+    row = sum(t.shape[1] * t.element_size() for t in ts) + sum(r.shape[1] * r.element_size() for r in rs)
+    return row + 4 + 12
+
+
+# ---------------------------------------------------------------- our arm
+
+class Runner:
+    """Buffers and the stage sequence of one workload on one device."""
+
+    def __init__(self, w):
+        import torch
+        from logprob_drift_scoring_gb300 import binding as B
+
+        self.B, self.w, self.torch = B, w, torch
+        dev = w.token_ids.device
+        n = w.n_rows
+        self.sharded = isinstance(w.train, list)
+        self.outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+        self.met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=dev)
+        if self.sharded:
+            ws = B.lpd_workspace_size(B.LPD_KIND_SHARDED, n, w.vocab, len(w.v_ranges))
+        else:
+            ws = B.lpd_workspace_size(B.LPD_KIND_SCORE, n)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 5 if n > 0 else 2
+
+    def step(self, ev=None):
+        """One pass of the path; with ev = (e0, e1, e2, e3) records events
+        around stage 1, stage 2 and stage 3 on the current stream."""
+        B, w = self.B, self.w
+        lt, lr, d = self.outs
+        if self.sharded:
+            if ev:
+                ev[0].record()
+            B.lpd_score_sharded(w.train, w.rollout, w.v_ranges, w.token_ids, w.action_mask, *w.clip, None,
+                                lt, lr, d, None, None, self.met, self.ws)
+            if ev:
+                ev[3].record()
+            return
+        if ev:
+            ev[0].record()
+        B.lpd_select_active(w.token_ids, w.action_mask, lt, lr, d, self.met, self.ws)
+        if ev:
+            ev[1].record()
+        B.lpd_token_logp(w.train, w.rollout, lt, lr, d, self.met, self.ws)
+        if ev:
+            ev[2].record()
+        B.lpd_drift_metrics(w.n_rows, w.clip[0], w.clip[1], self.met, self.ws)
+        if ev:
+            ev[3].record()
+
+
+def barrier_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def time_cpu_oracle(config: str, target_s: float = 12.0, max_rows: int = 4096, seed: int = 1234):
+    """The float64 oracle as it stands, single-threaded, on a bounded sample of
+    rows drawn with the workload's recipe (active rows only)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from logprob_drift_scoring_gb300 import workloads as W
+
+    vocab = CONFIGS[config]["vocab"]
+    dt_r = torch.float32 if config == "llama" else torch.bfloat16
+    sigma = 2.0 if config == "tiny" else 3.0
+    noise = {"tiny": 1e-3, "llama": 1e-3}.get(config, 2e-3)
+
+    def to_np(t):
+        if t.dtype == torch.bfloat16:
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        return t.contiguous().numpy()
+
+    lib = oracle.load()
+    probe = 8
+    w = W.synthetic(probe, vocab, seed=seed, device="cpu", dtype_rollout=dt_r, sigma=sigma, rollout_noise=noise,
+                    active_prob=1.0)
+    t0 = time.perf_counter()
+    oracle.score_rows(to_np(w.train), to_np(w.rollout), w.token_ids.numpy(), np.arange(probe), lib=lib)
+    per_row = (time.perf_counter() - t0) / probe
+    n = int(max(16, min(max_rows, target_s / max(per_row, 1e-9))))
+    w = W.synthetic(n, vocab, seed=seed + 1, device="cpu", dtype_rollout=dt_r, sigma=sigma, rollout_noise=noise,
+                    active_prob=1.0)
+    tn, rn, ids = to_np(w.train), to_np(w.rollout), w.token_ids.numpy()
+    t0 = time.perf_counter()
+    oracle.score_rows(tn, rn, ids, np.arange(n), lib=lib)
+    elapsed = time.perf_counter() - t0
+    return {"value": n / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} active rows of the {config} recipe, both sides, float64 serial C, {elapsed:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from logprob_drift_scoring_gb300 import binding as B
+
+    B.lib()  # fail loudly here if the CUDA library is missing
+    w = make_workload(args.config, dev, seed_offset=rank, batch=args.batch, seq=args.seq)
+    runner = Runner(w)
+    n_active = int(w.action_mask.sum().item())
+    bpt = bytes_per_active_token(w)
+
+    for _ in range(args.warmup):
+        runner.step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(K):
+            runner.step(evs[k])
+        stop.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = start.elapsed_time(stop)
+    total_ms = barrier_max(total_ms, world)
+    ms_step = total_ms / K
+    value = world * n_active / (ms_step / 1e3)
+
+    if runner.sharded:
+        stage2 = sum(e[0].elapsed_time(e[3]) for e in evs) / K
+        stage_ms = {"whole_call": stage2}
+    else:
+        s1 = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+        stage2 = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+        s3 = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+        stage_ms = {"select_active": round(s1, 4), "token_logp": round(stage2, 4), "drift_metrics": round(s3, 4)}
+
+    peaks = measured_peaks()
+    achieved = n_active * bpt / (stage2 / 1e3) / 1e9
+    traffic = profiled_traffic(args.config)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"{peaks['source']} copy bandwidth (burst)",
+                "span": "stage 2: row kernel + per-row finalise" if not runner.sharded else "whole call",
+                "algorithmic_bytes_per_launch": n_active * bpt}
+
+    e2e = None
+    if not args.no_e2e and not runner.sharded:
+        e2e = run_e2e(w, args, world)
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = time_cpu_oracle(args.config, target_s=args.cpu_seconds)
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": CONFIGS[args.config]["workload"] if not (args.batch or args.seq)
+                       else f"{args.config} reduced B={args.batch} T={args.seq}",
+                       "rows": w.n_rows, "active_tokens": n_active,
+                       "vocab": w.vocab, "logits_bytes": w.logits_bytes(), "l2": "inputs exceed L2 (no flush)",
+                       "parallelism": f"replicas x{world}", "input_dtypes": _dtypes(w)},
+            "stage_ms": stage_ms,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": runner.launches_per_step * K if not runner.sharded else 5 * K,
+            "clocks": clocks.summary(),
+            "impl": "lpd",
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return out
+
+
+def _dtypes(w):
+    t = w.train[0] if isinstance(w.train, list) else w.train
+    r = w.rollout[0] if isinstance(w.rollout, list) else w.rollout
+    return f"{str(t.dtype).replace('torch.', '')}/{str(r.dtype).replace('torch.', '')}"
+
+
+def run_e2e(w, args, world: int = 1):
+    """Through lpd_score with host inputs: per step, copy logits, ids and mask
+    from pinned host memory, score, and read the metrics record back."""
+    import torch
+    from logprob_drift_scoring_gb300 import binding as B
+
+    dev = w.token_ids.device
+    host = []
+    pinned = True
+    for t in (w.train, w.rollout, w.token_ids, w.action_mask):
+        try:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        except RuntimeError:
+            h = torch.empty(t.shape, dtype=t.dtype)
+            pinned = False
+        h.copy_(t)
+        host.append(h)
+    dbuf = [torch.empty_like(t) for t in (w.train, w.rollout, w.token_ids, w.action_mask)]
+    outs = [torch.empty(w.n_rows, dtype=torch.float32, device=dev) for _ in range(3)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=dev)
+    met_host = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, pin_memory=pinned)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, w.n_rows), dtype=torch.uint8, device=dev)
+    bi = sum(h.numel() * h.element_size() for h in host)
+    n_active = int(w.action_mask.sum().item())
+
+    def one():
+        for d, h in zip(dbuf, host):
+            d.copy_(h, non_blocking=True)
+        B.lpd_score(dbuf[0], dbuf[1], dbuf[2], dbuf[3], w.clip[0], w.clip[1], *outs, met, ws)
+        met_host.copy_(met, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    steps = args.e2e_steps
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = barrier_max(s.elapsed_time(e) / steps, world)
+    del dbuf, host
+    torch.cuda.empty_cache()
+    return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ms, 3), "pinned": pinned,
+            "steps": steps}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+
+    import oracle
+    from logprob_drift_scoring_gb300 import workloads as W
+
+    vocab = CONFIGS[args.config]["vocab"]
+    dt_r = torch.float32 if args.config == "llama" else torch.bfloat16
+    rows_per_step = args.ref_rows
+
+    def to_np(t):
+        if t.dtype == torch.bfloat16:
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        return t.contiguous().numpy()
+
+    lib = oracle.load()
+    times = []
+    for k in range(args.warmup + args.steps):
+        w = W.synthetic(rows_per_step, vocab, seed=5000 + k, device="cpu", dtype_rollout=dt_r, active_prob=1.0)
+        tn, rn, ids = to_np(w.train), to_np(w.rollout), w.token_ids.numpy()
+        mask = np.ones(rows_per_step, np.uint8)
+        t0 = time.perf_counter()
+        oracle.score(tn, rn, ids, mask, *w.clip, lib=lib)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = rows_per_step / (ms / 1e3)
+    sample = f"{rows_per_step} active rows per step of the {args.config} recipe (V={vocab}), float64 serial C"
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": CONFIGS[args.config]["workload"], "sample_rows_per_step": rows_per_step},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["lpd", "reference"], default="lpd")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="qwen")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")
+    ap.add_argument("--seq", type=int, default=None, help="override T (small profiling cases only)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * lpd.h - selected-token logprob drift scoring on one GB300 (sm_103a).
+ *
+ * C ABI of liblpd.so.  Plain pointers and sizes only; no C++ or torch types.
+ *
+ * What it computes ("WS2 Cross-Config Logprob Drift Contract", section
+ * "Measurement Contract"): the already-sampled sequence is teacher-forced
+ * through both the training-side and the rollout-side logits; for every
+ * active response/action token r
+ *
+ *     logp_side[r] = x_side[r, id[r]] - log(sum_j exp(x_side[r, j]))
+ *     dlogp[r]     = logp_train[r] - logp_rollout[r]
+ *
+ * and, over active tokens only (section "Diagnostics"): ratio0 = exp(dlogp)
+ * (reported as its mean), clipfrac0 (fraction of ratio0 outside the clip
+ * range), approx_kl0 = mean of exp(dlogp) - 1 - dlogp, and the mean, 95th and
+ * 99th percentile and maximum of |dlogp|.  Percentiles are nearest-rank: the
+ * value of 1-based rank ceil(p * A / 100) among the A ascending |dlogp|.
+ *
+ * Row convention ("[WS2] Framework for ablation experiment", LogProb knobs
+ * table, row 8, "pre-shifted input convention"): logits row r scores
+ * token_ids[r]; the caller does the shift.  action_mask[r] != 0 marks an
+ * active token; prompt and padding rows carry 0, so left and right padding
+ * look the same to the library.  Inactive rows are never read: their logits
+ * and token ids may hold anything.
+ *
+ * Determinism: each row's arithmetic order depends only on the vocabulary
+ * size and the logical column index, never on the row's position, the batch,
+ * the grid or the storage dtype, so the same row gives bitwise-identical
+ * results whatever batch it is scored in (the batch-composition control of
+ * "Attention Debug Matrix", section "Metrics", must be bitwise zero).  No
+ * floating-point atomics are used anywhere.
+ *
+ * Memory: the caller owns every buffer.  Logits, ids, mask, per-token outputs,
+ * the metrics record and the workspace are DEVICE pointers; nothing is
+ * allocated or retained by the library between calls.  All calls are
+ * asynchronous on the given stream (a cudaStream_t passed as void*, NULL for
+ * the legacy default stream) and may be captured in a CUDA graph.
+ *
+ * Errors: invalid arguments are detected on the host before anything is
+ * launched and returned as a negative LPD_ERR_* code.  Problems that only the
+ * device can see are reported in lpd_metrics.status (LPD_STATUS_* bits) and
+ * never trap: a token id outside [0, vocab) on an active row, or a non-finite
+ * log-sum-exp or selected logit on an active row.  When status != 0 the
+ * metric values are unspecified; per-token outputs of the offending rows are
+ * NaN or non-finite.
+ */
+#ifndef LPD_H
+#define LPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- element types --------------------------------------------------- */
+#define LPD_BF16 0 /* bfloat16, 2 bytes */
+#define LPD_F32 1  /* IEEE float32, 4 bytes */
+
+/* ---- return codes ----------------------------------------------------- */
+#define LPD_OK 0
+#define LPD_ERR_NULL_POINTER (-1) /* a required pointer is NULL */
+#define LPD_ERR_BAD_SIZE (-2)     /* n_rows < 0, vocab <= 0, hidden <= 0, ... */
+#define LPD_ERR_BAD_DTYPE (-3)    /* dtype not LPD_BF16 / LPD_F32, or mixed within a side */
+#define LPD_ERR_BAD_STRIDE (-4)   /* row_stride < columns of that tensor */
+#define LPD_ERR_BAD_CLIP (-5)     /* clip bounds not 0 < lo <= hi (finite) */
+#define LPD_ERR_BAD_SHARDS (-6)   /* shard ranges do not tile [0, vocab) exactly */
+#define LPD_ERR_WORKSPACE (-7)    /* workspace NULL or smaller than lpd_workspace_size() */
+#define LPD_ERR_CUDA (-8)         /* a CUDA runtime call failed (launch, attribute) */
+#define LPD_ERR_ALIGNMENT (-9)    /* a pointer or stride breaks a stated alignment rule */
+#define LPD_ERR_UNSUPPORTED (-10) /* a size outside what this build supports */
+
+/* ---- device-reported status bits (lpd_metrics.status) ------------------ */
+#define LPD_STATUS_TOKEN_OOB 1u /* an active row's token id is outside [0, vocab) */
+#define LPD_STATUS_NONFINITE 2u /* non-finite log-sum-exp or selected logit on an active row */
+#define LPD_STATUS_TIMEOUT 4u   /* an internal pipeline wait gave up (never expected) */
+
+/* ---- result flags (lpd_metrics.flags) --------------------------------- */
+#define LPD_FLAG_NO_ACTIVE 1u /* zero active tokens: every metric is 0 */
+
+/* ---- workspace kinds --------------------------------------------------- */
+#define LPD_KIND_SCORE 0   /* lpd_score and its stages */
+#define LPD_KIND_SHARDED 1 /* lpd_score_sharded */
+
+/* One side's logits: [n_rows, row_stride] row-major, columns [0, vocab) used. */
+typedef struct {
+    const void *ptr;    /* device pointer to row 0, column 0 */
+    int32_t dtype;      /* LPD_BF16 or LPD_F32 */
+    int32_t reserved;   /* set to 0 */
+    int64_t row_stride; /* elements between consecutive rows, >= vocab */
+} lpd_logits;
+
+/* One vocab shard of one side: [n_rows, row_stride] holding global columns
+ * [v_start, v_end) as local columns [0, v_end - v_start), as a tensor-parallel
+ * vocab split would produce ("[WS2] Framework for ablation experiment",
+ * LogProb knobs table, row 3: per-rank (vocab_start, vocab_end)). */
+typedef struct {
+    const void *ptr;
+    int32_t dtype;
+    int32_t reserved;
+    int64_t row_stride; /* >= v_end - v_start */
+    int64_t v_start;
+    int64_t v_end;
+} lpd_shard;
+
+/* Drift diagnostics over active tokens (device-resident, written by the
+ * library).  Field meaning: "WS2 Cross-Config Logprob Drift Contract",
+ * section "Diagnostics"; n_active and argmax_row are the active-token count
+ * and worst-token metadata of roadmap item B1 (argmax_row is the lowest row
+ * index among ties of max |dlogp|, -1 when there is no active token). */
+typedef struct {
+    int64_t n_active;
+    int64_t argmax_row;
+    uint32_t flags;  /* LPD_FLAG_* */
+    uint32_t status; /* LPD_STATUS_* bits, 0 when every active row was valid */
+    double ratio0_mean;
+    double clipfrac0;
+    double approx_kl0;
+    double mean_abs_dlogp;
+    double p95_abs_dlogp;
+    double p99_abs_dlogp;
+    double max_abs_dlogp;
+} lpd_metrics;
+
+/* Kernel backend descriptor ("WS2 Cross-Config Logprob Drift Contract",
+ * section "Kernel Integration Contract": stable id, semantic operator name,
+ * architectures, dtypes, determinism properties, build-time flags, fallback
+ * behaviour, build fingerprint; section "Mapping to Current Code": the
+ * fast-math and architecture build knobs). */
+typedef struct {
+    char backend_id[32];   /* "lpd.sm103a.v1" */
+    char op_name[48];      /* "selected_logprob_drift" */
+    char arch[16];         /* "sm_103a" */
+    char dtypes[32];       /* "bf16,f32" (per side, may differ) */
+    int32_t deterministic; /* 1: bitwise repeatable run to run */
+    int32_t batch_invariant; /* 1: a row's result is independent of its batch */
+    int32_t fast_math;     /* 0: built without --use_fast_math */
+    int32_t has_fallback;  /* 0: no CPU or library fallback exists */
+    char fingerprint[96];  /* compiler version and build date */
+} lpd_backend_info_t;
+
+/* ---- sizing and introspection ----------------------------------------- */
+
+/* Bytes of device workspace that a call of the given kind needs for n_rows
+ * rows (vocab and n_shards are used by the sharded kind; pass 0
+ * otherwise).  Returns 0 for invalid arguments. */
+size_t lpd_workspace_size(int32_t kind, int64_t n_rows, int64_t vocab, int32_t n_shards);
+
+/* Fills *info.  Returns LPD_OK, or LPD_ERR_NULL_POINTER. */
+int lpd_backend_info(lpd_backend_info_t *info);
+
+/* Static English text for a return code or a single status bit. */
+const char *lpd_strerror(int code);
+
+/* ---- the scoring path --------------------------------------------------- */
+
+/* Whole path ("Measurement Contract" and "Diagnostics" sections): select
+ * active rows, score both sides, then the metrics.  Equivalent to
+ * lpd_select_active + lpd_token_logp + lpd_drift_metrics on one stream.
+ *
+ * train, rollout   host structs describing device logits [n_rows, vocab];
+ *                  dtypes may differ between the sides.
+ * token_ids        device int32[n_rows].
+ * action_mask      device uint8[n_rows].
+ * clip_lo, clip_hi ratio0 bounds; a ratio equal to a bound is inside.
+ * out_logp_train, out_logp_rollout, out_dlogp
+ *                  device float32[n_rows] each, or NULL to skip; inactive rows
+ *                  receive 0.
+ * out_metrics      device lpd_metrics (required).
+ * workspace        device buffer of at least
+ *                  lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0) bytes,
+ *                  256-byte aligned.
+ * stream           cudaStream_t or NULL.
+ * n_rows may be 0 (then out_metrics reports zero active tokens). */
+int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows,
+              int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask,
+              double clip_lo, double clip_hi, float *out_logp_train,
+              float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Stage 1 of lpd_score ("Measurement Contract": prompt, padding and masked
+ * positions are excluded): the order-preserving list of active rows with
+ * their token ids, and their count, into the workspace; zeroes the per-token
+ * outputs of inactive rows and clears out_metrics->status.  The three stages
+ * must run in order on one stream with the same workspace, n_rows and output
+ * pointers. */
+int lpd_select_active(int64_t n_rows, const int32_t *token_ids, const uint8_t *action_mask,
+                      float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
+                      lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Stage 2 of lpd_score: the streaming row pass over the rows stage 1 listed.
+ * For each active row, both sides' log-sum-exp in one read of each logits row,
+ * the selected-logit gather, and the per-token logp_train, logp_rollout and
+ * dlogp (plus the per-row values stage 3 reduces). */
+int lpd_token_logp(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows,
+                   int64_t vocab, float *out_logp_train, float *out_logp_rollout,
+                   float *out_dlogp, lpd_metrics *out_metrics, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* Stage 3 of lpd_score ("Diagnostics"): metrics over the active rows scored
+ * by stage 2, into out_metrics (everything but status, which stages 1-2
+ * own). */
+int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi,
+                      lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Vocab-sharded scoring ("[WS2] Framework for ablation experiment", LogProb
+ * knobs table, rows 3-5 and 8).  Each side's vocabulary arrives as n_shards
+ * tensors whose [v_start, v_end) ranges must tile [0, vocab) exactly, in any
+ * array order (else LPD_ERR_BAD_SHARDS, "fail closed on missing vocab-shard
+ * bounds").  Each shard gives its own partial (max, sum exp); the partials are
+ * merged in global vocab-shard order (ascending v_start), and the selected
+ * logit comes from the single shard that owns the id.  All shards of a side
+ * share one dtype.  1 <= n_shards <= 16.
+ *
+ * merge_perm       optional HOST int32[n_shards]: a permutation of the shard
+ *                  positions in vocab order.  When given, each row is merged a
+ *                  second time in that order and the resulting logp is written
+ *                  to out_perm_logp_train / out_perm_logp_rollout (device
+ *                  float32[n_rows] each, may be NULL) as a merge-order drift
+ *                  diagnostic (row 5: merge order as a drift source).
+ * The fixed-order result is what out_logp_* / out_dlogp / out_metrics carry.
+ * workspace        lpd_workspace_size(LPD_KIND_SHARDED, n_rows, vocab, n_shards). */
+int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards,
+                      int64_t n_rows, int64_t vocab, const int32_t *token_ids,
+                      const uint8_t *action_mask, double clip_lo, double clip_hi,
+                      const int32_t *merge_perm, float *out_logp_train,
+                      float *out_logp_rollout, float *out_dlogp,
+                      float *out_perm_logp_train, float *out_perm_logp_rollout,
+                      lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LPD_H */

@@ -1,0 +1,248 @@
+"""Thin Python binding of liblpd (include/lpd.h): same names, marshalling only.
+
+Every function here converts torch tensors to the C structs and pointers of
+the C ABI and calls the library; all arithmetic runs in the CUDA kernels.
+There is no CPU or library fallback: if liblpd.so cannot be loaded (or
+built), importing the binding fails.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+from . import _build
+
+# ---- constants (mirror include/lpd.h) --------------------------------------
+LPD_BF16, LPD_F32 = 0, 1
+LPD_OK = 0
+LPD_ERR_NULL_POINTER = -1
+LPD_ERR_BAD_SIZE = -2
+LPD_ERR_BAD_DTYPE = -3
+LPD_ERR_BAD_STRIDE = -4
+LPD_ERR_BAD_CLIP = -5
+LPD_ERR_BAD_SHARDS = -6
+LPD_ERR_WORKSPACE = -7
+LPD_ERR_CUDA = -8
+LPD_ERR_ALIGNMENT = -9
+LPD_ERR_UNSUPPORTED = -10
+LPD_STATUS_TOKEN_OOB = 1
+LPD_STATUS_NONFINITE = 2
+LPD_STATUS_TIMEOUT = 4
+LPD_FLAG_NO_ACTIVE = 1
+LPD_KIND_SCORE, LPD_KIND_SHARDED = 0, 1
+
+
+class LpdLogits(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("row_stride", ctypes.c_int64)]
+
+
+class LpdShard(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("row_stride", ctypes.c_int64), ("v_start", ctypes.c_int64), ("v_end", ctypes.c_int64)]
+
+
+class LpdMetrics(ctypes.Structure):
+    _fields_ = [("n_active", ctypes.c_int64), ("argmax_row", ctypes.c_int64), ("flags", ctypes.c_uint32),
+                ("status", ctypes.c_uint32), ("ratio0_mean", ctypes.c_double), ("clipfrac0", ctypes.c_double),
+                ("approx_kl0", ctypes.c_double), ("mean_abs_dlogp", ctypes.c_double),
+                ("p95_abs_dlogp", ctypes.c_double), ("p99_abs_dlogp", ctypes.c_double),
+                ("max_abs_dlogp", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class LpdBackendInfo(ctypes.Structure):
+    _fields_ = [("backend_id", ctypes.c_char * 32), ("op_name", ctypes.c_char * 48), ("arch", ctypes.c_char * 16),
+                ("dtypes", ctypes.c_char * 32), ("deterministic", ctypes.c_int32),
+                ("batch_invariant", ctypes.c_int32), ("fast_math", ctypes.c_int32),
+                ("has_fallback", ctypes.c_int32), ("fingerprint", ctypes.c_char * 96)]
+
+
+METRICS_BYTES = ctypes.sizeof(LpdMetrics)
+
+# every symbol include/lpd.h declares
+EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
+            "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded")
+
+
+class LpdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {lib().lpd_strerror(code).decode()} (code {code})")
+
+
+_LIB: ctypes.CDLL | None = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded liblpd.so (built in-tree on first use if nvcc is present)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(str(path))
+        P, I32, I64, SZ, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_double
+        L.lpd_workspace_size.restype = SZ
+        L.lpd_workspace_size.argtypes = [I32, I64, I64, I32]
+        L.lpd_backend_info.restype = ctypes.c_int
+        L.lpd_backend_info.argtypes = [P]
+        L.lpd_strerror.restype = ctypes.c_char_p
+        L.lpd_strerror.argtypes = [ctypes.c_int]
+        L.lpd_score.restype = ctypes.c_int
+        L.lpd_score.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
+        L.lpd_select_active.restype = ctypes.c_int
+        L.lpd_select_active.argtypes = [I64, P, P, P, P, P, P, P, SZ, P]
+        L.lpd_token_logp.restype = ctypes.c_int
+        L.lpd_token_logp.argtypes = [P, P, I64, I64, P, P, P, P, P, SZ, P]
+        L.lpd_drift_metrics.restype = ctypes.c_int
+        L.lpd_drift_metrics.argtypes = [I64, D, D, P, P, SZ, P]
+        L.lpd_score_sharded.restype = ctypes.c_int
+        L.lpd_score_sharded.argtypes = [P, P, I32, I64, I64, P, P, D, D, P, P, P, P, P, P, P, P, SZ, P]
+        _LIB = L
+    return _LIB
+
+
+# ---- marshalling helpers ----------------------------------------------------
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return LPD_BF16
+    if t.dtype == torch.float32:
+        return LPD_F32
+    return 99  # rejected by the library with LPD_ERR_BAD_DTYPE
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def logits_struct(t) -> LpdLogits:
+    """lpd_logits for a 2-D tensor with unit column stride (rows may be padded)."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("logits must be 2-D with contiguous columns")
+    return LpdLogits(t.data_ptr(), _dtype_code(t), 0, t.stride(0))
+
+
+def shard_array(shards, v_ranges):
+    arr = (LpdShard * len(shards))()
+    for i, (t, (v0, v1)) in enumerate(zip(shards, v_ranges)):
+        if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError("shard logits must be 2-D with contiguous columns")
+        arr[i] = LpdShard(t.data_ptr(), _dtype_code(t), 0, t.stride(0), int(v0), int(v1))
+    return arr
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != LPD_OK:
+        raise LpdError(rc, where)
+
+
+# ---- the C ABI, one Python function per entry point ---------------------------
+
+def lpd_workspace_size(kind: int, n_rows: int, vocab: int = 0, n_shards: int = 0) -> int:
+    return int(lib().lpd_workspace_size(kind, n_rows, vocab, n_shards))
+
+
+def lpd_backend_info() -> dict:
+    info = LpdBackendInfo()
+    _check(lib().lpd_backend_info(ctypes.byref(info)), "lpd_backend_info")
+    out = {}
+    for name, _ in info._fields_:
+        v = getattr(info, name)
+        out[name] = v.decode() if isinstance(v, bytes) else v
+    return out
+
+
+def lpd_strerror(code: int) -> str:
+    return lib().lpd_strerror(code).decode()
+
+
+def lpd_score(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
+              out_dlogp, out_metrics, workspace, stream=None) -> None:
+    t, r = logits_struct(train), logits_struct(rollout)
+    rc = lib().lpd_score(ctypes.byref(t), ctypes.byref(r), train.shape[0], train.shape[1], _ptr(token_ids),
+                         _ptr(action_mask), float(clip_lo), float(clip_hi), _ptr(out_logp_train),
+                         _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics), _ptr(workspace),
+                         workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(rc, "lpd_score")
+
+
+def lpd_select_active(token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace,
+                      stream=None) -> None:
+    n = action_mask.shape[0]
+    rc = lib().lpd_select_active(n, _ptr(token_ids), _ptr(action_mask), _ptr(out_logp_train), _ptr(out_logp_rollout),
+                                 _ptr(out_dlogp), _ptr(out_metrics), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(rc, "lpd_select_active")
+
+
+def lpd_token_logp(train, rollout, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace,
+                   stream=None) -> None:
+    t, r = logits_struct(train), logits_struct(rollout)
+    rc = lib().lpd_token_logp(ctypes.byref(t), ctypes.byref(r), train.shape[0], train.shape[1],
+                              _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics),
+                              _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "lpd_token_logp")
+
+
+def lpd_drift_metrics(n_rows, clip_lo, clip_hi, out_metrics, workspace, stream=None) -> None:
+    rc = lib().lpd_drift_metrics(n_rows, float(clip_lo), float(clip_hi), _ptr(out_metrics), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "lpd_drift_metrics")
+
+
+def lpd_score_sharded(train_shards, rollout_shards, v_ranges, token_ids, action_mask, clip_lo, clip_hi,
+                      merge_perm, out_logp_train, out_logp_rollout, out_dlogp, out_perm_logp_train,
+                      out_perm_logp_rollout, out_metrics, workspace, stream=None) -> None:
+    ts, rs = shard_array(train_shards, v_ranges), shard_array(rollout_shards, v_ranges)
+    n_rows = train_shards[0].shape[0]
+    vocab = max(v1 for _, v1 in v_ranges)
+    perm = None
+    if merge_perm is not None:
+        perm = (ctypes.c_int32 * len(merge_perm))(*[int(k) for k in merge_perm])
+    rc = lib().lpd_score_sharded(ts, rs, len(train_shards), n_rows, vocab, _ptr(token_ids), _ptr(action_mask),
+                                 float(clip_lo), float(clip_hi), perm, _ptr(out_logp_train), _ptr(out_logp_rollout),
+                                 _ptr(out_dlogp), _ptr(out_perm_logp_train), _ptr(out_perm_logp_rollout),
+                                 _ptr(out_metrics), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "lpd_score_sharded")
+
+
+# ---- convenience: allocate with torch, call, read back ------------------------
+
+def read_metrics(buf) -> dict:
+    """Copy a device lpd_metrics record (uint8 tensor) to the host as a dict."""
+    host = buf.detach().to("cpu", copy=True).numpy().tobytes()
+    return LpdMetrics.from_buffer_copy(host).as_dict()
+
+
+@dataclass
+class ScoreResult:
+    logp_train: object
+    logp_rollout: object
+    dlogp: object
+    metrics: dict
+
+
+def score(train, rollout, token_ids, action_mask, clip=(0.8, 1.2), stream=None) -> ScoreResult:
+    """Allocate outputs and workspace with torch on the logits' device, run
+    lpd_score, and return per-token tensors plus the metrics as a dict."""
+    import torch
+
+    dev = train.device
+    n = train.shape[0]
+    outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
+    ws = torch.empty(lpd_workspace_size(LPD_KIND_SCORE, n), dtype=torch.uint8, device=dev)
+    lpd_score(train, rollout, token_ids, action_mask, clip[0], clip[1], *outs, met, ws, stream=stream)
+    return ScoreResult(outs[0], outs[1], outs[2], read_metrics(met))

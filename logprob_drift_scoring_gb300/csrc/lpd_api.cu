@@ -1,0 +1,369 @@
+// C ABI of liblpd: host-side validation, workspace carving and the stage
+// sequence.  Every argument problem is caught here, before any launch, and
+// returned as a negative LPD_ERR_* code (include/lpd.h).  Nothing is allocated:
+// the caller passes every buffer, including the workspace.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "lpd_internal.cuh"
+
+namespace lpd {
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+namespace {
+
+constexpr int64_t kMaxRows = INT32_MAX;   // rows are addressed as int32 in the row list
+constexpr int64_t kMaxVocab = INT32_MAX;  // token ids are int32
+
+int elt_bytes(int32_t dtype) { return dtype == LPD_BF16 ? 2 : 4; }
+bool valid_dtype(int32_t dtype) { return dtype == LPD_BF16 || dtype == LPD_F32; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_clip(double lo, double hi) {
+    if (!std::isfinite(lo) || !std::isfinite(hi) || !(lo > 0.0) || !(lo <= hi)) return LPD_ERR_BAD_CLIP;
+    return LPD_OK;
+}
+
+int check_rows_vocab(int64_t n_rows, int64_t vocab) {
+    if (n_rows < 0 || vocab <= 0) return LPD_ERR_BAD_SIZE;
+    if (n_rows > kMaxRows || vocab > kMaxVocab) return LPD_ERR_UNSUPPORTED;
+    return LPD_OK;
+}
+
+// Elements must sit on their natural boundary (2 bytes for bf16, 4 for fp32).
+bool elt_aligned(const void *p, int32_t dtype) {
+    return (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(elt_bytes(dtype))) == 0;
+}
+
+int check_logits(const lpd_logits *x, int64_t n_rows, int64_t vocab) {
+    if (!x) return LPD_ERR_NULL_POINTER;
+    if (!x->ptr && n_rows > 0) return LPD_ERR_NULL_POINTER;
+    if (!valid_dtype(x->dtype)) return LPD_ERR_BAD_DTYPE;
+    if (x->row_stride < vocab) return LPD_ERR_BAD_STRIDE;
+    if (!elt_aligned(x->ptr, x->dtype)) return LPD_ERR_ALIGNMENT;
+    return LPD_OK;
+}
+
+int check_workspace(void *ws, size_t bytes, size_t need) {
+    if (!ws) return LPD_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LPD_ERR_ALIGNMENT;
+    if (bytes < need) return LPD_ERR_WORKSPACE;
+    return LPD_OK;
+}
+
+struct Ws {
+    WsHeader *hdr;
+    int2 *rowid;
+    float2 *pick;
+    float4 *part;
+    double *dval;
+    uint32_t *keys;
+    BlockPartial *blockpart;
+};
+
+Ws carve(void *base, int64_t n_rows, int n_seg) {
+    const WsLayout L = ws_layout(n_rows, n_seg);
+    char *b = static_cast<char *>(base);
+    return Ws{reinterpret_cast<WsHeader *>(b + L.header),  reinterpret_cast<int2 *>(b + L.rowid),
+              reinterpret_cast<float2 *>(b + L.pick),      reinterpret_cast<float4 *>(b + L.part),
+              reinterpret_cast<double *>(b + L.dval),      reinterpret_cast<uint32_t *>(b + L.keys),
+              reinterpret_cast<BlockPartial *>(b + L.blockpart)};
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LPD_OK : LPD_ERR_CUDA; }
+
+// A row of a side can stream through the bulk-copy ring when every row
+// starts on a 16-byte boundary.
+bool rows_aligned(const void *ptr, int64_t stride, int32_t dtype) {
+    return aligned16(ptr) && ((stride * elt_bytes(dtype)) % 16) == 0;
+}
+
+int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *lt, float *lr, float *d,
+               lpd_metrics *met, const Ws &w, cudaStream_t s) {
+    return cuda_status(launch_select_active(n_rows, mask, ids, lt, lr, d, met, w.hdr, w.rowid, s));
+}
+
+// Stage 2: the streaming row pass, then the per-row finalise.
+int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, const int32_t *perm, int n_perm,
+             int64_t n_rows, int64_t vocab, float *lt, float *lr, float *d, float *plt, float *plr,
+             lpd_metrics *met, const Ws &w, cudaStream_t s) {
+    if (n_rows == 0) return LPD_OK;
+    RowArgs a{};
+    for (int k = 0; k < n_seg; ++k) a.seg[k] = segs[k];
+    a.n_seg = n_seg;
+    a.vocab = vocab;
+    a.hdr = w.hdr;
+    a.rowid = w.rowid;
+    a.part = w.part;
+    a.pick = w.pick;
+    a.status = &met->status;
+    int rc = cuda_status(launch_rows(a, dt, dr, tma, s));
+    if (rc) return rc;
+    FinArgs f{};
+    f.n_seg = n_seg;
+    f.n_perm = n_perm;
+    for (int j = 0; j < n_perm; ++j) f.perm[j] = static_cast<int8_t>(perm[j]);
+    f.vocab = vocab;
+    f.hdr = w.hdr;
+    f.rowid = w.rowid;
+    f.part = w.part;
+    f.pick = w.pick;
+    f.dval = w.dval;
+    f.keys = w.keys;
+    f.out_lt = lt;
+    f.out_lr = lr;
+    f.out_d = d;
+    f.out_perm_lt = plt;
+    f.out_perm_lr = plr;
+    f.status = &met->status;
+    return cuda_status(launch_finalize(f, n_rows, s));
+}
+
+// Stage 3: metric terms per block, then the merge and the percentile select.
+int run_metrics(int64_t n_rows, double clip_lo, double clip_hi, lpd_metrics *met, const Ws &w, cudaStream_t s) {
+    return cuda_status(launch_metrics(n_rows, std::log(clip_lo), std::log(clip_hi), w.hdr, w.rowid, w.dval, w.keys,
+                                      w.blockpart, met, s));
+}
+
+int validate_pair(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab) {
+    int rc = check_rows_vocab(n_rows, vocab);
+    if (rc) return rc;
+    if ((rc = check_logits(train, n_rows, vocab))) return rc;
+    if ((rc = check_logits(rollout, n_rows, vocab))) return rc;
+    return LPD_OK;
+}
+
+Segment whole_vocab(const lpd_logits *t, const lpd_logits *r, int64_t vocab) {
+    Segment sg{};
+    sg.t = static_cast<const char *>(t->ptr);
+    sg.r = static_cast<const char *>(r->ptr);
+    sg.t_stride = t->row_stride * elt_bytes(t->dtype);
+    sg.r_stride = r->row_stride * elt_bytes(r->dtype);
+    sg.v_start = 0;
+    sg.len = vocab;
+    return sg;
+}
+
+// Exact tiling of [0, vocab) by the shard ranges, in any array order ("fail
+// closed on missing vocab-shard bounds"); on success `order` lists the shard
+// indices by ascending v_start (the global vocab-shard order).
+int check_shards(const lpd_shard *sh, int n, int64_t n_rows, int64_t vocab, int *order) {
+    if (!sh) return LPD_ERR_NULL_POINTER;
+    for (int k = 0; k < n; ++k) {
+        if (!sh[k].ptr && n_rows > 0) return LPD_ERR_NULL_POINTER;
+        if (!valid_dtype(sh[k].dtype)) return LPD_ERR_BAD_DTYPE;
+        if (sh[k].dtype != sh[0].dtype) return LPD_ERR_BAD_DTYPE;
+        if (sh[k].v_start < 0 || sh[k].v_end <= sh[k].v_start || sh[k].v_end > vocab) return LPD_ERR_BAD_SHARDS;
+        if (sh[k].row_stride < sh[k].v_end - sh[k].v_start) return LPD_ERR_BAD_STRIDE;
+        if (!elt_aligned(sh[k].ptr, sh[k].dtype)) return LPD_ERR_ALIGNMENT;
+        order[k] = k;
+    }
+    std::sort(order, order + n, [&](int x, int y) { return sh[x].v_start < sh[y].v_start; });
+    int64_t next = 0;
+    for (int j = 0; j < n; ++j) {
+        if (sh[order[j]].v_start != next) return LPD_ERR_BAD_SHARDS;
+        next = sh[order[j]].v_end;
+    }
+    return next == vocab ? LPD_OK : LPD_ERR_BAD_SHARDS;
+}
+
+}  // namespace
+}  // namespace lpd
+
+using namespace lpd;
+
+extern "C" {
+
+size_t lpd_workspace_size(int32_t kind, int64_t n_rows, int64_t vocab, int32_t n_shards) {
+    if (n_rows < 0 || n_rows > kMaxRows) return 0;
+    switch (kind) {
+        case LPD_KIND_SCORE:
+            return ws_layout(n_rows, 1).total;
+        case LPD_KIND_SHARDED:
+            if (n_shards < 1 || n_shards > kMaxSegments) return 0;
+            return ws_layout(n_rows, n_shards).total;
+        default:
+            (void)vocab;
+            return 0;
+    }
+}
+
+int lpd_backend_info(lpd_backend_info_t *info) {
+    if (!info) return LPD_ERR_NULL_POINTER;
+    std::memset(info, 0, sizeof(*info));
+    std::snprintf(info->backend_id, sizeof info->backend_id, "lpd.sm103a.v1");
+    std::snprintf(info->op_name, sizeof info->op_name, "selected_logprob_drift");
+    std::snprintf(info->arch, sizeof info->arch, "sm_103a");
+    std::snprintf(info->dtypes, sizeof info->dtypes, "bf16,f32");
+    info->deterministic = 1;
+    info->batch_invariant = 1;
+#ifdef __USE_FAST_MATH__
+    info->fast_math = 1;
+#else
+    info->fast_math = 0;
+#endif
+    info->has_fallback = 0;
+    std::snprintf(info->fingerprint, sizeof info->fingerprint, "nvcc %d.%d sm_103a %s %s", __CUDACC_VER_MAJOR__,
+                  __CUDACC_VER_MINOR__, __DATE__, __TIME__);
+    return LPD_OK;
+}
+
+const char *lpd_strerror(int code) {
+    switch (code) {
+        case LPD_OK: return "success";
+        case LPD_ERR_NULL_POINTER: return "a required pointer is NULL";
+        case LPD_ERR_BAD_SIZE: return "invalid size (n_rows < 0, vocab <= 0, hidden <= 0 or similar)";
+        case LPD_ERR_BAD_DTYPE: return "unsupported or mixed element type";
+        case LPD_ERR_BAD_STRIDE: return "row stride smaller than the number of columns";
+        case LPD_ERR_BAD_CLIP: return "clip bounds must be finite with 0 < lo <= hi";
+        case LPD_ERR_BAD_SHARDS: return "vocab shards do not tile [0, vocab) exactly";
+        case LPD_ERR_WORKSPACE: return "workspace missing or smaller than lpd_workspace_size()";
+        case LPD_ERR_CUDA: return "a CUDA runtime call failed";
+        case LPD_ERR_ALIGNMENT: return "a pointer or stride breaks an alignment rule";
+        case LPD_ERR_UNSUPPORTED: return "size outside what this build supports";
+        case static_cast<int>(LPD_STATUS_TOKEN_OOB): return "status: active token id outside [0, vocab)";
+        case static_cast<int>(LPD_STATUS_NONFINITE): return "status: non-finite log-sum-exp or selected logit";
+        case static_cast<int>(LPD_STATUS_TIMEOUT): return "status: an internal pipeline wait gave up";
+        default: return "unknown code";
+    }
+}
+
+int lpd_select_active(int64_t n_rows, const int32_t *token_ids, const uint8_t *action_mask, float *out_logp_train,
+                      float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (n_rows < 0) return LPD_ERR_BAD_SIZE;
+    if (n_rows > kMaxRows) return LPD_ERR_UNSUPPORTED;
+    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    int rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0));
+    if (rc) return rc;
+    const Ws w = carve(workspace, n_rows, 1);
+    return run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, w,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lpd_token_logp(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab,
+                   float *out_logp_train, float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = validate_pair(train, rollout, n_rows, vocab);
+    if (rc) return rc;
+    if (!out_metrics) return LPD_ERR_NULL_POINTER;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const Ws w = carve(workspace, n_rows, 1);
+    const Segment sg = whole_vocab(train, rollout, vocab);
+    const bool tma = rows_aligned(train->ptr, train->row_stride, train->dtype) &&
+                     rows_aligned(rollout->ptr, rollout->row_stride, rollout->dtype);
+    return run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
+                    out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, static_cast<cudaStream_t>(stream));
+}
+
+int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi, lpd_metrics *out_metrics, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (n_rows < 0) return LPD_ERR_BAD_SIZE;
+    if (n_rows > kMaxRows) return LPD_ERR_UNSUPPORTED;
+    if (!out_metrics) return LPD_ERR_NULL_POINTER;
+    int rc = check_clip(clip_lo, clip_hi);
+    if (rc) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const Ws w = carve(workspace, n_rows, 1);
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, static_cast<cudaStream_t>(stream));
+}
+
+int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab,
+              const int32_t *token_ids, const uint8_t *action_mask, double clip_lo, double clip_hi,
+              float *out_logp_train, float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
+              void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = validate_pair(train, rollout, n_rows, vocab);
+    if (rc) return rc;
+    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Ws w = carve(workspace, n_rows, 1);
+    const Segment sg = whole_vocab(train, rollout, vocab);
+    const bool tma = rows_aligned(train->ptr, train->row_stride, train->dtype) &&
+                     rows_aligned(rollout->ptr, rollout->row_stride, rollout->dtype);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    if ((rc = run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
+                       out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s)))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards, int64_t n_rows,
+                      int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask, double clip_lo,
+                      double clip_hi, const int32_t *merge_perm, float *out_logp_train, float *out_logp_rollout,
+                      float *out_dlogp, float *out_perm_logp_train, float *out_perm_logp_rollout,
+                      lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_rows_vocab(n_rows, vocab);
+    if (rc) return rc;
+    if (n_shards < 1 || n_shards > kMaxSegments) return LPD_ERR_UNSUPPORTED;
+    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    int ot[kMaxSegments], orr[kMaxSegments];
+    if ((rc = check_shards(train, n_shards, n_rows, vocab, ot))) return rc;
+    if ((rc = check_shards(rollout, n_shards, n_rows, vocab, orr))) return rc;
+    // both sides must use the same split: shard j (in vocab order) covers the
+    // same range on each side
+    for (int j = 0; j < n_shards; ++j)
+        if (train[ot[j]].v_start != rollout[orr[j]].v_start || train[ot[j]].v_end != rollout[orr[j]].v_end)
+            return LPD_ERR_BAD_SHARDS;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if (merge_perm) {
+        bool seen[kMaxSegments] = {false};
+        for (int j = 0; j < n_shards; ++j) {
+            const int k = merge_perm[j];
+            if (k < 0 || k >= n_shards || seen[k]) return LPD_ERR_BAD_SHARDS;
+            seen[k] = true;
+        }
+    }
+    if ((rc = check_workspace(workspace, workspace_bytes,
+                              lpd_workspace_size(LPD_KIND_SHARDED, n_rows, vocab, n_shards))))
+        return rc;
+    Segment segs[kMaxSegments];
+    bool tma = true;
+    for (int j = 0; j < n_shards; ++j) {
+        const lpd_shard &a = train[ot[j]], &b = rollout[orr[j]];
+        segs[j].t = static_cast<const char *>(a.ptr);
+        segs[j].r = static_cast<const char *>(b.ptr);
+        segs[j].t_stride = a.row_stride * elt_bytes(a.dtype);
+        segs[j].r_stride = b.row_stride * elt_bytes(b.dtype);
+        segs[j].v_start = a.v_start;
+        segs[j].len = a.v_end - a.v_start;
+        tma = tma && rows_aligned(a.ptr, a.row_stride, a.dtype) && rows_aligned(b.ptr, b.row_stride, b.dtype);
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Ws w = carve(workspace, n_rows, n_shards);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    if (merge_perm && (out_perm_logp_train || out_perm_logp_rollout)) {
+        // zero the diagnostic outputs of inactive rows as stage 1 does for the others
+        if (out_perm_logp_train && (rc = cuda_status(cudaMemsetAsync(out_perm_logp_train, 0, n_rows * sizeof(float), s))))
+            return rc;
+        if (out_perm_logp_rollout && (rc = cuda_status(cudaMemsetAsync(out_perm_logp_rollout, 0, n_rows * sizeof(float), s))))
+            return rc;
+    }
+    if ((rc = run_rows(segs, n_shards, train[0].dtype, rollout[0].dtype, tma, merge_perm, merge_perm ? n_shards : 0,
+                       n_rows, vocab, out_logp_train, out_logp_rollout, out_dlogp, out_perm_logp_train,
+                       out_perm_logp_rollout, out_metrics, w, s)))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// Internal definitions shared by the kernels and the C-ABI layer of liblpd.
+// Nothing here is part of the public interface (include/lpd.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lpd.h"
+
+namespace lpd {
+
+// ---------------------------------------------------------------- geometry
+// The streaming row kernel runs one CTA per SM: 16 consumer warps plus one
+// producer warp.  A tile is 4096 logical columns of one vocab segment; consumer
+// thread t owns columns [4t, 4t+4) and [2048+4t, 2048+4t+4) of every tile.
+// These constants fix each row's arithmetic order, so they are part of the
+// batch-invariance contract: changing them changes results (bitwise), but never
+// makes them depend on the batch.
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;  // 512
+constexpr int kRowThreads = kConsumers + 32;     // + producer warp
+constexpr int kTile = 8 * kConsumers;            // 4096 columns
+constexpr int kHalfTile = kTile / 2;
+constexpr int kMaxSegments = 16;                 // shards per side
+constexpr int kRingBytes = 192 * 1024;           // shared-memory staging ring
+constexpr int kFinThreads = 256;                 // rows per finalise block
+constexpr int kSelThreads = 1024;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- workspace
+// Device workspace carved into fixed regions; every region 256-byte aligned.
+struct WsHeader {
+    int64_t n_active;
+    int64_t reserved[31];
+};
+
+struct BlockPartial {  // one finalise block's share of the metrics
+    double sum_abs;
+    double sum_k3;
+    double sum_em1;
+    double max_abs;
+    int64_t argmax_row;
+    int64_t n_clip;
+};
+
+struct WsLayout {
+    size_t header, rowid, pick, part, dval, keys, blockpart, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t n_rows, int n_seg) {
+    WsLayout L{};
+    size_t off = 0;
+    const size_t R = size_t(n_rows);
+    L.header = off;    off += align256(sizeof(WsHeader));
+    L.rowid = off;     off += align256(R * sizeof(int2));          // (row, token id) of active rows
+    L.pick = off;      off += align256(R * sizeof(float2));        // selected logits (train, rollout)
+    L.part = off;      off += align256(R * size_t(n_seg) * kConsumerWarps * sizeof(float4));
+    L.dval = off;      off += align256(R * sizeof(double));        // dlogp per active row
+    L.keys = off;      off += align256(R * sizeof(uint32_t));      // |dlogp| as fp32 bits
+    L.blockpart = off; off += align256(((R + kFinThreads - 1) / kFinThreads) * sizeof(BlockPartial));
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------- segments
+// One vocab segment (a shard, or the whole vocabulary) of both sides.
+struct Segment {
+    const char *t;      // train base (row 0, local column 0)
+    const char *r;      // rollout base
+    int64_t t_stride;   // bytes between rows
+    int64_t r_stride;
+    int64_t v_start;    // global column of local column 0
+    int64_t len;        // columns in this segment
+};
+
+struct RowArgs {
+    Segment seg[kMaxSegments];
+    int n_seg;
+    int64_t vocab;
+    const WsHeader *hdr;
+    const int2 *rowid;
+    float4 *part;
+    float2 *pick;
+    uint32_t *status;
+};
+
+struct FinArgs {
+    int n_seg;
+    int n_perm;                    // 0: no merge-order diagnostic
+    int8_t perm[kMaxSegments];
+    int64_t vocab;
+    const WsHeader *hdr;
+    const int2 *rowid;
+    const float4 *part;
+    const float2 *pick;
+    double *dval;
+    uint32_t *keys;
+    float *out_lt, *out_lr, *out_d;
+    float *out_perm_lt, *out_perm_lr;
+    uint32_t *status;
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int32_t *ids,
+                                 float *out_lt, float *out_lr, float *out_d,
+                                 lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
+                                 cudaStream_t stream);
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma,
+                        cudaStream_t stream);
+cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
+cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
+                           const int2 *rowid, const double *dval, const uint32_t *keys,
+                           BlockPartial *bp, lpd_metrics *metrics, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace lpd

@@ -1,0 +1,387 @@
+// Active-row selection, per-row finalisation, and the drift metrics.
+//
+// Method: "WS2 Cross-Config Logprob Drift Contract", sections "Measurement
+// Contract" (dlogp = train - rollout on active response/action tokens only)
+// and "Diagnostics" (ratio0, clipfrac0, approx_kl0, mean/p95/p99/max |dlogp|),
+// and roadmap item B1 (zero active tokens, worst-token metadata).
+//
+// Every reduction here has a fixed shape: block partials over fixed row
+// ranges, merged in block order, trees with a fixed pairing.  There are no
+// floating-point atomics, so results are bitwise repeatable.
+#include <cfloat>
+#include <climits>
+
+#include <math_constants.h>
+
+#include "lpd_internal.cuh"
+
+namespace lpd {
+namespace {
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Same merge as the row kernel's butterfly (kept bit-identical on purpose).
+__device__ __forceinline__ void merge_pair(float &m, float &s, float mo, float so) {
+    const float mn = fmaxf(m, mo);
+    s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, mn), kLog2e))),
+                  __fmul_rn(so, ex2(__fmul_rn(__fsub_rn(mo, mn), kLog2e))));
+    m = mn;
+}
+
+// ---------------------------------------------------------------- stage 1
+// One CTA walks the mask in chunks of 16384 rows (16 consecutive rows per
+// thread), block-scans the per-thread counts and writes the (row, token id)
+// pairs of active rows in row order.
+__global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, const uint8_t *mask,
+                                                             const int32_t *ids, float *out_lt,
+                                                             float *out_lr, float *out_d,
+                                                             lpd_metrics *metrics, WsHeader *hdr,
+                                                             int2 *rowid) {
+    __shared__ int warp_excl[32];
+    __shared__ int chunk_total;
+    __shared__ long long base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) base = 0;
+    __syncthreads();
+    for (int64_t chunk = 0; chunk < n_rows; chunk += 1024 * 16) {
+        const int64_t r0 = chunk + static_cast<int64_t>(tid) * 16;
+        uint32_t bits = 0;
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int64_t r = r0 + q;
+            if (r < n_rows) {
+                if (mask[r]) {
+                    bits |= 1u << q;
+                    ++cnt;
+                } else {
+                    if (out_lt) out_lt[r] = 0.f;
+                    if (out_lr) out_lr[r] = 0.f;
+                    if (out_d) out_d[r] = 0.f;
+                }
+            }
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_excl[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = warp_excl[lane];
+            int wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += y;
+            }
+            warp_excl[lane] = wi - w;
+            if (lane == 31) chunk_total = wi;
+        }
+        __syncthreads();
+        int64_t pos = base + warp_excl[warp] + (incl - cnt);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            if (bits >> q & 1u) {
+                const int64_t r = r0 + q;
+                rowid[pos++] = make_int2(static_cast<int>(r), ids[r]);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) base += chunk_total;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        hdr->n_active = base;
+        metrics->status = 0u;
+    }
+}
+
+// ---------------------------------------------------------------- stage 2b
+struct Part {
+    double sum_abs, sum_k3, sum_em1, max_abs;
+    long long argmax_row, n_clip;
+};
+
+__device__ __forceinline__ void combine(Part &x, const Part &y) {
+    x.sum_abs += y.sum_abs;
+    x.sum_k3 += y.sum_k3;
+    x.sum_em1 += y.sum_em1;
+    x.n_clip += y.n_clip;
+    if (y.max_abs > x.max_abs || (y.max_abs == x.max_abs && y.argmax_row < x.argmax_row)) {
+        x.max_abs = y.max_abs;
+        x.argmax_row = y.argmax_row;
+    }
+}
+
+__device__ __forceinline__ Part neutral_part() {
+    Part p;
+    p.sum_abs = p.sum_k3 = p.sum_em1 = 0.0;
+    p.max_abs = -1.0;
+    p.argmax_row = LLONG_MAX;
+    p.n_clip = 0;
+    return p;
+}
+
+// Fixed-pairing tree over a block's Part values held in shared memory.
+template <int kN>
+__device__ __forceinline__ void block_tree(Part *sh) {
+#pragma unroll 1
+    for (int stride = kN / 2; stride > 0; stride >>= 1) {
+        if (threadIdx.x < stride) combine(sh[threadIdx.x], sh[threadIdx.x + stride]);
+        __syncthreads();
+    }
+}
+
+// One thread per active row: merge the 16 warp partials of each segment, then
+// the segments in vocab order (and optionally in a given permutation), then
+// the per-row arithmetic in fp64:
+//   lse = m + log(s),  logp = x[id] - lse,
+//   dlogp = (x_t[id] - x_r[id]) - (m_t - m_r) - log1p((s_t - s_r) / s_r)
+// (the last form keeps dlogp accurate when both sides are nearly equal).
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_constant__ FinArgs a) {
+    const int64_t n_active = a.hdr->n_active;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    if (i >= n_active) return;
+    const int2 rid = a.rowid[i];
+    const int64_t r = rid.x, id = rid.y;
+    uint32_t bad = 0;
+    double d;
+    if (id < 0 || id >= a.vocab) {
+        bad |= LPD_STATUS_TOKEN_OOB;
+        d = CUDART_NAN;
+        if (a.out_lt) a.out_lt[r] = CUDART_NAN_F;
+        if (a.out_lr) a.out_lr[r] = CUDART_NAN_F;
+        if (a.out_perm_lt) a.out_perm_lt[r] = CUDART_NAN_F;
+        if (a.out_perm_lr) a.out_perm_lr[r] = CUDART_NAN_F;
+    } else {
+        const float2 xs = a.pick[i];
+        float smt[kMaxSegments], sst[kMaxSegments], smr[kMaxSegments], ssr[kMaxSegments];
+        float mt = -FLT_MAX, st = 0.f, mr = -FLT_MAX, sr = 0.f;
+        for (int k = 0; k < a.n_seg; ++k) {
+            float kmt = -FLT_MAX, kst = 0.f, kmr = -FLT_MAX, ksr = 0.f;
+            const float4 *pw = a.part + (i * a.n_seg + k) * kConsumerWarps;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float4 q = pw[w];
+                merge_pair(kmt, kst, q.x, q.y);
+                merge_pair(kmr, ksr, q.z, q.w);
+            }
+            smt[k] = kmt;
+            sst[k] = kst;
+            smr[k] = kmr;
+            ssr[k] = ksr;
+            merge_pair(mt, st, kmt, kst);  // global vocab-shard order
+            merge_pair(mr, sr, kmr, ksr);
+        }
+        const double lse_t = static_cast<double>(mt) + log(static_cast<double>(st));
+        const double lse_r = static_cast<double>(mr) + log(static_cast<double>(sr));
+        const double xt = xs.x, xr = xs.y;
+        const double q = (static_cast<double>(st) - static_cast<double>(sr)) / static_cast<double>(sr);
+        d = ((xt - xr) - (static_cast<double>(mt) - static_cast<double>(mr))) - log1p(q);
+        if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
+        if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
+        if (a.out_lr) a.out_lr[r] = static_cast<float>(xr - lse_r);
+        if (a.n_perm) {
+            float pmt = -FLT_MAX, pst = 0.f, pmr = -FLT_MAX, psr = 0.f;
+            for (int j = 0; j < a.n_perm; ++j) {
+                const int k = a.perm[j];
+                merge_pair(pmt, pst, smt[k], sst[k]);
+                merge_pair(pmr, psr, smr[k], ssr[k]);
+            }
+            if (a.out_perm_lt)
+                a.out_perm_lt[r] = static_cast<float>(xt - (static_cast<double>(pmt) + log(static_cast<double>(pst))));
+            if (a.out_perm_lr)
+                a.out_perm_lr[r] = static_cast<float>(xr - (static_cast<double>(pmr) + log(static_cast<double>(psr))));
+        }
+    }
+    if (a.out_d) a.out_d[r] = static_cast<float>(d);
+    a.dval[i] = d;
+    a.keys[i] = __float_as_uint(fabsf(static_cast<float>(d)));
+    if (bad) atomicOr(a.status, bad);
+}
+
+// ---------------------------------------------------------------- stage 3a
+// Per-row metric terms of the Diagnostics table, reduced per block of 256
+// active rows with a fixed tree: sum |d|, sum (exp(d) - 1 - d) evaluated as
+// expm1(d) - d, sum expm1(d) (ratio0 mean = 1 + that / A), the count of
+// ratio0 outside [lo, hi] (as d < ln lo or d > ln hi), and max |d| with the
+// lowest row index among ties.
+__global__ void __launch_bounds__(kFinThreads) terms_kernel(double ln_clip_lo, double ln_clip_hi,
+                                                            const WsHeader *hdr, const int2 *rowid,
+                                                            const double *dval, BlockPartial *bp) {
+    __shared__ Part sh[kFinThreads];
+    const int64_t n_active = hdr->n_active;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    Part p = neutral_part();
+    if (i < n_active) {
+        const double d = dval[i];
+        const double em1 = expm1(d);
+        p.sum_abs = fabs(d);
+        p.sum_em1 = em1;
+        p.sum_k3 = em1 - d;
+        p.max_abs = fabs(d);
+        p.argmax_row = rowid[i].x;
+        p.n_clip = (d < ln_clip_lo || d > ln_clip_hi) ? 1 : 0;
+    }
+    sh[threadIdx.x] = p;
+    __syncthreads();
+    block_tree<kFinThreads>(sh);
+    if (threadIdx.x == 0) {
+        BlockPartial &o = bp[blockIdx.x];
+        o.sum_abs = sh[0].sum_abs;
+        o.sum_k3 = sh[0].sum_k3;
+        o.sum_em1 = sh[0].sum_em1;
+        o.max_abs = sh[0].max_abs;
+        o.argmax_row = sh[0].argmax_row;
+        o.n_clip = sh[0].n_clip;
+    }
+}
+
+// ---------------------------------------------------------------- stage 3b
+// One CTA: merge the finalise blocks' partials (thread tid < 256 folds blocks
+// tid, tid+256, ... in order, then a fixed tree), then nearest-rank p95 and
+// p99 of |dlogp| by a most-significant-digit radix select over the fp32 bit
+// patterns of |dlogp| (monotone for non-negative floats), 8 bits per pass,
+// both ranks in the same passes.  The maximum comes exact from the partials.
+__global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, const WsHeader *hdr,
+                                                              const uint32_t *keys, const BlockPartial *bp,
+                                                              lpd_metrics *out) {
+    constexpr int kFold = 256;  // threads that fold block partials
+    __shared__ Part sh[kFold];
+    __shared__ uint32_t hist[2][256];
+    __shared__ uint32_t prefix[2];
+    __shared__ long long rank[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t n_active = hdr->n_active;
+
+    Part p = neutral_part();
+    for (int64_t b = tid; tid < kFold && b < n_blocks; b += kFold) {
+        Part q;
+        q.sum_abs = bp[b].sum_abs;
+        q.sum_k3 = bp[b].sum_k3;
+        q.sum_em1 = bp[b].sum_em1;
+        q.max_abs = bp[b].max_abs;
+        q.argmax_row = bp[b].argmax_row;
+        q.n_clip = bp[b].n_clip;
+        combine(p, q);
+    }
+    if (tid < kFold) sh[tid] = p;
+    if (tid < 2) {
+        prefix[tid] = 0;
+        const long long pct = tid == 0 ? 95 : 99;
+        rank[tid] = (pct * n_active + 99) / 100;  // ceil(p * A / 100), 1-based
+    }
+    __syncthreads();
+    block_tree<kFold>(sh);
+
+    if (n_active > 0) {
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
+            if (tid < 512) (&hist[0][0])[tid] = 0;
+            __syncthreads();
+            const uint32_t p0 = prefix[0], p1 = prefix[1];
+            for (int64_t i = tid; i < n_active; i += kSelThreads) {
+                const uint32_t key = keys[i];
+                const uint32_t dig = (key >> shift) & 255u;
+                if ((key & hi_mask) == p0) atomicAdd(&hist[0][dig], 1u);
+                if ((key & hi_mask) == p1) atomicAdd(&hist[1][dig], 1u);
+            }
+            __syncthreads();
+            if (warp < 2) {
+                uint32_t c[8];
+                uint32_t tot = 0;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    c[b] = hist[warp][8 * lane + b];
+                    tot += c[b];
+                }
+                uint32_t incl = tot;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                const long long k = rank[warp];
+                const long long before = static_cast<long long>(incl - tot);
+                if (before < k && k <= static_cast<long long>(incl)) {
+                    long long acc = before;
+                    int digit = -1;
+                    long long newk = 0;
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        if (digit < 0 && acc + c[b] >= k) {
+                            digit = 8 * lane + b;
+                            newk = k - acc;
+                        }
+                        acc += c[b];
+                    }
+                    prefix[warp] |= static_cast<uint32_t>(digit) << shift;
+                    rank[warp] = newk;
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    if (tid == 0) {
+        const Part &t = sh[0];
+        out->n_active = n_active;
+        if (n_active > 0) {
+            const double A = static_cast<double>(n_active);
+            out->argmax_row = t.argmax_row;
+            out->flags = 0u;
+            out->ratio0_mean = 1.0 + t.sum_em1 / A;
+            out->clipfrac0 = static_cast<double>(t.n_clip) / A;
+            out->approx_kl0 = t.sum_k3 / A;
+            out->mean_abs_dlogp = t.sum_abs / A;
+            out->p95_abs_dlogp = static_cast<double>(__uint_as_float(prefix[0]));
+            out->p99_abs_dlogp = static_cast<double>(__uint_as_float(prefix[1]));
+            out->max_abs_dlogp = t.max_abs;
+        } else {
+            out->argmax_row = -1;
+            out->flags = LPD_FLAG_NO_ACTIVE;
+            out->ratio0_mean = out->clipfrac0 = out->approx_kl0 = out->mean_abs_dlogp = 0.0;
+            out->p95_abs_dlogp = out->p99_abs_dlogp = out->max_abs_dlogp = 0.0;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int32_t *ids, float *out_lt,
+                                 float *out_lr, float *out_d, lpd_metrics *metrics, WsHeader *hdr,
+                                 int2 *rowid, cudaStream_t stream) {
+    select_active_kernel<<<1, 1024, 0, stream>>>(n_rows, mask, ids, out_lt, out_lr, out_d, metrics, hdr, rowid);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream) {
+    const int64_t blocks = (n_rows + kFinThreads - 1) / kFinThreads;
+    if (blocks == 0) return cudaSuccess;
+    finalize_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
+                           const int2 *rowid, const double *dval, const uint32_t *keys, BlockPartial *bp,
+                           lpd_metrics *metrics, cudaStream_t stream) {
+    const int64_t blocks = (n_rows + kFinThreads - 1) / kFinThreads;
+    if (blocks > 0) {
+        terms_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(ln_clip_lo, ln_clip_hi, hdr,
+                                                                               rowid, dval, bp);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    metrics_kernel<<<1, kSelThreads, 0, stream>>>(blocks, hdr, keys, bp, metrics);
+    return cudaGetLastError();
+}
+
+}  // namespace lpd

@@ -1,0 +1,392 @@
+// Streaming row pass: for every active row, the partial log-sum-exp of each
+// vocab segment of both the training-side and the rollout-side logits, in one
+// read of each row, plus the selected-logit gather.
+//
+// Method: "WS2 Cross-Config Logprob Drift Contract", section "Measurement
+// Contract" (teacher-forced selected-token logp on both sides); "[WS2]
+// Framework for ablation experiment", LogProb knobs table, rows 3-5 and 8
+// (per-shard partial (max, sum exp) and single-owner gather).
+//
+// Layout of the work.  One persistent CTA per SM takes active rows i =
+// blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams each row
+// through a ring of shared-memory stages with 1-D bulk copies (TMA,
+// cp.async.bulk, completion on an mbarrier); every stage holds the same 4096
+// columns of both sides.  16 consumer warps read the stage, and thread t owns
+// columns [4t, 4t+4) and [2048+4t, 2048+4t+4) of every tile.  Each thread keeps
+// an online (max m, sum s) pair per side in fp32; at the end of a segment each
+// warp merges its 32 pairs in a fixed butterfly and writes one pair per side
+// to the workspace.  The finalise kernel merges the 16 warp pairs, the
+// segments and does the fp64 row arithmetic.
+//
+// Batch invariance ("Attention Debug Matrix", section "Metrics": the
+// batch-composition control must be bitwise zero): the value that reaches a
+// thread, the order in which it accumulates, and the merge trees depend only
+// on the logical column index, never on the row index, the grid, the load path
+// or the storage dtype (bf16 and fp32 inputs are widened to fp32 first and
+// then share one arithmetic path, written with explicit round-to-nearest
+// intrinsics so the compiler cannot contract it differently per dtype).
+#include <cfloat>
+
+#include "lpd_internal.cuh"
+
+namespace lpd {
+namespace {
+
+struct Bf16 {
+    static constexpr int kBytes = 2;
+};
+struct F32 {
+    static constexpr int kBytes = 4;
+};
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: a stage takes microseconds
+constexpr uint32_t kWaitLimitIters = 1u << 30;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// 2^x on the special-function unit.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---- mbarrier and bulk copy (inline PTX) ----------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  Gives up (and tells every
+// other thread of the CTA to give up) after kWaitLimitNs, recording
+// LPD_STATUS_TIMEOUT; a pipeline stage normally completes in microseconds.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           uint32_t *status, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1; n < kWaitLimitIters; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+    }
+    *abort_flag = 1;
+    atomicOr(status, LPD_STATUS_TIMEOUT);
+    return false;
+}
+
+// ---- element access ------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <class D>
+__device__ __forceinline__ float ldg_elem(const char *p);
+template <>
+__device__ __forceinline__ float ldg_elem<Bf16>(const char *p) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p))) << 16);
+}
+template <>
+__device__ __forceinline__ float ldg_elem<F32>(const char *p) {
+    return __ldg(reinterpret_cast<const float *>(p));
+}
+
+template <class D>
+__device__ __forceinline__ float lds_elem(const char *stage, int col);
+template <>
+__device__ __forceinline__ float lds_elem<Bf16>(const char *stage, int col) {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(stage + 2 * col)) << 16);
+}
+template <>
+__device__ __forceinline__ float lds_elem<F32>(const char *stage, int col) {
+    return *reinterpret_cast<const float *>(stage + 4 * col);
+}
+
+// Four consecutive columns starting at `col` (a multiple of 4) of a stage.
+template <class D>
+__device__ __forceinline__ void lds4(const char *stage, int col, float *v);
+template <>
+__device__ __forceinline__ void lds4<Bf16>(const char *stage, int col, float *v) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(stage + 2 * col);
+    v[0] = bf16_lo(w.x);
+    v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y);
+    v[3] = bf16_hi(w.y);
+}
+template <>
+__device__ __forceinline__ void lds4<F32>(const char *stage, int col, float *v) {
+    const float4 w = *reinterpret_cast<const float4 *>(stage + 4 * col);
+    v[0] = w.x;
+    v[1] = w.y;
+    v[2] = w.z;
+    v[3] = w.w;
+}
+
+// Column owned by slot q (0..7) of consumer thread t within a tile.
+__device__ __forceinline__ int slot_col(int t, int q) {
+    return q < 4 ? 4 * t + q : kHalfTile + 4 * t + (q - 4);
+}
+
+// ---- the arithmetic (shared by every load path and dtype) ------------------
+// Online log-sum-exp of eight values into (m, s): s = sum exp(x - m).  The
+// chunk maximum is taken first, the running sum is rescaled at most once, and
+// the eight terms are added in a fixed pairwise tree.  Values of -inf (masked
+// tail columns) contribute exactly 0; the floor -FLT_MAX keeps (x - m) defined
+// for rows that are -inf everywhere.
+__device__ __forceinline__ void accumulate8(const float *v, float &m, float &s) {
+    const float cm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                           fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+    if (cm > m) {
+        s = __fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
+        m = cm;
+    }
+    float e[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = ex2(__fmul_rn(__fsub_rn(v[q], m), kLog2e));
+    const float t = __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
+                              __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+    s = __fadd_rn(s, t);
+}
+
+// Merge (mo, so) into (m, s).  Symmetric in its two operands bit for bit
+// (max and IEEE addition commute), so a butterfly leaves every lane equal.
+__device__ __forceinline__ void merge_pair(float &m, float &s, float mo, float so) {
+    const float mn = fmaxf(m, mo);
+    s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, mn), kLog2e))),
+                  __fmul_rn(so, ex2(__fmul_rn(__fsub_rn(mo, mn), kLog2e))));
+    m = mn;
+}
+
+__device__ __forceinline__ float select8(const float *v, int q) {
+    float x = v[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) x = (q == k) ? v[k] : x;
+    return x;
+}
+
+template <class DT, class DR, bool kTma>
+__global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
+    extern __shared__ __align__(1024) char smem[];
+    __shared__ int abort_flag;
+    constexpr int kStageT = kTile * DT::kBytes;
+    constexpr int kStageR = kTile * DR::kBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + n_stages;
+    char *ring = smem + 1024;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_active = a.hdr->n_active;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        if (kTma) {
+            for (int s = 0; s < n_stages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kConsumerWarps);
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (!kTma || lane != 0) return;
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; ok && i < n_active; i += gridDim.x) {
+            const int64_t r = a.rowid[i].x;
+            for (int k = 0; ok && k < a.n_seg; ++k) {
+                const Segment &sg = a.seg[k];
+                const char *tb = sg.t + r * sg.t_stride;
+                const char *rb = sg.r + r * sg.r_stride;
+                for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
+                    const uint32_t stage = it % n_stages, round = it / n_stages;
+                    if (round > 0 && !wait_phase(&empty[stage], (round - 1) & 1, &abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t nv = min(static_cast<int64_t>(kTile), sg.len - c0);
+                    const uint32_t bt = static_cast<uint32_t>(nv * DT::kBytes) & ~15u;
+                    const uint32_t br = static_cast<uint32_t>(nv * DR::kBytes) & ~15u;
+                    char *st = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
+                    mbar_arrive_expect_tx(&full[stage], bt + br);
+                    if (bt) bulk_g2s(st, tb + c0 * DT::kBytes, bt, &full[stage], policy);
+                    if (br) bulk_g2s(st + kStageT, rb + c0 * DR::kBytes, br, &full[stage], policy);
+                    ++it;
+                }
+            }
+        }
+        // Before the CTA (and its shared memory) goes away, every copy this
+        // thread issued must have landed: the last n_stages ones are the only
+        // ones that can still be in flight.  Normally they completed long ago
+        // (the consumers waited for them); after an abandoned pipeline this is
+        // the bounded wait for the stragglers.
+        (void)ok;
+        const uint32_t first = it > static_cast<uint32_t>(n_stages) ? it - n_stages : 0;
+        for (uint32_t j = first; j < it; ++j)
+            wait_phase(&full[j % n_stages], (j / n_stages) & 1, &abort_flag, a.status, false);
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int t = threadIdx.x;
+    uint32_t it = 0;
+    for (int64_t i = blockIdx.x; i < n_active; i += gridDim.x) {
+        const int2 rid = a.rowid[i];
+        const int64_t r = rid.x, id = rid.y;
+        // Which segment, tile and slot hold the selected column, and whether
+        // this thread owns it (single-owner gather).
+        int pick_seg = -1, pick_slot = 0;
+        int64_t pick_c0 = -1;
+        bool pick_mine = false;
+        if (id >= 0 && id < a.vocab) {
+            for (int k = 0; k < a.n_seg; ++k) {
+                const int64_t c = id - a.seg[k].v_start;
+                if (c >= 0 && c < a.seg[k].len) {
+                    const int pos = static_cast<int>(c % kTile);
+                    pick_seg = k;
+                    pick_c0 = c - pos;
+                    pick_slot = (pos / kHalfTile) * 4 + (pos & 3);
+                    pick_mine = ((pos % kHalfTile) >> 2) == t;
+                }
+            }
+        }
+        for (int k = 0; k < a.n_seg; ++k) {
+            const Segment &sg = a.seg[k];
+            const char *tb = sg.t + r * sg.t_stride;
+            const char *rb = sg.r + r * sg.r_stride;
+            float mt = -FLT_MAX, st = 0.f, mr = -FLT_MAX, sr = 0.f;
+            for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
+                const int nv = static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
+                float vt[8], vr[8];
+                if (kTma) {
+                    const uint32_t stage = it % n_stages, round = it / n_stages;
+                    // the whole warp leaves together if any lane gave up, so no
+                    // lane is left behind at a warp-synchronous instruction
+                    const bool ok = wait_phase(&full[stage], round & 1, &abort_flag, a.status);
+                    if (__any_sync(0xffffffffu, !ok)) return;
+                    const char *stg = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
+                    if (nv == kTile) {
+                        lds4<DT>(stg, 4 * t, vt);
+                        lds4<DT>(stg, kHalfTile + 4 * t, vt + 4);
+                        lds4<DR>(stg + kStageT, 4 * t, vr);
+                        lds4<DR>(stg + kStageT, kHalfTile + 4 * t, vr + 4);
+                    } else {
+                        // ragged last tile: the bulk copy moved whole 16-byte
+                        // units; the few columns after them come from global
+                        const int nbt = static_cast<int>((static_cast<uint32_t>(nv * DT::kBytes) & ~15u) / DT::kBytes);
+                        const int nbr = static_cast<int>((static_cast<uint32_t>(nv * DR::kBytes) & ~15u) / DR::kBytes);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int col = slot_col(t, q);
+                            vt[q] = col < nbt ? lds_elem<DT>(stg, col)
+                                  : col < nv  ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes)
+                                              : -INFINITY;
+                            vr[q] = col < nbr ? lds_elem<DR>(stg + kStageT, col)
+                                  : col < nv  ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes)
+                                              : -INFINITY;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);  // values are in registers now
+                    ++it;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int col = slot_col(t, q);
+                        vt[q] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
+                        vr[q] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
+                    }
+                }
+                if (pick_mine && k == pick_seg && c0 == pick_c0)
+                    a.pick[i] = make_float2(select8(vt, pick_slot), select8(vr, pick_slot));
+                accumulate8(vt, mt, st);
+                accumulate8(vr, mr, sr);
+            }
+            // fixed butterfly over the warp
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float mto = __shfl_xor_sync(0xffffffffu, mt, off);
+                const float sto = __shfl_xor_sync(0xffffffffu, st, off);
+                const float mro = __shfl_xor_sync(0xffffffffu, mr, off);
+                const float sro = __shfl_xor_sync(0xffffffffu, sr, off);
+                merge_pair(mt, st, mto, sto);
+                merge_pair(mr, sr, mro, sro);
+            }
+            if (lane == 0)
+                a.part[(i * a.n_seg + k) * kConsumerWarps + warp] = make_float4(mt, st, mr, sr);
+        }
+    }
+}
+
+template <class DT, class DR, bool kTma>
+cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
+    const int stage_bytes = kTile * (DT::kBytes + DR::kBytes);
+    const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
+    const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
+    auto kern = row_kernel<DT, DR, kTma>;
+    static int configured_device = -1;  // attribute is per device; cheap to repeat
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    kern<<<device_sm_count(), kRowThreads, smem, stream>>>(a, n_stages);
+    return cudaGetLastError();
+}
+
+template <bool kTma>
+cudaError_t dispatch(const RowArgs &a, int dt, int dr, cudaStream_t stream) {
+    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma>(a, stream);
+    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma>(a, stream);
+    return launch_typed<F32, F32, kTma>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, cudaStream_t stream) {
+    return use_tma ? dispatch<true>(a, dtype_t, dtype_r, stream) : dispatch<false>(a, dtype_t, dtype_r, stream);
+}
+
+}  // namespace lpd

@@ -1,0 +1,149 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/lpd.h declares, and rejects invalid arguments on the host with the
+documented codes before launching anything."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from logprob_drift_scoring_gb300 import binding as B
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "lpd.h"
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(lpd_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.lib()
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTED), names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_struct_sizes_match_header_layout():
+    assert ctypes.sizeof(B.LpdLogits) == 24
+    assert ctypes.sizeof(B.LpdShard) == 40
+    assert ctypes.sizeof(B.LpdMetrics) == 80
+    assert ctypes.sizeof(B.LpdBackendInfo) == 32 + 48 + 16 + 32 + 16 + 96
+
+
+def test_backend_info():
+    info = B.lpd_backend_info()
+    assert info["backend_id"] == "lpd.sm103a.v1"
+    assert info["op_name"] == "selected_logprob_drift"
+    assert info["arch"] == "sm_103a"
+    assert info["deterministic"] == 1 and info["batch_invariant"] == 1
+    assert info["fast_math"] == 0 and info["has_fallback"] == 0
+    assert "nvcc" in info["fingerprint"]
+
+
+def test_strerror_covers_every_code():
+    for code in range(0, -11, -1):
+        assert B.lpd_strerror(code) != "unknown code", code
+    for bit in (B.LPD_STATUS_TOKEN_OOB, B.LPD_STATUS_NONFINITE, B.LPD_STATUS_TIMEOUT):
+        assert B.lpd_strerror(bit).startswith("status")
+    assert B.lpd_strerror(12345) == "unknown code"
+
+
+def test_workspace_size():
+    small = B.lpd_workspace_size(B.LPD_KIND_SCORE, 10)
+    big = B.lpd_workspace_size(B.LPD_KIND_SCORE, 100000)
+    assert 0 < small < big and small % 256 == 0 and big % 256 == 0
+    assert B.lpd_workspace_size(B.LPD_KIND_SCORE, 0) > 0
+    assert B.lpd_workspace_size(B.LPD_KIND_SCORE, -1) == 0
+    assert B.lpd_workspace_size(B.LPD_KIND_SHARDED, 100, 1000, 4) > B.lpd_workspace_size(B.LPD_KIND_SCORE, 100)
+    assert B.lpd_workspace_size(B.LPD_KIND_SHARDED, 100, 1000, 0) == 0
+    assert B.lpd_workspace_size(B.LPD_KIND_SHARDED, 100, 1000, 17) == 0
+    assert B.lpd_workspace_size(99, 100) == 0
+
+
+# Fake device addresses: validation must reject these calls before any launch.
+FAKE = 0x7F0000000000
+WS_OK = FAKE + 0x100000
+
+
+def _call_score(t=None, r=None, n_rows=8, vocab=16, ids=FAKE, mask=FAKE, lo=0.8, hi=1.2, met=FAKE,
+                ws=WS_OK, ws_bytes=1 << 20):
+    lib = B.lib()
+    t = t if t is not None else B.LpdLogits(FAKE, B.LPD_BF16, 0, vocab)
+    r = r if r is not None else B.LpdLogits(FAKE, B.LPD_F32, 0, vocab)
+    return lib.lpd_score(ctypes.byref(t) if t != "null" else None, ctypes.byref(r), n_rows, vocab, ids, mask,
+                         lo, hi, None, None, None, met, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(t="null"), B.LPD_ERR_NULL_POINTER),
+    (dict(t=B.LpdLogits(None, B.LPD_BF16, 0, 16)), B.LPD_ERR_NULL_POINTER),
+    (dict(ids=None), B.LPD_ERR_NULL_POINTER),
+    (dict(mask=None), B.LPD_ERR_NULL_POINTER),
+    (dict(met=None), B.LPD_ERR_NULL_POINTER),
+    (dict(n_rows=-1), B.LPD_ERR_BAD_SIZE),
+    (dict(vocab=0), B.LPD_ERR_BAD_SIZE),
+    (dict(vocab=1 << 31), B.LPD_ERR_UNSUPPORTED),
+    (dict(t=B.LpdLogits(FAKE, 7, 0, 16)), B.LPD_ERR_BAD_DTYPE),
+    (dict(r=B.LpdLogits(FAKE, B.LPD_F32, 0, 15)), B.LPD_ERR_BAD_STRIDE),
+    (dict(t=B.LpdLogits(FAKE + 1, B.LPD_BF16, 0, 16)), B.LPD_ERR_ALIGNMENT),
+    (dict(r=B.LpdLogits(FAKE + 2, B.LPD_F32, 0, 16)), B.LPD_ERR_ALIGNMENT),
+    (dict(lo=1.3, hi=1.2), B.LPD_ERR_BAD_CLIP),
+    (dict(lo=0.0), B.LPD_ERR_BAD_CLIP),
+    (dict(lo=-0.5), B.LPD_ERR_BAD_CLIP),
+    (dict(hi=float("inf")), B.LPD_ERR_BAD_CLIP),
+    (dict(lo=float("nan")), B.LPD_ERR_BAD_CLIP),
+    (dict(ws=None), B.LPD_ERR_WORKSPACE),
+    (dict(ws_bytes=16), B.LPD_ERR_WORKSPACE),
+    (dict(ws=WS_OK + 8), B.LPD_ERR_ALIGNMENT),
+])
+def test_score_rejects_invalid_arguments(kwargs, code):
+    assert _call_score(**kwargs) == code
+
+
+def _call_sharded(shards_t, shards_r, vocab=100, perm=None, n_rows=4):
+    lib = B.lib()
+    n = len(shards_t)
+    ts = (B.LpdShard * n)(*shards_t)
+    rs = (B.LpdShard * n)(*shards_r)
+    p = (ctypes.c_int32 * n)(*perm) if perm is not None else None
+    return lib.lpd_score_sharded(ts, rs, n, n_rows, vocab, FAKE, FAKE, 0.8, 1.2, p, None, None, None, None, None,
+                                 FAKE, WS_OK, 1 << 24, None)
+
+
+def _sh(v0, v1, dtype=B.LPD_BF16, stride=None):
+    return B.LpdShard(FAKE, dtype, 0, stride if stride is not None else v1 - v0, v0, v1)
+
+
+@pytest.mark.parametrize("t,r,perm,code", [
+    ([_sh(0, 50), _sh(51, 100)], [_sh(0, 50), _sh(51, 100)], None, B.LPD_ERR_BAD_SHARDS),        # gap
+    ([_sh(0, 51), _sh(50, 100)], [_sh(0, 51), _sh(50, 100)], None, B.LPD_ERR_BAD_SHARDS),        # overlap
+    ([_sh(0, 50), _sh(25, 75)], [_sh(0, 50), _sh(25, 75)], None, B.LPD_ERR_BAD_SHARDS),          # overlap hides gap
+    ([_sh(0, 50), _sh(50, 101)], [_sh(0, 50), _sh(50, 101)], None, B.LPD_ERR_BAD_SHARDS),        # past vocab
+    ([_sh(0, 50)], [_sh(0, 50)], None, B.LPD_ERR_BAD_SHARDS),                                   # short
+    ([_sh(0, 50), _sh(50, 100)], [_sh(0, 40), _sh(40, 100)], None, B.LPD_ERR_BAD_SHARDS),        # sides differ
+    ([_sh(0, 50), _sh(50, 100, B.LPD_F32)], [_sh(0, 50), _sh(50, 100)], None, B.LPD_ERR_BAD_DTYPE),
+    ([_sh(0, 50), _sh(50, 100, stride=49)], [_sh(0, 50), _sh(50, 100)], None, B.LPD_ERR_BAD_STRIDE),
+    ([_sh(0, 50), _sh(50, 100)], [_sh(0, 50), _sh(50, 100)], [0, 0], B.LPD_ERR_BAD_SHARDS),      # not a permutation
+    ([_sh(0, 50), _sh(50, 100)], [_sh(0, 50), _sh(50, 100)], [0, 2], B.LPD_ERR_BAD_SHARDS),
+])
+def test_sharded_rejects_bad_maps(t, r, perm, code):
+    assert _call_sharded(t, r, perm=perm) == code
+
+
+def test_sharded_shard_count_limits():
+    assert _call_sharded([], [], vocab=100) == B.LPD_ERR_UNSUPPORTED
+    many = [_sh(k, k + 1) for k in range(17)]
+    assert _call_sharded(many, many, vocab=17) == B.LPD_ERR_UNSUPPORTED
+
+
+def test_stage_entry_points_validate():
+    lib = B.lib()
+    assert lib.lpd_select_active(-1, FAKE, FAKE, None, None, None, FAKE, WS_OK, 1 << 20, None) == B.LPD_ERR_BAD_SIZE
+    assert lib.lpd_select_active(4, None, FAKE, None, None, None, FAKE, WS_OK, 1 << 20, None) == B.LPD_ERR_NULL_POINTER
+    assert lib.lpd_drift_metrics(4, 1.0, 0.5, FAKE, WS_OK, 1 << 20, None) == B.LPD_ERR_BAD_CLIP
+    assert lib.lpd_drift_metrics(4, 0.8, 1.2, None, WS_OK, 1 << 20, None) == B.LPD_ERR_NULL_POINTER
+    t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 10)
+    assert lib.lpd_token_logp(ctypes.byref(t), ctypes.byref(t), 4, 11, None, None, None, FAKE, WS_OK, 1 << 20,
+                              None) == B.LPD_ERR_BAD_STRIDE

@@ -1,0 +1,362 @@
+"""CUDA path against the float64 oracle, through the C ABI (needs a GPU).
+
+Bars (see tests/helpers.py): per-token logp within 1e-4 absolute, approx_kl0
+and mean_abs_dlogp within 1e-4 relative, percentiles within 1e-4 absolute,
+counts and selection exact, batch-invariance controls bitwise.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from logprob_drift_scoring_gb300 import binding as B
+from logprob_drift_scoring_gb300 import workloads as W
+from tests.helpers import LOGP_ATOL, assert_metrics_match, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def run(train, rollout, ids, mask, clip=(0.8, 1.2)):
+    res = B.score(train, rollout, ids, mask, clip)
+    torch.cuda.synchronize()
+    return res
+
+
+def oracle_score(train, rollout, ids, mask, clip=(0.8, 1.2)):
+    return oracle.score(to_oracle(train), to_oracle(rollout), ids.cpu().numpy(), mask.cpu().numpy(), *clip)
+
+
+def check_against_oracle(w, clip=(0.8, 1.2)):
+    res = run(w.train, w.rollout, w.token_ids, w.action_mask, clip)
+    ref = oracle_score(w.train, w.rollout, w.token_ids, w.action_mask, clip)
+    mask = w.action_mask.cpu().numpy()
+    lt, lr, d = (x.cpu().numpy().astype(np.float64) for x in (res.logp_train, res.logp_rollout, res.dlogp))
+    act = mask != 0
+    assert np.all(lt[~act] == 0) and np.all(lr[~act] == 0) and np.all(d[~act] == 0)
+    if act.any():
+        assert np.max(np.abs(lt[act] - ref.logp_train[act])) <= LOGP_ATOL
+        assert np.max(np.abs(lr[act] - ref.logp_rollout[act])) <= LOGP_ATOL
+        assert np.max(np.abs(d[act] - ref.dlogp[act])) <= LOGP_ATOL
+    assert_metrics_match(res.metrics, ref.metrics, ref.dlogp, mask, clip)
+    return res, ref
+
+
+# ------------------------------------------------------------------ parity
+
+def test_tiny_config_vs_oracle():
+    w = W.tiny(device=DEV)
+    res, ref = check_against_oracle(w)
+    assert res.metrics["n_active"] == int(w.action_mask.sum())
+    # the tiny drift is ~1e-3: dlogp itself must be far better than the logp bar
+    act = w.action_mask.cpu().numpy() != 0
+    err = np.abs(res.dlogp.cpu().numpy()[act] - ref.dlogp[act])
+    assert err.max() <= 1e-6, err.max()
+
+
+CASES = {
+    # name: (rows, vocab, dtype_t, dtype_r, kwargs)
+    "bf16_3tiles_ragged_tma": (300, 3 * 4096 + 520, torch.bfloat16, torch.bfloat16, {}),
+    "bf16_unaligned_rows_generic": (257, 3 * 4096 + 517, torch.bfloat16, torch.bfloat16, {}),
+    "bf16_padded_rows_tma_subvector_tail": (130, 3 * 4096 + 517, torch.bfloat16, torch.bfloat16, dict(row_pad=3)),
+    "mixed_bf16_f32": (200, 9000, torch.bfloat16, torch.float32, {}),
+    "mixed_f32_bf16_one_tile": (150, 4096, torch.float32, torch.bfloat16, {}),
+    "f32_f32_vocab5": (90, 5, torch.float32, torch.float32, {}),
+    "bf16_vocab1": (40, 1, torch.bfloat16, torch.bfloat16, {}),
+    "bf16_vocab2": (40, 2, torch.bfloat16, torch.bfloat16, {}),
+    "bf16_vocab7_generic": (40, 7, torch.bfloat16, torch.bfloat16, {}),
+    "many_rows_small_vocab": (5000, 256, torch.bfloat16, torch.bfloat16, {}),
+    "spiky_wide": (64, 151936, torch.bfloat16, torch.bfloat16, dict(spike_frac=0.2)),
+    "independent_rollout_clipping": (400, 2000, torch.bfloat16, torch.bfloat16, dict(rollout_noise=0.4)),
+    "f32_unaligned_generic": (100, 4097, torch.float32, torch.float32, {}),
+    "f32_vocab5_padded_tma_tail": (90, 5, torch.float32, torch.float32, dict(row_pad=3)),
+    "bf16_vocab7_padded_tma_tail": (40, 7, torch.bfloat16, torch.bfloat16, dict(row_pad=1)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_parity_synthetic(name):
+    rows, vocab, dt, dr, kw = CASES[name]
+    w = W.synthetic(rows, vocab, seed=zlib.crc32(name.encode()) % 1000, device=DEV, dtype_train=dt, dtype_rollout=dr, **kw)
+    res, ref = check_against_oracle(w)
+    if name == "independent_rollout_clipping":
+        assert ref.metrics["clipfrac0"] > 0.05
+
+
+# --------------------------------------------------------- bitwise controls
+
+def test_identical_inputs_give_exact_zeros():
+    w = W.synthetic(300, 5000, seed=5, device=DEV)
+    res = run(w.train, w.train, w.token_ids, w.action_mask)
+    assert torch.all(res.dlogp == 0)
+    assert torch.equal(res.logp_train, res.logp_rollout)
+    m = res.metrics
+    assert m["ratio0_mean"] == 1.0 and m["approx_kl0"] == 0.0 and m["clipfrac0"] == 0.0
+    assert m["mean_abs_dlogp"] == m["p95_abs_dlogp"] == m["p99_abs_dlogp"] == m["max_abs_dlogp"] == 0.0
+
+
+def test_bf16_against_its_fp32_upcast_is_bitwise_zero():
+    w = W.synthetic(200, 12808, seed=6, device=DEV)
+    up = w.train.float().contiguous()
+    res = run(w.train, up, w.token_ids, w.action_mask)
+    assert torch.all(res.dlogp == 0)
+    assert torch.equal(res.logp_train, res.logp_rollout)
+
+
+def _embed(rows_t, rows_r, ids, n_total, offset, seed):
+    """Place the given rows at [offset, offset+k) of a bigger batch whose other
+    rows are inactive garbage (padding on either side)."""
+    k, V = rows_t.shape
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    t = (100 * torch.randn((n_total, V), generator=g, device=DEV)).to(rows_t.dtype)
+    r = (100 * torch.randn((n_total, V), generator=g, device=DEV)).to(rows_r.dtype)
+    i = torch.randint(-5, V + 5, (n_total,), generator=g, device=DEV, dtype=torch.int32)
+    m = torch.zeros(n_total, dtype=torch.uint8, device=DEV)
+    t[offset:offset + k] = rows_t
+    r[offset:offset + k] = rows_r
+    i[offset:offset + k] = ids
+    m[offset:offset + k] = 1
+    return t, r, i, m
+
+
+def test_batch_composition_control_bitwise():
+    base = W.synthetic(64, 3 * 4096 + 520, seed=7, device=DEV, active_prob=1.0)
+    full = run(base.train, base.rollout, base.token_ids, base.action_mask)
+    outs = (full.logp_train, full.logp_rollout, full.dlogp)
+    # batch of 1, each row alone at a different offset
+    for j in (0, 5, 63):
+        t, r, i, m = _embed(base.train[j:j + 1], base.rollout[j:j + 1], base.token_ids[j:j + 1], 3, j % 3, j)
+        res = run(t, r, i, m)
+        off = j % 3
+        for a, b in zip((res.logp_train, res.logp_rollout, res.dlogp), outs):
+            assert torch.equal(a[off:off + 1], b[j:j + 1])
+    # batches of 7 at shifted offsets with left and right padding
+    for start, total, off in ((0, 7, 0), (10, 20, 13), (57, 9, 2), (30, 160, 100)):
+        sl = slice(start, start + 7)
+        t, r, i, m = _embed(base.train[sl], base.rollout[sl], base.token_ids[sl], total, off, start)
+        res = run(t, r, i, m)
+        for a, b in zip((res.logp_train, res.logp_rollout, res.dlogp), outs):
+            assert torch.equal(a[off:off + 7], b[sl])
+    # batch of 64 inside a larger batch
+    t, r, i, m = _embed(base.train, base.rollout, base.token_ids, 200, 77, 99)
+    res = run(t, r, i, m)
+    for a, b in zip((res.logp_train, res.logp_rollout, res.dlogp), outs):
+        assert torch.equal(a[77:141], b)
+
+
+def test_load_path_does_not_change_bits():
+    # same rows stored with 16-byte aligned rows (bulk-copy ring) and with an
+    # odd row stride (plain loads): identical results
+    base = W.synthetic(50, 3 * 4096 + 517, seed=8, device=DEV, row_pad=3, active_prob=1.0)
+    aligned = run(base.train, base.rollout, base.token_ids, base.action_mask)
+    t2 = base.train.contiguous()   # stride 12805 elements: rows not 16-byte aligned
+    r2 = base.rollout.contiguous()
+    assert (t2.stride(0) * 2) % 16 != 0
+    generic = run(t2, r2, base.token_ids, base.action_mask)
+    for a, b in zip((aligned.logp_train, aligned.logp_rollout, aligned.dlogp),
+                    (generic.logp_train, generic.logp_rollout, generic.dlogp)):
+        assert torch.equal(a, b)
+
+
+def test_run_to_run_bitwise():
+    w = W.synthetic(700, 20000, seed=9, device=DEV)
+    a = run(w.train, w.rollout, w.token_ids, w.action_mask)
+    b = run(w.train, w.rollout, w.token_ids, w.action_mask)
+    for x, y in zip((a.logp_train, a.logp_rollout, a.dlogp), (b.logp_train, b.logp_rollout, b.dlogp)):
+        assert torch.equal(x, y)
+    assert a.metrics == b.metrics
+
+
+# ------------------------------------------------------------------- edges
+
+def test_zero_rows():
+    t = torch.empty((0, 100), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty(0, dtype=torch.int32, device=DEV)
+    mask = torch.empty(0, dtype=torch.uint8, device=DEV)
+    res = run(t, t, ids, mask)
+    m = res.metrics
+    assert m["n_active"] == 0 and m["flags"] == B.LPD_FLAG_NO_ACTIVE and m["status"] == 0
+    assert m["argmax_row"] == -1 and m["max_abs_dlogp"] == 0.0
+
+
+def test_all_masked():
+    w = W.synthetic(100, 3000, seed=10, device=DEV)
+    mask = torch.zeros_like(w.action_mask)
+    res, ref = check_against_oracle(W.Workload("m", w.train, w.rollout, w.token_ids, mask, w.vocab))
+    assert res.metrics["n_active"] == 0 and res.metrics["flags"] == B.LPD_FLAG_NO_ACTIVE
+    assert torch.all(res.dlogp == 0)
+
+
+def test_token_out_of_range():
+    w = W.synthetic(50, 1000, seed=11, device=DEV, active_prob=1.0)
+    ids = w.token_ids.clone()
+    ids[7] = 1000
+    res = run(w.train, w.rollout, ids, w.action_mask)
+    assert res.metrics["status"] == B.LPD_STATUS_TOKEN_OOB
+    assert torch.isnan(res.logp_train[7]) and torch.isnan(res.dlogp[7])
+    ids[7] = -3
+    assert run(w.train, w.rollout, ids, w.action_mask).metrics["status"] == B.LPD_STATUS_TOKEN_OOB
+    # the same bad id on an inactive row is never looked at
+    mask = w.action_mask.clone()
+    mask[7] = 0
+    res2 = run(w.train, w.rollout, ids, mask)
+    assert res2.metrics["status"] == 0
+
+
+def test_nonfinite_logits():
+    w = W.synthetic(20, 5000, seed=12, device=DEV, active_prob=1.0)
+    t = w.train.clone()
+    t[3, 100] = float("nan")
+    assert run(t, w.rollout, w.token_ids, w.action_mask).metrics["status"] == B.LPD_STATUS_NONFINITE
+    t = w.train.clone()
+    t[4, :] = float("-inf")
+    assert run(t, w.rollout, w.token_ids, w.action_mask).metrics["status"] == B.LPD_STATUS_NONFINITE
+    # -inf columns elsewhere are fine and agree with the oracle
+    t = w.train.clone()
+    cols = (w.token_ids[5].item() + 1) % 5000
+    t[5, cols] = float("-inf")
+    t[6, 4999] = float("-inf")
+    w2 = W.Workload("ninf", t, w.rollout, w.token_ids, w.action_mask, w.vocab)
+    res, ref = check_against_oracle(w2)
+    assert res.metrics["status"] == 0
+    # garbage in inactive rows changes nothing
+    mask = w.action_mask.clone()
+    mask[9] = 0
+    t = w.train.clone()
+    t[9] = float("nan")
+    res3 = run(t, w.rollout, w.token_ids, mask)
+    assert res3.metrics["status"] == 0
+
+
+def test_stage_entry_points_equal_lpd_score():
+    w = W.synthetic(333, 7000, seed=13, device=DEV)
+    full = run(w.train, w.rollout, w.token_ids, w.action_mask)
+    n = w.n_rows
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for _ in range(3)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, n), dtype=torch.uint8, device=DEV)
+    B.lpd_select_active(w.token_ids, w.action_mask, *outs, met, ws)
+    B.lpd_token_logp(w.train, w.rollout, *outs, met, ws)
+    B.lpd_drift_metrics(n, 0.8, 1.2, met, ws)
+    torch.cuda.synchronize()
+    for a, b in zip(outs, (full.logp_train, full.logp_rollout, full.dlogp)):
+        assert torch.equal(a, b)
+    assert B.read_metrics(met) == full.metrics
+
+
+# ------------------------------------------------------------------ sharded
+
+def _sharded_call(w, perm=None):
+    n = w.n_rows
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for _ in range(5)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SHARDED, n, w.vocab, len(w.v_ranges)), dtype=torch.uint8,
+                     device=DEV)
+    B.lpd_score_sharded(w.train, w.rollout, w.v_ranges, w.token_ids, w.action_mask, 0.8, 1.2, perm, *outs, met, ws)
+    torch.cuda.synchronize()
+    return outs, B.read_metrics(met)
+
+
+def _small_sharded(bounds, rows=120, seed=20):
+    base = W.synthetic(rows, bounds[-1][1], seed=seed, device=DEV)
+    ts = [base.train[:, a:b].contiguous() for a, b in bounds]
+    rs = [base.rollout[:, a:b].contiguous() for a, b in bounds]
+    return base, W.Workload("sh", ts, rs, base.token_ids, base.action_mask, base.vocab, v_ranges=list(bounds))
+
+
+@pytest.mark.parametrize("bounds", [
+    [(0, 4096), (4096, 8192), (8192, 12288), (12288, 16384)],
+    [(0, 1000), (1000, 9000), (9000, 9001), (9001, 12000)],
+    [(0, 5000)],
+])
+def test_sharded_vs_oracle(bounds):
+    base, w = _small_sharded(bounds)
+    perm = list(range(len(bounds)))[::-1]
+    (lt, lr, d, plt, plr), met = _sharded_call(w, perm)
+    mask = w.action_mask.cpu().numpy()
+    ref = oracle.score_sharded([to_oracle(x) for x in w.train], [to_oracle(x) for x in w.rollout], w.v_ranges,
+                               w.token_ids.cpu().numpy(), mask)
+    ref_p = oracle.score_sharded([to_oracle(x) for x in w.train], [to_oracle(x) for x in w.rollout], w.v_ranges,
+                                 w.token_ids.cpu().numpy(), mask, order=perm)
+    act = mask != 0
+    for got, want in ((lt, ref.logp_train), (lr, ref.logp_rollout), (d, ref.dlogp),
+                      (plt, ref_p.logp_train), (plr, ref_p.logp_rollout)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g[act] - want[act])) <= LOGP_ATOL
+        assert np.all(g[~act] == 0)
+    assert_metrics_match(met, ref.metrics, ref.dlogp, mask)
+    # the fixed-order result is bitwise repeatable
+    (lt2, _, d2, _, _), met2 = _sharded_call(w, perm)
+    assert torch.equal(lt, lt2) and torch.equal(d, d2) and met == met2
+    # array order of the shards does not matter (merge order is vocab order)
+    rev = W.Workload("rev", w.train[::-1], w.rollout[::-1], w.token_ids, w.action_mask, w.vocab,
+                     v_ranges=w.v_ranges[::-1])
+    (lt3, _, d3, _, _), _ = _sharded_call(rev)
+    assert torch.equal(lt, lt3) and torch.equal(d, d3)
+
+
+# --------------------------------------------------------------- full size
+
+def _sampled_parity(w, n_sample=256, seed=0):
+    """Per-token parity on sampled active rows against the oracle, and the
+    metrics against the oracle's metric function applied to the GPU's own
+    per-token dlogp (a property that holds at any size)."""
+    res = run(w.train, w.rollout, w.token_ids, w.action_mask, w.clip)
+    mask = w.action_mask.cpu().numpy()
+    act_rows = np.flatnonzero(mask)
+    assert res.metrics["n_active"] == act_rows.size
+    assert res.metrics["status"] == 0
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(act_rows, size=min(n_sample, act_rows.size), replace=False))
+    rows = np.unique(np.concatenate([rows, act_rows[:2], act_rows[-2:]]))
+    sel = torch.as_tensor(rows, device=DEV)
+    ids = w.token_ids.cpu().numpy()
+    ref = oracle.score_rows(to_oracle(w.train[sel]), to_oracle(w.rollout[sel]), ids[rows],
+                            np.arange(rows.size), lib=None)
+    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout),
+                      (res.dlogp, ref.dlogp)):
+        g = got[sel].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g - want)) <= LOGP_ATOL
+    d = res.dlogp.cpu().numpy().astype(np.float64)
+    prop = oracle.metrics(d, mask, *w.clip)
+    prop["status"] = 0
+    assert_metrics_match(res.metrics, prop, d, mask, w.clip, ambiguity=1e-6)
+    return res
+
+
+def test_full_size_qwen_vocab():
+    w = W.qwen(device=DEV)
+    _sampled_parity(w)
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_full_size_llama_mixed_dtype():
+    w = W.llama(device=DEV)
+    _sampled_parity(w)
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_full_size_sharded():
+    w = W.sharded(device=DEV)
+    (lt, lr, d, plt, plr), met = _sharded_call(w, perm=[2, 0, 3, 1])
+    assert met["n_active"] == w.n_rows and met["status"] == 0
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(w.n_rows, size=128, replace=False))
+    sel = torch.as_tensor(rows, device=DEV)
+    ids = w.token_ids.cpu().numpy()[rows]
+    ref = oracle.score_sharded([to_oracle(x[sel]) for x in w.train], [to_oracle(x[sel]) for x in w.rollout],
+                               w.v_ranges, ids, np.ones(rows.size, np.uint8))
+    for got, want in ((lt, ref.logp_train), (lr, ref.logp_rollout), (d, ref.dlogp), (plt, ref.logp_train)):
+        g = got[sel].cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g - want)) <= LOGP_ATOL
+    dd = d.cpu().numpy().astype(np.float64)
+    prop = oracle.metrics(dd, np.ones(w.n_rows, np.uint8))
+    prop["status"] = 0
+    assert_metrics_match(met, prop, dd, np.ones(w.n_rows, np.uint8), ambiguity=1e-6)
+    del w
+    torch.cuda.empty_cache()
