@@ -58,7 +58,7 @@ inline WsLayout ws_layout(int64_t n_rows, int n_seg) {
     L.header = off;    off += align256(sizeof(WsHeader));
     L.rowid = off;     off += align256(R * sizeof(int2));          // (row, token id) of active rows
     L.pick = off;      off += align256(R * sizeof(float2));        // selected logits (train, rollout)
-    L.part = off;      off += align256(R * size_t(n_seg) * kConsumerWarps * sizeof(float4));
+    L.part = off;      off += align256(R * size_t(n_seg) * kConsumerWarps * 2 * sizeof(float4));  // warp states
     L.dval = off;      off += align256(R * sizeof(double));        // dlogp per active row
     L.keys = off;      off += align256(R * sizeof(uint32_t));      // |dlogp| as fp32 bits
     L.blockpart = off; off += align256(((R + kFinThreads - 1) / kFinThreads) * sizeof(BlockPartial));

@@ -24,12 +24,39 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Same merge as the row kernel's butterfly (kept bit-identical on purpose).
-__device__ __forceinline__ void merge_pair(float &m, float &s, float mo, float so) {
-    const float mn = fmaxf(m, mo);
-    s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, mn), kLog2e))),
-                  __fmul_rn(so, ex2(__fmul_rn(__fsub_rn(mo, mn), kLog2e))));
-    m = mn;
+// Row state of one vocab range: train max and sum exp, the difference sum on
+// the train reference, rollout max and sum exp (the row kernel's per-warp
+// state).  The merge is the row kernel's butterfly merge, bit for bit.
+struct Acc {
+    float mt, st, dd, mr, sr;
+};
+
+__device__ __forceinline__ Acc acc_init() {
+    Acc a;
+    a.mt = -FLT_MAX;
+    a.mr = -FLT_MAX;
+    a.st = a.dd = a.sr = 0.f;
+    return a;
+}
+
+__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
+    const float mt = fmaxf(a.mt, b.mt);
+    const float fa = ex2(__fmul_rn(__fsub_rn(a.mt, mt), kLog2e));
+    const float fb = ex2(__fmul_rn(__fsub_rn(b.mt, mt), kLog2e));
+    a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
+    a.dd = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(b.dd, fb));
+    a.mt = mt;
+    const float mr = fmaxf(a.mr, b.mr);
+    a.sr = __fadd_rn(__fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, mr), kLog2e))),
+                     __fmul_rn(b.sr, ex2(__fmul_rn(__fsub_rn(b.mr, mr), kLog2e))));
+    a.mr = mr;
+}
+
+__device__ __forceinline__ double lse_train(const Acc &a) {
+    return static_cast<double>(a.mt) + log(static_cast<double>(a.st));
+}
+__device__ __forceinline__ double lse_rollout(const Acc &a) {
+    return static_cast<double>(a.mr) + log(static_cast<double>(a.sr));
 }
 
 // ---------------------------------------------------------------- stage 1
@@ -139,12 +166,15 @@ __device__ __forceinline__ void block_tree(Part *sh) {
     }
 }
 
-// One thread per active row: merge the 16 warp partials of each segment, then
+// One thread per active row: merge the 16 warp states of each segment, then
 // the segments in vocab order (and optionally in a given permutation), then
 // the per-row arithmetic in fp64:
 //   lse = m + log(s),  logp = x[id] - lse,
-//   dlogp = (x_t[id] - x_r[id]) - (m_t - m_r) - log1p((s_t - s_r) / s_r)
-// (the last form keeps dlogp accurate when both sides are nearly equal).
+//   dlogp = (x_t[id] - x_r[id]) + log1p(-dd / s_t)      when |dd| < s_t / 2,
+//   dlogp = (x_t[id] - x_r[id]) - (lse_t - lse_r)       otherwise.
+// Both are the same quantity; the first keeps dlogp accurate when the two rows
+// nearly agree (dd is the sum of the term differences), the second covers rows
+// far apart, where dlogp is large.
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_constant__ FinArgs a) {
     const int64_t n_active = a.hdr->n_active;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
@@ -162,43 +192,40 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
         if (a.out_perm_lr) a.out_perm_lr[r] = CUDART_NAN_F;
     } else {
         const float2 xs = a.pick[i];
-        float smt[kMaxSegments], sst[kMaxSegments], smr[kMaxSegments], ssr[kMaxSegments];
-        float mt = -FLT_MAX, st = 0.f, mr = -FLT_MAX, sr = 0.f;
+        Acc seg[kMaxSegments];
+        Acc row = acc_init();
         for (int k = 0; k < a.n_seg; ++k) {
-            float kmt = -FLT_MAX, kst = 0.f, kmr = -FLT_MAX, ksr = 0.f;
-            const float4 *pw = a.part + (i * a.n_seg + k) * kConsumerWarps;
-#pragma unroll
+            Acc sk = acc_init();
+            const float4 *pw = a.part + (i * a.n_seg + k) * kConsumerWarps * 2;
+#pragma unroll 4
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float4 q = pw[w];
-                merge_pair(kmt, kst, q.x, q.y);
-                merge_pair(kmr, ksr, q.z, q.w);
+                const float4 p0 = pw[2 * w], p1 = pw[2 * w + 1];
+                Acc o;
+                o.mt = p0.x;
+                o.st = p0.y;
+                o.dd = p0.z;
+                o.mr = p0.w;
+                o.sr = p1.x;
+                merge_acc(sk, o);
             }
-            smt[k] = kmt;
-            sst[k] = kst;
-            smr[k] = kmr;
-            ssr[k] = ksr;
-            merge_pair(mt, st, kmt, kst);  // global vocab-shard order
-            merge_pair(mr, sr, kmr, ksr);
+            seg[k] = sk;
+            merge_acc(row, sk);  // global vocab-shard order
         }
-        const double lse_t = static_cast<double>(mt) + log(static_cast<double>(st));
-        const double lse_r = static_cast<double>(mr) + log(static_cast<double>(sr));
+        const double lse_t = lse_train(row), lse_r = lse_rollout(row);
         const double xt = xs.x, xr = xs.y;
-        const double q = (static_cast<double>(st) - static_cast<double>(sr)) / static_cast<double>(sr);
-        d = ((xt - xr) - (static_cast<double>(mt) - static_cast<double>(mr))) - log1p(q);
+        const double st = row.st, dd = row.dd;
+        if (fabs(dd) < 0.5 * st)
+            d = (xt - xr) + log1p(-dd / st);
+        else
+            d = (xt - xr) - (lse_t - lse_r);
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
         if (a.out_lr) a.out_lr[r] = static_cast<float>(xr - lse_r);
         if (a.n_perm) {
-            float pmt = -FLT_MAX, pst = 0.f, pmr = -FLT_MAX, psr = 0.f;
-            for (int j = 0; j < a.n_perm; ++j) {
-                const int k = a.perm[j];
-                merge_pair(pmt, pst, smt[k], sst[k]);
-                merge_pair(pmr, psr, smr[k], ssr[k]);
-            }
-            if (a.out_perm_lt)
-                a.out_perm_lt[r] = static_cast<float>(xt - (static_cast<double>(pmt) + log(static_cast<double>(pst))));
-            if (a.out_perm_lr)
-                a.out_perm_lr[r] = static_cast<float>(xr - (static_cast<double>(pmr) + log(static_cast<double>(psr))));
+            Acc pr = acc_init();
+            for (int j = 0; j < a.n_perm; ++j) merge_acc(pr, seg[a.perm[j]]);
+            if (a.out_perm_lt) a.out_perm_lt[r] = static_cast<float>(xt - lse_train(pr));
+            if (a.out_perm_lr) a.out_perm_lr[r] = static_cast<float>(xr - lse_rollout(pr));
         }
     }
     if (a.out_d) a.out_d[r] = static_cast<float>(d);

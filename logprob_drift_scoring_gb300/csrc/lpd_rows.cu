@@ -13,9 +13,9 @@
 // cp.async.bulk, completion on an mbarrier); every stage holds the same 4096
 // columns of both sides.  16 consumer warps read the stage, and thread t owns
 // columns [4t, 4t+4) and [2048+4t, 2048+4t+4) of every tile.  Each thread keeps
-// an online (max m, sum s) pair per side in fp32; at the end of a segment each
-// warp merges its 32 pairs in a fixed butterfly and writes one pair per side
-// to the workspace.  The finalise kernel merges the 16 warp pairs, the
+// an online (max, sum exp) pair per side in fp32 plus the sum of the two
+// sides' term differences; at the end of a segment each warp merges its 32
+// states in a fixed butterfly and writes one state to the workspace.  The finalise kernel merges the 16 warp pairs, the
 // segments and does the fp64 row arithmetic.
 //
 // Batch invariance ("Attention Debug Matrix", section "Metrics": the
@@ -161,33 +161,79 @@ __device__ __forceinline__ int slot_col(int t, int q) {
 }
 
 // ---- the arithmetic (shared by every load path and dtype) ------------------
-// Online log-sum-exp of eight values into (m, s): s = sum exp(x - m).  The
-// chunk maximum is taken first, the running sum is rescaled at most once, and
-// the eight terms are added in a fixed pairwise tree.  Values of -inf (masked
-// tail columns) contribute exactly 0; the floor -FLT_MAX keeps (x - m) defined
-// for rows that are -inf everywhere.
-__device__ __forceinline__ void accumulate8(const float *v, float &m, float &s) {
-    const float cm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
-                           fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
-    if (cm > m) {
-        s = __fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
-        m = cm;
-    }
-    float e[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) e[q] = ex2(__fmul_rn(__fsub_rn(v[q], m), kLog2e));
-    const float t = __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
-                              __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
-    s = __fadd_rn(s, t);
+// Per-thread online state for one vocab segment of one row:
+//   mt, st  train side: running max and sum exp(x_t - mt)
+//   mr, sr  rollout side: running max and sum exp(x_r - mr)
+//   dd      sum (exp(x_t - mt) - exp(x_r - mt)), the difference of the two
+//           sides' terms on the train side's reference.
+// dd is what makes dlogp = (x_t[id] - x_r[id]) + log1p(-dd / st) accurate when
+// the two rows are nearly equal: identical logits contribute exactly zero, so
+// its rounding is relative to the difference itself, not to the full sums.
+struct Acc {
+    float mt, st, dd, mr, sr;
+};
+
+__device__ __forceinline__ Acc acc_init() {
+    Acc a;
+    a.mt = -FLT_MAX;
+    a.mr = -FLT_MAX;
+    a.st = a.dd = a.sr = 0.f;
+    return a;
 }
 
-// Merge (mo, so) into (m, s).  Symmetric in its two operands bit for bit
-// (max and IEEE addition commute), so a butterfly leaves every lane equal.
-__device__ __forceinline__ void merge_pair(float &m, float &s, float mo, float so) {
-    const float mn = fmaxf(m, mo);
-    s = __fadd_rn(__fmul_rn(s, ex2(__fmul_rn(__fsub_rn(m, mn), kLog2e))),
-                  __fmul_rn(so, ex2(__fmul_rn(__fsub_rn(mo, mn), kLog2e))));
-    m = mn;
+__device__ __forceinline__ float max8(const float *v) {
+    return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+}
+
+__device__ __forceinline__ float sum8(const float *e) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
+                     __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+}
+
+// Online log-sum-exp of eight columns of both sides into the state.  Each
+// side's chunk maximum is taken first and its running sums are rescaled at most
+// once; the eight terms are added in a fixed pairwise tree.  -inf columns
+// (masked tails) contribute exactly 0; the -FLT_MAX floor keeps (x - m)
+// defined for rows that are -inf everywhere.
+__device__ __forceinline__ void accumulate8(const float *vt, const float *vr, Acc &a) {
+    const float cmt = max8(vt), cmr = max8(vr);
+    if (cmt > a.mt) {
+        const float f = ex2(__fmul_rn(__fsub_rn(a.mt, cmt), kLog2e));
+        a.st = __fmul_rn(a.st, f);
+        a.dd = __fmul_rn(a.dd, f);
+        a.mt = cmt;
+    }
+    if (cmr > a.mr) {
+        a.sr = __fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, cmr), kLog2e)));
+        a.mr = cmr;
+    }
+    // rollout terms re-expressed on the train reference: exp(x_r - mt) = e_r * g
+    const float g = (a.mr == a.mt) ? 1.f : ex2(__fmul_rn(__fsub_rn(a.mr, a.mt), kLog2e));
+    float et[8], er[8], dq[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        et[q] = ex2(__fmul_rn(__fsub_rn(vt[q], a.mt), kLog2e));
+        er[q] = ex2(__fmul_rn(__fsub_rn(vr[q], a.mr), kLog2e));
+        dq[q] = __fmaf_rn(-er[q], g, et[q]);
+    }
+    a.st = __fadd_rn(a.st, sum8(et));
+    a.sr = __fadd_rn(a.sr, sum8(er));
+    a.dd = __fadd_rn(a.dd, sum8(dq));
+}
+
+// Merge state b into a.  Symmetric in a and b bit for bit (max and IEEE
+// addition commute), so a butterfly leaves every lane with the same value.
+__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
+    const float mt = fmaxf(a.mt, b.mt);
+    const float fa = ex2(__fmul_rn(__fsub_rn(a.mt, mt), kLog2e));
+    const float fb = ex2(__fmul_rn(__fsub_rn(b.mt, mt), kLog2e));
+    a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
+    a.dd = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(b.dd, fb));
+    a.mt = mt;
+    const float mr = fmaxf(a.mr, b.mr);
+    a.sr = __fadd_rn(__fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, mr), kLog2e))),
+                     __fmul_rn(b.sr, ex2(__fmul_rn(__fsub_rn(b.mr, mr), kLog2e))));
+    a.mr = mr;
 }
 
 __device__ __forceinline__ float select8(const float *v, int q) {
@@ -292,7 +338,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
             const Segment &sg = a.seg[k];
             const char *tb = sg.t + r * sg.t_stride;
             const char *rb = sg.r + r * sg.r_stride;
-            float mt = -FLT_MAX, st = 0.f, mr = -FLT_MAX, sr = 0.f;
+            Acc acc = acc_init();
             for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
                 const int nv = static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
                 float vt[8], vr[8];
@@ -337,21 +383,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 }
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
                     a.pick[i] = make_float2(select8(vt, pick_slot), select8(vr, pick_slot));
-                accumulate8(vt, mt, st);
-                accumulate8(vr, mr, sr);
+                accumulate8(vt, vr, acc);
             }
             // fixed butterfly over the warp
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                const float mto = __shfl_xor_sync(0xffffffffu, mt, off);
-                const float sto = __shfl_xor_sync(0xffffffffu, st, off);
-                const float mro = __shfl_xor_sync(0xffffffffu, mr, off);
-                const float sro = __shfl_xor_sync(0xffffffffu, sr, off);
-                merge_pair(mt, st, mto, sto);
-                merge_pair(mr, sr, mro, sro);
+                Acc o;
+                o.mt = __shfl_xor_sync(0xffffffffu, acc.mt, off);
+                o.st = __shfl_xor_sync(0xffffffffu, acc.st, off);
+                o.dd = __shfl_xor_sync(0xffffffffu, acc.dd, off);
+                o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
+                o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
+                merge_acc(acc, o);
             }
-            if (lane == 0)
-                a.part[(i * a.n_seg + k) * kConsumerWarps + warp] = make_float4(mt, st, mr, sr);
+            if (lane == 0) {
+                float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;
+                dst[0] = make_float4(acc.mt, acc.st, acc.dd, acc.mr);
+                dst[1] = make_float4(acc.sr, 0.f, 0.f, 0.f);
+            }
         }
     }
 }
