@@ -62,7 +62,8 @@ def measured_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha1()
-    for rel in KERNEL_SOURCES + ["logprob_drift_scoring_gb300/csrc/lpd_internal.cuh"]:
+    for rel in KERNEL_SOURCES + ["logprob_drift_scoring_gb300/csrc/lpd_internal.cuh",
+                                 "logprob_drift_scoring_gb300/csrc/lpd_acc.cuh"]:
         h.update((ROOT / rel).read_bytes())
     return h.hexdigest()[:12]
 

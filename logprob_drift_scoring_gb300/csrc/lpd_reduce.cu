@@ -13,44 +13,11 @@
 
 #include <math_constants.h>
 
+#include "lpd_acc.cuh"
 #include "lpd_internal.cuh"
 
 namespace lpd {
 namespace {
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Row state of one vocab range: train max and sum exp, the difference sum on
-// the train reference, rollout max and sum exp (the row kernel's per-warp
-// state).  The merge is the row kernel's butterfly merge, bit for bit.
-struct Acc {
-    float mt, st, dd, mr, sr;
-};
-
-__device__ __forceinline__ Acc acc_init() {
-    Acc a;
-    a.mt = -FLT_MAX;
-    a.mr = -FLT_MAX;
-    a.st = a.dd = a.sr = 0.f;
-    return a;
-}
-
-__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
-    const float mt = fmaxf(a.mt, b.mt);
-    const float fa = ex2(__fmul_rn(__fsub_rn(a.mt, mt), kLog2e));
-    const float fb = ex2(__fmul_rn(__fsub_rn(b.mt, mt), kLog2e));
-    a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
-    a.dd = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(b.dd, fb));
-    a.mt = mt;
-    const float mr = fmaxf(a.mr, b.mr);
-    a.sr = __fadd_rn(__fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, mr), kLog2e))),
-                     __fmul_rn(b.sr, ex2(__fmul_rn(__fsub_rn(b.mr, mr), kLog2e))));
-    a.mr = mr;
-}
 
 __device__ __forceinline__ double lse_train(const Acc &a) {
     return static_cast<double>(a.mt) + log(static_cast<double>(a.st));
@@ -170,11 +137,10 @@ __device__ __forceinline__ void block_tree(Part *sh) {
 // the segments in vocab order (and optionally in a given permutation), then
 // the per-row arithmetic in fp64:
 //   lse = m + log(s),  logp = x[id] - lse,
-//   dlogp = (x_t[id] - x_r[id]) + log1p(-dd / s_t)      when |dd| < s_t / 2,
-//   dlogp = (x_t[id] - x_r[id]) - (lse_t - lse_r)       otherwise.
-// Both are the same quantity; the first keeps dlogp accurate when the two rows
-// nearly agree (dd is the sum of the term differences), the second covers rows
-// far apart, where dlogp is large.
+//   dlogp = (x_t[id] - x_r[id]) - (m_t - m_r) + log(s_r / s_t),
+// with log(s_r / s_t) = log1p(-dd / s_t) when |dd| < s_t / 2 (dd = s_t - s_r
+// carried separately, see lpd_acc.cuh), which keeps dlogp accurate when the
+// two rows nearly agree and exactly 0 when they differ by a constant shift.
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_constant__ FinArgs a) {
     const int64_t n_active = a.hdr->n_active;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
@@ -213,11 +179,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
         }
         const double lse_t = lse_train(row), lse_r = lse_rollout(row);
         const double xt = xs.x, xr = xs.y;
-        const double st = row.st, dd = row.dd;
-        if (fabs(dd) < 0.5 * st)
-            d = (xt - xr) + log1p(-dd / st);
-        else
-            d = (xt - xr) - (lse_t - lse_r);
+        const double st = row.st, sr = row.sr, dd = row.dd;
+        const double l_ratio = fabs(dd) < 0.5 * st ? log1p(-dd / st) : log(sr / st);
+        d = ((xt - xr) - (static_cast<double>(row.mt) - static_cast<double>(row.mr))) + l_ratio;
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
         if (a.out_lr) a.out_lr[r] = static_cast<float>(xr - lse_r);

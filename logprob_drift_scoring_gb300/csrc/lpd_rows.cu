@@ -27,6 +27,7 @@
 // intrinsics so the compiler cannot contract it differently per dtype).
 #include <cfloat>
 
+#include "lpd_acc.cuh"
 #include "lpd_internal.cuh"
 
 namespace lpd {
@@ -50,13 +51,6 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-// 2^x on the special-function unit.
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // ---- mbarrier and bulk copy (inline PTX) ----------------------------------
@@ -161,26 +155,6 @@ __device__ __forceinline__ int slot_col(int t, int q) {
 }
 
 // ---- the arithmetic (shared by every load path and dtype) ------------------
-// Per-thread online state for one vocab segment of one row:
-//   mt, st  train side: running max and sum exp(x_t - mt)
-//   mr, sr  rollout side: running max and sum exp(x_r - mr)
-//   dd      sum (exp(x_t - mt) - exp(x_r - mt)), the difference of the two
-//           sides' terms on the train side's reference.
-// dd is what makes dlogp = (x_t[id] - x_r[id]) + log1p(-dd / st) accurate when
-// the two rows are nearly equal: identical logits contribute exactly zero, so
-// its rounding is relative to the difference itself, not to the full sums.
-struct Acc {
-    float mt, st, dd, mr, sr;
-};
-
-__device__ __forceinline__ Acc acc_init() {
-    Acc a;
-    a.mt = -FLT_MAX;
-    a.mr = -FLT_MAX;
-    a.st = a.dd = a.sr = 0.f;
-    return a;
-}
-
 __device__ __forceinline__ float max8(const float *v) {
     return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
 }
@@ -190,50 +164,34 @@ __device__ __forceinline__ float sum8(const float *e) {
                      __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
 }
 
-// Online log-sum-exp of eight columns of both sides into the state.  Each
-// side's chunk maximum is taken first and its running sums are rescaled at most
-// once; the eight terms are added in a fixed pairwise tree.  -inf columns
-// (masked tails) contribute exactly 0; the -FLT_MAX floor keeps (x - m)
-// defined for rows that are -inf everywhere.
+// Online log-sum-exp of eight columns of both sides into the state (see
+// lpd_acc.cuh).  Each side's chunk maximum is taken first and the sums are
+// rescaled at most once per chunk; the eight terms of each sum are added in a
+// fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
+// -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
 __device__ __forceinline__ void accumulate8(const float *vt, const float *vr, Acc &a) {
     const float cmt = max8(vt), cmr = max8(vr);
-    if (cmt > a.mt) {
-        const float f = ex2(__fmul_rn(__fsub_rn(a.mt, cmt), kLog2e));
-        a.st = __fmul_rn(a.st, f);
-        a.dd = __fmul_rn(a.dd, f);
-        a.mt = cmt;
+    if (cmt > a.mt || cmr > a.mr) {
+        const float nmt = fmaxf(a.mt, cmt), nmr = fmaxf(a.mr, cmr);
+        const float at = __fmul_rn(__fsub_rn(a.mt, nmt), kLog2e);
+        const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), kLog2e);
+        const float ft = ex2(at), fr = ex2(ar);
+        a.dd = __fadd_rn(__fmul_rn(a.dd, ft), __fmul_rn(a.sr, scale_diff(ft, fr, at, ar)));
+        a.st = __fmul_rn(a.st, ft);
+        a.sr = __fmul_rn(a.sr, fr);
+        a.mt = nmt;
+        a.mr = nmr;
     }
-    if (cmr > a.mr) {
-        a.sr = __fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, cmr), kLog2e)));
-        a.mr = cmr;
-    }
-    // rollout terms re-expressed on the train reference: exp(x_r - mt) = e_r * g
-    const float g = (a.mr == a.mt) ? 1.f : ex2(__fmul_rn(__fsub_rn(a.mr, a.mt), kLog2e));
     float et[8], er[8], dq[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         et[q] = ex2(__fmul_rn(__fsub_rn(vt[q], a.mt), kLog2e));
         er[q] = ex2(__fmul_rn(__fsub_rn(vr[q], a.mr), kLog2e));
-        dq[q] = __fmaf_rn(-er[q], g, et[q]);
+        dq[q] = __fsub_rn(et[q], er[q]);
     }
     a.st = __fadd_rn(a.st, sum8(et));
     a.sr = __fadd_rn(a.sr, sum8(er));
     a.dd = __fadd_rn(a.dd, sum8(dq));
-}
-
-// Merge state b into a.  Symmetric in a and b bit for bit (max and IEEE
-// addition commute), so a butterfly leaves every lane with the same value.
-__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
-    const float mt = fmaxf(a.mt, b.mt);
-    const float fa = ex2(__fmul_rn(__fsub_rn(a.mt, mt), kLog2e));
-    const float fb = ex2(__fmul_rn(__fsub_rn(b.mt, mt), kLog2e));
-    a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
-    a.dd = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(b.dd, fb));
-    a.mt = mt;
-    const float mr = fmaxf(a.mr, b.mr);
-    a.sr = __fadd_rn(__fmul_rn(a.sr, ex2(__fmul_rn(__fsub_rn(a.mr, mr), kLog2e))),
-                     __fmul_rn(b.sr, ex2(__fmul_rn(__fsub_rn(b.mr, mr), kLog2e))));
-    a.mr = mr;
 }
 
 __device__ __forceinline__ float select8(const float *v, int q) {

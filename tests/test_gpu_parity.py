@@ -106,6 +106,20 @@ def test_bf16_against_its_fp32_upcast_is_bitwise_zero():
     assert torch.equal(res.logp_train, res.logp_rollout)
 
 
+def test_constant_shift_gives_exact_zero():
+    # a rollout that is the train logits plus a constant has the same
+    # distribution: logp is identical and dlogp must be exactly zero
+    w = W.synthetic(120, 3 * 4096 + 520, seed=14, device=DEV, dtype_rollout=torch.float32)
+    shifted = (w.train.float() + 0.75).contiguous()
+    assert torch.equal(shifted - 0.75, w.train.float())
+    res = run(w.train, shifted, w.token_ids, w.action_mask)
+    assert torch.all(res.dlogp == 0)
+    m = res.metrics
+    assert m["approx_kl0"] == 0.0 and m["mean_abs_dlogp"] == 0.0 and m["ratio0_mean"] == 1.0
+    ref = oracle_score(w.train, shifted, w.token_ids, w.action_mask)
+    assert np.max(np.abs(ref.dlogp)) < 1e-12
+
+
 def _embed(rows_t, rows_r, ids, n_total, offset, seed):
     """Place the given rows at [offset, offset+k) of a bigger batch whose other
     rows are inactive garbage (padding on either side)."""
