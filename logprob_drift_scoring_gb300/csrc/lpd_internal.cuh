@@ -6,22 +6,24 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/lpd.h"
+#include "lpd.h"
 
 namespace lpd {
 
 // ---------------------------------------------------------------- geometry
 // The streaming row kernel runs one CTA per SM: 16 consumer warps plus one
-// producer warp.  A tile is 4096 logical columns of one vocab segment; consumer
-// thread t owns columns [4t, 4t+4) and [2048+4t, 2048+4t+4) of every tile.
+// producer warp.  A tile is 8192 logical columns of one vocab segment, read as
+// four groups of 2048; consumer thread t owns columns [2048 g + 4t, 2048 g + 4t
+// + 4) of group g = 0..3 of every tile (16 columns per thread per tile).
 // These constants fix each row's arithmetic order, so they are part of the
 // batch-invariance contract: changing them changes results (bitwise), but never
 // makes them depend on the batch.
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;  // 512
 constexpr int kRowThreads = kConsumers + 32;     // + producer warp
-constexpr int kTile = 8 * kConsumers;            // 4096 columns
-constexpr int kHalfTile = kTile / 2;
+constexpr int kColsPerThread = 16;
+constexpr int kGroupCols = 4 * kConsumers;       // 2048
+constexpr int kTile = kColsPerThread * kConsumers;  // 8192 columns
 constexpr int kMaxSegments = 16;                 // shards per side
 constexpr int kRingBytes = 192 * 1024;           // shared-memory staging ring
 constexpr int kFinThreads = 256;                 // rows per finalise block

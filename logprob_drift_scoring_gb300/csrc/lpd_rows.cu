@@ -129,75 +129,139 @@ __device__ __forceinline__ float lds_elem<F32>(const char *stage, int col) {
     return *reinterpret_cast<const float *>(stage + 4 * col);
 }
 
-// Four consecutive columns starting at `col` (a multiple of 4) of a stage.
-template <class D>
-__device__ __forceinline__ void lds4(const char *stage, int col, float *v);
-template <>
-__device__ __forceinline__ void lds4<Bf16>(const char *stage, int col, float *v) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(stage + 2 * col);
-    v[0] = bf16_lo(w.x);
-    v[1] = bf16_hi(w.x);
-    v[2] = bf16_lo(w.y);
-    v[3] = bf16_hi(w.y);
+// ---- packed fp32 pairs ------------------------------------------------------
+// Two fp32 values in one 64-bit register pair, operated on with the f32x2
+// instructions.  Each half is rounded exactly like the scalar .rn operation, so
+// packing changes the instruction count, not the arithmetic.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2(float a, float b) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
 }
-template <>
-__device__ __forceinline__ void lds4<F32>(const char *stage, int col, float *v) {
-    const float4 w = *reinterpret_cast<const float4 *>(stage + 4 * col);
-    v[0] = w.x;
-    v[1] = w.y;
-    v[2] = w.z;
-    v[3] = w.w;
+__device__ __forceinline__ float f2_lo(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t ex2_2(f2_t a) { return f2(ex2(f2_lo(a)), ex2(f2_hi(a))); }
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
-// Column owned by slot q (0..7) of consumer thread t within a tile.
-__device__ __forceinline__ int slot_col(int t, int q) {
-    return q < 4 ? 4 * t + q : kHalfTile + 4 * t + (q - 4);
+// Four consecutive columns starting at `col` (a multiple of 4) of a stage, as
+// two packed pairs.
+template <class D>
+__device__ __forceinline__ void lds4(const char *stage, int col, f2_t *v);
+template <>
+__device__ __forceinline__ void lds4<Bf16>(const char *stage, int col, f2_t *v) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(stage + 2 * col);
+    v[0] = f2(bf16_lo(w.x), bf16_hi(w.x));
+    v[1] = f2(bf16_lo(w.y), bf16_hi(w.y));
 }
+template <>
+__device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
+    const float4 w = *reinterpret_cast<const float4 *>(stage + 4 * col);
+    v[0] = f2(w.x, w.y);
+    v[1] = f2(w.z, w.w);
+}
+
+// Column of slot q (0..15) of consumer thread t within a tile.
+__device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroupCols + 4 * t + (q & 3); }
 
 // ---- the arithmetic (shared by every load path and dtype) ------------------
-__device__ __forceinline__ float max8(const float *v) {
-    return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+// Streaming form of the state of lpd_acc.cuh: the three sums are kept as
+// packed (even column, odd column) pairs, folded into one Acc at the end of a
+// segment.
+struct Acc2 {
+    float mt, mr;
+    f2_t st, sr, dd;
+};
+
+__device__ __forceinline__ Acc2 acc2_init() {
+    Acc2 a;
+    a.mt = -FLT_MAX;
+    a.mr = -FLT_MAX;
+    a.st = a.sr = a.dd = f2(0.f, 0.f);
+    return a;
 }
 
-__device__ __forceinline__ float sum8(const float *e) {
-    return __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
-                     __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+__device__ __forceinline__ Acc acc2_fold(const Acc2 &a) {
+    Acc r;
+    r.mt = a.mt;
+    r.mr = a.mr;
+    r.st = __fadd_rn(f2_lo(a.st), f2_hi(a.st));
+    r.sr = __fadd_rn(f2_lo(a.sr), f2_hi(a.sr));
+    r.dd = __fadd_rn(f2_lo(a.dd), f2_hi(a.dd));
+    return r;
 }
 
-// Online log-sum-exp of eight columns of both sides into the state (see
+__device__ __forceinline__ float max16(const f2_t *v) {
+    const float a = max3(f2_lo(v[0]), f2_hi(v[0]), f2_lo(v[1]));
+    const float b = max3(f2_hi(v[1]), f2_lo(v[2]), f2_hi(v[2]));
+    const float c = max3(f2_lo(v[3]), f2_hi(v[3]), f2_lo(v[4]));
+    const float d = max3(f2_hi(v[4]), f2_lo(v[5]), f2_hi(v[5]));
+    const float e = max3(f2_lo(v[6]), f2_hi(v[6]), f2_lo(v[7]));
+    return fmaxf(max3(a, b, c), max3(d, e, f2_hi(v[7])));
+}
+
+// Fixed pairwise tree over eight packed pairs.
+__device__ __forceinline__ f2_t tree8(const f2_t *e) {
+    return add2(add2(add2(e[0], e[1]), add2(e[2], e[3])), add2(add2(e[4], e[5]), add2(e[6], e[7])));
+}
+
+// Online log-sum-exp of sixteen columns of both sides into the state (see
 // lpd_acc.cuh).  Each side's chunk maximum is taken first and the sums are
-// rescaled at most once per chunk; the eight terms of each sum are added in a
+// rescaled at most once per chunk; the sixteen terms of each sum are added in a
 // fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
 // -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
-__device__ __forceinline__ void accumulate8(const float *vt, const float *vr, Acc &a) {
-    const float cmt = max8(vt), cmr = max8(vr);
+__device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a) {
+    const float cmt = max16(vt), cmr = max16(vr);
     if (cmt > a.mt || cmr > a.mr) {
         const float nmt = fmaxf(a.mt, cmt), nmr = fmaxf(a.mr, cmr);
         const float at = __fmul_rn(__fsub_rn(a.mt, nmt), kLog2e);
         const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), kLog2e);
         const float ft = ex2(at), fr = ex2(ar);
-        a.dd = __fadd_rn(__fmul_rn(a.dd, ft), __fmul_rn(a.sr, scale_diff(ft, fr, at, ar)));
-        a.st = __fmul_rn(a.st, ft);
-        a.sr = __fmul_rn(a.sr, fr);
+        const float corr = scale_diff(ft, fr, at, ar);
+        a.dd = add2(mul2(a.dd, f2(ft, ft)), mul2(a.sr, f2(corr, corr)));
+        a.st = mul2(a.st, f2(ft, ft));
+        a.sr = mul2(a.sr, f2(fr, fr));
         a.mt = nmt;
         a.mr = nmr;
     }
-    float et[8], er[8], dq[8];
+    const f2_t mt2 = f2(a.mt, a.mt), mr2 = f2(a.mr, a.mr), l2 = f2(kLog2e, kLog2e);
+    f2_t et[8], er[8], dq[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        et[q] = ex2(__fmul_rn(__fsub_rn(vt[q], a.mt), kLog2e));
-        er[q] = ex2(__fmul_rn(__fsub_rn(vr[q], a.mr), kLog2e));
-        dq[q] = __fsub_rn(et[q], er[q]);
+    for (int p = 0; p < 8; ++p) {
+        et[p] = ex2_2(mul2(sub2(vt[p], mt2), l2));
+        er[p] = ex2_2(mul2(sub2(vr[p], mr2), l2));
+        dq[p] = sub2(et[p], er[p]);
     }
-    a.st = __fadd_rn(a.st, sum8(et));
-    a.sr = __fadd_rn(a.sr, sum8(er));
-    a.dd = __fadd_rn(a.dd, sum8(dq));
+    a.st = add2(a.st, tree8(et));
+    a.sr = add2(a.sr, tree8(er));
+    a.dd = add2(a.dd, tree8(dq));
 }
 
-__device__ __forceinline__ float select8(const float *v, int q) {
-    float x = v[0];
+__device__ __forceinline__ float select16(const f2_t *v, int q) {
+    float x = f2_lo(v[0]);
 #pragma unroll
-    for (int k = 1; k < 8; ++k) x = (q == k) ? v[k] : x;
+    for (int k = 1; k < 16; ++k) x = (q == k) ? ((k & 1) ? f2_hi(v[k >> 1]) : f2_lo(v[k >> 1])) : x;
     return x;
 }
 
@@ -287,8 +351,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     const int pos = static_cast<int>(c % kTile);
                     pick_seg = k;
                     pick_c0 = c - pos;
-                    pick_slot = (pos / kHalfTile) * 4 + (pos & 3);
-                    pick_mine = ((pos % kHalfTile) >> 2) == t;
+                    pick_slot = (pos / kGroupCols) * 4 + (pos & 3);
+                    pick_mine = ((pos % kGroupCols) >> 2) == t;
                 }
             }
         }
@@ -296,10 +360,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
             const Segment &sg = a.seg[k];
             const char *tb = sg.t + r * sg.t_stride;
             const char *rb = sg.r + r * sg.r_stride;
-            Acc acc = acc_init();
+            Acc2 acc2 = acc2_init();
             for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
                 const int nv = static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
-                float vt[8], vr[8];
+                f2_t vt[8], vr[8];  // slots (2p, 2p+1) in pair p
                 if (kTma) {
                     const uint32_t stage = it % n_stages, round = it / n_stages;
                     // the whole warp leaves together if any lane gave up, so no
@@ -308,24 +372,31 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     if (__any_sync(0xffffffffu, !ok)) return;
                     const char *stg = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
                     if (nv == kTile) {
-                        lds4<DT>(stg, 4 * t, vt);
-                        lds4<DT>(stg, kHalfTile + 4 * t, vt + 4);
-                        lds4<DR>(stg + kStageT, 4 * t, vr);
-                        lds4<DR>(stg + kStageT, kHalfTile + 4 * t, vr + 4);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
+                            lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
+                        }
                     } else {
                         // ragged last tile: the bulk copy moved whole 16-byte
                         // units; the few columns after them come from global
                         const int nbt = static_cast<int>((static_cast<uint32_t>(nv * DT::kBytes) & ~15u) / DT::kBytes);
                         const int nbr = static_cast<int>((static_cast<uint32_t>(nv * DR::kBytes) & ~15u) / DR::kBytes);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int col = slot_col(t, q);
-                            vt[q] = col < nbt ? lds_elem<DT>(stg, col)
-                                  : col < nv  ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes)
-                                              : -INFINITY;
-                            vr[q] = col < nbr ? lds_elem<DR>(stg + kStageT, col)
-                                  : col < nv  ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes)
-                                              : -INFINITY;
+                        for (int p = 0; p < 8; ++p) {
+                            float x[2], y[2];
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int col = slot_col(t, 2 * p + h);
+                                x[h] = col < nbt ? lds_elem<DT>(stg, col)
+                                     : col < nv  ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes)
+                                                 : -INFINITY;
+                                y[h] = col < nbr ? lds_elem<DR>(stg + kStageT, col)
+                                     : col < nv  ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes)
+                                                 : -INFINITY;
+                            }
+                            vt[p] = f2(x[0], x[1]);
+                            vr[p] = f2(y[0], y[1]);
                         }
                     }
                     __syncwarp();
@@ -333,16 +404,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     ++it;
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int col = slot_col(t, q);
-                        vt[q] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
-                        vr[q] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
+                    for (int p = 0; p < 8; ++p) {
+                        float x[2], y[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = slot_col(t, 2 * p + h);
+                            x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
+                            y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
+                        }
+                        vt[p] = f2(x[0], x[1]);
+                        vr[p] = f2(y[0], y[1]);
                     }
                 }
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
-                    a.pick[i] = make_float2(select8(vt, pick_slot), select8(vr, pick_slot));
-                accumulate8(vt, vr, acc);
+                    a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
+                accumulate16(vt, vr, acc2);
             }
+            Acc acc = acc2_fold(acc2);
             // fixed butterfly over the warp
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {

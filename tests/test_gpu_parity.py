@@ -109,14 +109,19 @@ def test_bf16_against_its_fp32_upcast_is_bitwise_zero():
 def test_constant_shift_gives_exact_zero():
     # a rollout that is the train logits plus a constant has the same
     # distribution: logp is identical and dlogp must be exactly zero
-    w = W.synthetic(120, 3 * 4096 + 520, seed=14, device=DEV, dtype_rollout=torch.float32)
-    shifted = (w.train.float() + 0.75).contiguous()
-    assert torch.equal(shifted - 0.75, w.train.float())
-    res = run(w.train, shifted, w.token_ids, w.action_mask)
+    # (values on a 1/16 grid in [-8, 8): exact in bf16, and exact after the shift)
+    w = W.synthetic(120, 3 * 4096 + 520, seed=14, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(14)
+    grid = torch.randint(-127, 128, (w.n_rows, w.vocab), generator=g, device=DEV).float() / 16
+    train = grid.to(torch.bfloat16)
+    assert torch.equal(train.float(), grid)
+    shifted = (grid + 0.75).contiguous()
+    assert torch.equal(shifted - 0.75, grid)
+    res = run(train, shifted, w.token_ids, w.action_mask)
     assert torch.all(res.dlogp == 0)
     m = res.metrics
     assert m["approx_kl0"] == 0.0 and m["mean_abs_dlogp"] == 0.0 and m["ratio0_mean"] == 1.0
-    ref = oracle_score(w.train, shifted, w.token_ids, w.action_mask)
+    ref = oracle_score(train, shifted, w.token_ids, w.action_mask)
     assert np.max(np.abs(ref.dlogp)) < 1e-12
 
 
