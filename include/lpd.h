@@ -233,6 +233,32 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* ---- scoring without a caller-provided workspace -------------------------- */
+
+/* Largest n_rows lpd_score_noalloc accepts: its built-in scratch is sized for
+ * this many rows (about 17.7 MB of device memory per GPU that loads the
+ * library, held until the process exits). */
+#define LPD_NOALLOC_MAX_ROWS 32768
+
+/* lpd_score without the workspace argument, for callers that cannot allocate
+ * device memory (for example code running inside another engine whose caching
+ * allocator owns the device, or a plugin host that hands out only a stream and
+ * the tensors).  The pages have no counterpart to this entry point.
+ *
+ * Arguments, outputs and results are those of lpd_score; the workspace comes
+ * from a fixed array inside the library.  Returns LPD_ERR_UNSUPPORTED when
+ * n_rows > LPD_NOALLOC_MAX_ROWS, before touching the GPU.  It allocates
+ * nothing.  The first call on each device (with that device current) looks up
+ * the array's address, so make that first call before any stream capture on
+ * the device.  All calls on a device share the array and it keeps the previous
+ * call's contents (nothing in it needs to start at zero); calls whose work
+ * overlaps on the GPU race on it, so order them on one stream. */
+int lpd_score_noalloc(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows,
+                      int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask,
+                      double clip_lo, double clip_hi, float *out_logp_train,
+                      float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
+                      void *stream);
+
 #ifdef __cplusplus
 }
 #endif

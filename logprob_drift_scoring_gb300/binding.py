@@ -64,7 +64,8 @@ METRICS_BYTES = ctypes.sizeof(LpdMetrics)
 
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
-            "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded")
+            "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc")
+LPD_NOALLOC_MAX_ROWS = 32768
 
 
 class LpdError(RuntimeError):
@@ -99,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_drift_metrics.argtypes = [I64, D, D, P, P, SZ, P]
         L.lpd_score_sharded.restype = ctypes.c_int
         L.lpd_score_sharded.argtypes = [P, P, I32, I64, I64, P, P, D, D, P, P, P, P, P, P, P, P, SZ, P]
+        L.lpd_score_noalloc.restype = ctypes.c_int
+        L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
         _LIB = L
     return _LIB
 
@@ -216,6 +219,17 @@ def lpd_score_sharded(train_shards, rollout_shards, v_ranges, token_ids, action_
                                  _ptr(out_dlogp), _ptr(out_perm_logp_train), _ptr(out_perm_logp_rollout),
                                  _ptr(out_metrics), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "lpd_score_sharded")
+
+
+def lpd_score_noalloc(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
+                      out_dlogp, out_metrics, stream=None) -> None:
+    """lpd_score with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory; n_rows <= 32768)."""
+    t, r = logits_struct(train), logits_struct(rollout)
+    rc = lib().lpd_score_noalloc(ctypes.byref(t), ctypes.byref(r), train.shape[0], train.shape[1], _ptr(token_ids),
+                                 _ptr(action_mask), float(clip_lo), float(clip_hi), _ptr(out_logp_train),
+                                 _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics), _stream(stream))
+    _check(rc, "lpd_score_noalloc")
 
 
 # ---- convenience: allocate with torch, call, read back ------------------------

@@ -51,9 +51,9 @@ struct WsLayout {
     size_t header, rowid, pick, part, dval, keys, blockpart, total;
 };
 
-inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int64_t n_rows, int n_seg) {
+constexpr WsLayout ws_layout(int64_t n_rows, int n_seg) {
     WsLayout L{};
     size_t off = 0;
     const size_t R = size_t(n_rows);
