@@ -30,11 +30,11 @@ __device__ __forceinline__ double lse_rollout(const Acc &a) {
 // One CTA walks the mask in chunks of 16384 rows (16 consecutive rows per
 // thread), block-scans the per-thread counts and writes the (row, token id)
 // pairs of active rows in row order.
-__global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, const uint8_t *mask,
-                                                             const int32_t *ids, float *out_lt,
-                                                             float *out_lr, float *out_d,
-                                                             lpd_metrics *metrics, WsHeader *hdr,
-                                                             int2 *rowid) {
+__global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, const uint8_t *__restrict__ mask,
+                                                             const int32_t *__restrict__ ids,
+                                                             float *__restrict__ out_lt, float *__restrict__ out_lr,
+                                                             float *__restrict__ out_d, lpd_metrics *metrics,
+                                                             WsHeader *hdr, int2 *__restrict__ rowid) {
     __shared__ int warp_excl[32];
     __shared__ int chunk_total;
     __shared__ long long base;
@@ -43,20 +43,25 @@ __global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, con
     __syncthreads();
     for (int64_t chunk = 0; chunk < n_rows; chunk += 1024 * 16) {
         const int64_t r0 = chunk + static_cast<int64_t>(tid) * 16;
+        // all of this thread's loads first (independent), then the stores
+        uint8_t mk[16];
+        int32_t idv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) mk[q] = (r0 + q < n_rows) ? mask[r0 + q] : 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) idv[q] = mk[q] ? ids[r0 + q] : 0;
         uint32_t bits = 0;
         int cnt = 0;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             const int64_t r = r0 + q;
-            if (r < n_rows) {
-                if (mask[r]) {
-                    bits |= 1u << q;
-                    ++cnt;
-                } else {
-                    if (out_lt) out_lt[r] = 0.f;
-                    if (out_lr) out_lr[r] = 0.f;
-                    if (out_d) out_d[r] = 0.f;
-                }
+            if (mk[q]) {
+                bits |= 1u << q;
+                ++cnt;
+            } else if (r < n_rows) {
+                if (out_lt) out_lt[r] = 0.f;
+                if (out_lr) out_lr[r] = 0.f;
+                if (out_d) out_d[r] = 0.f;
             }
         }
         int incl = cnt;
@@ -82,10 +87,7 @@ __global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, con
         int64_t pos = base + warp_excl[warp] + (incl - cnt);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-            if (bits >> q & 1u) {
-                const int64_t r = r0 + q;
-                rowid[pos++] = make_int2(static_cast<int>(r), ids[r]);
-            }
+            if (bits >> q & 1u) rowid[pos++] = make_int2(static_cast<int>(r0 + q), idv[q]);
         }
         __syncthreads();
         if (tid == 0) base += chunk_total;
@@ -279,11 +281,22 @@ __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, 
             if (tid < 512) (&hist[0][0])[tid] = 0;
             __syncthreads();
             const uint32_t p0 = prefix[0], p1 = prefix[1];
-            for (int64_t i = tid; i < n_active; i += kSelThreads) {
-                const uint32_t key = keys[i];
+            // |dlogp| keys crowd into few digits, so lanes of a warp that hold
+            // the same digit are counted together (one shared atomic per group)
+            for (int64_t base = 0; base < n_active; base += kSelThreads) {
+                const int64_t i = base + tid;
+                const bool valid = i < n_active;
+                const uint32_t key = valid ? keys[i] : 0u;
                 const uint32_t dig = (key >> shift) & 255u;
-                if ((key & hi_mask) == p0) atomicAdd(&hist[0][dig], 1u);
-                if ((key & hi_mask) == p1) atomicAdd(&hist[1][dig], 1u);
+#pragma unroll
+                for (int tgt = 0; tgt < 2; ++tgt) {
+                    const bool in = valid && (key & hi_mask) == (tgt == 0 ? p0 : p1);
+                    const unsigned members = __ballot_sync(0xffffffffu, in);
+                    if (in) {
+                        const unsigned grp = __match_any_sync(members, dig);
+                        if (lane == __ffs(grp) - 1) atomicAdd(&hist[tgt][dig], static_cast<uint32_t>(__popc(grp)));
+                    }
+                }
             }
             __syncthreads();
             if (warp < 2) {
