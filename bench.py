@@ -42,6 +42,7 @@ CONFIGS = {
     "llama": dict(workload="llama-vocab B=64 T=1024 V=128256 bf16/fp32", vocab=128256),
     "sharded": dict(workload="vocab-sharded B=1 T=32768 V=151936 (4 shards) bf16/bf16", vocab=151936),
     "tiny": dict(workload="tiny B=2 T=64 V=1024 bf16/bf16", vocab=1024),
+    "fused": dict(workload="fused LM head: 16384 tokens x H=4096, W [151936, 4096] bf16", vocab=151936),
 }
 METRIC = "active tokens/sec scored; achieved HBM GB/s vs GB300 peak (logp+drift pass)"
 UNIT = "active_tokens/s"
@@ -164,6 +165,8 @@ def make_workload(config: str, device, seed_offset: int = 0, batch=None, seq=Non
         return W.sharded(seed=3 + seed_offset, device=device, seq=seq or 32768)
     if config == "tiny":
         return W.tiny(seed=0 + seed_offset, device=device)
+    if config == "fused":
+        return W.fused(seed=4 + seed_offset, device=device, rows=seq or 16384)
     raise SystemExit(f"unknown config {config}")
 
 
@@ -279,6 +282,66 @@ def time_cpu_oracle(config: str, target_s: float = 12.0, max_rows: int = 4096, s
             "sample": f"{n} active rows of the {config} recipe, both sides, float64 serial C, {elapsed:.1f} s"}
 
 
+def measured_tflops() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"tflops": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured sustained"}
+    return {"tflops": 1700.0, "source": "fallback sustained"}
+
+
+def run_fused(args, w, world, rank):
+    """The fused LM-head path: one lpd_score_fused call per step."""
+    import torch
+    from logprob_drift_scoring_gb300 import binding as B
+
+    dev = w.token_ids.device
+    n = w.n_rows
+    outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=dev)
+    ws = torch.empty(B.lpd_fused_workspace_size(n, w.hidden, w.vocab), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.lpd_score_fused(w.hidden_train, w.hidden_rollout, w.weight, w.token_ids, w.action_mask, *w.clip, *outs,
+                          met, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            step()
+        stop.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = barrier_max(start.elapsed_time(stop) / args.steps, world)
+    n_active = int(w.action_mask.sum().item())
+    flops = 2.0 * 2.0 * n_active * w.hidden * w.vocab  # both sides
+    peak = measured_tflops()
+    achieved = flops / (ms / 1e3) / 1e12
+    if rank != 0:
+        return None
+    out = {
+        "metric": METRIC, "value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": CONFIGS["fused"]["workload"], "rows": n, "active_tokens": n_active,
+                   "hidden": w.hidden, "vocab": w.vocab, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak["tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peak["tflops"], 4), "traffic": None,
+                     "peak_source": f"{peak['source']} bf16 GEMM", "span": "whole lpd_score_fused call",
+                     "algorithmic_flops_per_launch": flops},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * args.steps, "clocks": clocks.summary(),
+        "impl": "lpd",
+    }
+    print(json.dumps(out), flush=True)
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -293,6 +356,13 @@ def run_ours(args):
 
     B.lib()  # fail loudly here if the CUDA library is missing
     w = make_workload(args.config, dev, seed_offset=rank, batch=args.batch, seq=args.seq)
+    if args.config == "fused":
+        out = run_fused(args, w, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return out
     runner = Runner(w)
     n_active = int(w.action_mask.sum().item())
     bpt = bytes_per_active_token(w)

@@ -233,6 +233,31 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* Fused LM-head scoring ("[WS2] Framework for ablation experiment", LogProb
+ * knobs table, rows 9-10: the head GEMM and its fusion tiling).  The logits
+ * x_side[r, v] = sum_k hidden_side[r, k] * W[v, k] are formed tile by tile on
+ * the tensor cores (bf16 inputs, fp32 accumulation in a fixed k order, no
+ * split-K) and folded into an online log-sum-exp as they are produced; they are
+ * never written to memory.  Per-token outputs, metrics, status and errors are
+ * those of lpd_score.
+ *
+ * hidden_train, hidden_rollout  device bf16 [n_rows, hidden], row-major, dense.
+ * W                             device bf16 [vocab, hidden], row-major, dense.
+ * hidden must be a multiple of 64 and the three pointers 16-byte aligned, else
+ * LPD_ERR_ALIGNMENT.
+ * workspace        lpd_fused_workspace_size(n_rows, hidden, vocab) bytes,
+ *                  256-byte aligned (holds the active hidden rows of both sides
+ *                  densely and one 20-byte partial per active row and 256-wide
+ *                  vocab tile). */
+size_t lpd_fused_workspace_size(int64_t n_rows, int64_t hidden, int64_t vocab);
+
+int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const void *W,
+                    int64_t n_rows, int64_t hidden, int64_t vocab, const int32_t *token_ids,
+                    const uint8_t *action_mask, double clip_lo, double clip_hi,
+                    float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
+                    lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
 /* ---- scoring without a caller-provided workspace -------------------------- */
 
 /* Largest n_rows lpd_score_noalloc accepts: its built-in scratch is sized for

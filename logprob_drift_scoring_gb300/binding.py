@@ -64,7 +64,8 @@ METRICS_BYTES = ctypes.sizeof(LpdMetrics)
 
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
-            "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc")
+            "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
+            "lpd_fused_workspace_size", "lpd_score_fused")
 LPD_NOALLOC_MAX_ROWS = 32768
 
 
@@ -100,6 +101,10 @@ def lib() -> ctypes.CDLL:
         L.lpd_drift_metrics.argtypes = [I64, D, D, P, P, SZ, P]
         L.lpd_score_sharded.restype = ctypes.c_int
         L.lpd_score_sharded.argtypes = [P, P, I32, I64, I64, P, P, D, D, P, P, P, P, P, P, P, P, SZ, P]
+        L.lpd_fused_workspace_size.restype = SZ
+        L.lpd_fused_workspace_size.argtypes = [I64, I64, I64]
+        L.lpd_score_fused.restype = ctypes.c_int
+        L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
         _LIB = L
@@ -221,6 +226,20 @@ def lpd_score_sharded(train_shards, rollout_shards, v_ranges, token_ids, action_
     _check(rc, "lpd_score_sharded")
 
 
+def lpd_fused_workspace_size(n_rows: int, hidden: int, vocab: int) -> int:
+    return int(lib().lpd_fused_workspace_size(n_rows, hidden, vocab))
+
+
+def lpd_score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip_lo, clip_hi, out_logp_train,
+                    out_logp_rollout, out_dlogp, out_metrics, workspace, stream=None) -> None:
+    n_rows, hidden = hidden_train.shape
+    rc = lib().lpd_score_fused(_ptr(hidden_train), _ptr(hidden_rollout), _ptr(W), n_rows, hidden, W.shape[0],
+                               _ptr(token_ids), _ptr(action_mask), float(clip_lo), float(clip_hi),
+                               _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics),
+                               _ptr(workspace), workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(rc, "lpd_score_fused")
+
+
 def lpd_score_noalloc(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
                       out_dlogp, out_metrics, stream=None) -> None:
     """lpd_score with the library's built-in scratch instead of a workspace
@@ -238,6 +257,20 @@ def read_metrics(buf) -> dict:
     """Copy a device lpd_metrics record (uint8 tensor) to the host as a dict."""
     host = buf.detach().to("cpu", copy=True).numpy().tobytes()
     return LpdMetrics.from_buffer_copy(host).as_dict()
+
+
+def score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip=(0.8, 1.2), stream=None):
+    """Allocate outputs and workspace with torch, run lpd_score_fused."""
+    import torch
+
+    dev = hidden_train.device
+    n = hidden_train.shape[0]
+    outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
+    ws = torch.empty(lpd_fused_workspace_size(n, hidden_train.shape[1], W.shape[0]), dtype=torch.uint8, device=dev)
+    lpd_score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip[0], clip[1], *outs, met, ws,
+                    stream=stream)
+    return ScoreResult(outs[0], outs[1], outs[2], read_metrics(met))
 
 
 @dataclass

@@ -77,4 +77,113 @@ __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
     a.mr = mr;
 }
 
+// ---- packed fp32 pairs ---------------------------------------------------------
+// Two fp32 values in one 64-bit register pair, operated on with the f32x2
+// instructions.  Each half is rounded exactly like the scalar .rn operation, so
+// packing changes the instruction count, not the arithmetic.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2(float a, float b) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+    f2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2_t ex2_2(f2_t a) { return f2(ex2(f2_lo(a)), ex2(f2_hi(a))); }
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// ---- streaming form (row kernel and fused epilogue) -------------------------------
+// Streaming form of the state of lpd_acc.cuh: the three sums are kept as
+// packed (even column, odd column) pairs, folded into one Acc at the end of a
+// segment.
+struct Acc2 {
+    float mt, mr;
+    f2_t st, sr, dd;
+};
+
+__device__ __forceinline__ Acc2 acc2_init() {
+    Acc2 a;
+    a.mt = -FLT_MAX;
+    a.mr = -FLT_MAX;
+    a.st = a.sr = a.dd = f2(0.f, 0.f);
+    return a;
+}
+
+__device__ __forceinline__ Acc acc2_fold(const Acc2 &a) {
+    Acc r;
+    r.mt = a.mt;
+    r.mr = a.mr;
+    r.st = __fadd_rn(f2_lo(a.st), f2_hi(a.st));
+    r.sr = __fadd_rn(f2_lo(a.sr), f2_hi(a.sr));
+    r.dd = __fadd_rn(f2_lo(a.dd), f2_hi(a.dd));
+    return r;
+}
+
+__device__ __forceinline__ float max16(const f2_t *v) {
+    const float a = max3(f2_lo(v[0]), f2_hi(v[0]), f2_lo(v[1]));
+    const float b = max3(f2_hi(v[1]), f2_lo(v[2]), f2_hi(v[2]));
+    const float c = max3(f2_lo(v[3]), f2_hi(v[3]), f2_lo(v[4]));
+    const float d = max3(f2_hi(v[4]), f2_lo(v[5]), f2_hi(v[5]));
+    const float e = max3(f2_lo(v[6]), f2_hi(v[6]), f2_lo(v[7]));
+    return fmaxf(max3(a, b, c), max3(d, e, f2_hi(v[7])));
+}
+
+// Fixed pairwise tree over eight packed pairs.
+__device__ __forceinline__ f2_t tree8(const f2_t *e) {
+    return add2(add2(add2(e[0], e[1]), add2(e[2], e[3])), add2(add2(e[4], e[5]), add2(e[6], e[7])));
+}
+
+// Online log-sum-exp of sixteen columns of both sides into the state (see
+// lpd_acc.cuh).  Each side's chunk maximum is taken first and the sums are
+// rescaled at most once per chunk; the sixteen terms of each sum are added in a
+// fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
+// -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
+__device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a) {
+    const float cmt = max16(vt), cmr = max16(vr);
+    if (cmt > a.mt || cmr > a.mr) {
+        const float nmt = fmaxf(a.mt, cmt), nmr = fmaxf(a.mr, cmr);
+        const float at = __fmul_rn(__fsub_rn(a.mt, nmt), kLog2e);
+        const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), kLog2e);
+        const float ft = ex2(at), fr = ex2(ar);
+        const float corr = scale_diff(ft, fr, at, ar);
+        a.dd = add2(mul2(a.dd, f2(ft, ft)), mul2(a.sr, f2(corr, corr)));
+        a.st = mul2(a.st, f2(ft, ft));
+        a.sr = mul2(a.sr, f2(fr, fr));
+        a.mt = nmt;
+        a.mr = nmr;
+    }
+    const f2_t mt2 = f2(a.mt, a.mt), mr2 = f2(a.mr, a.mr), l2 = f2(kLog2e, kLog2e);
+    f2_t et[8], er[8], dq[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        et[p] = ex2_2(mul2(sub2(vt[p], mt2), l2));
+        er[p] = ex2_2(mul2(sub2(vr[p], mr2), l2));
+        dq[p] = sub2(et[p], er[p]);
+    }
+    a.st = add2(a.st, tree8(et));
+    a.sr = add2(a.sr, tree8(er));
+    a.dd = add2(a.dd, tree8(dq));
+}
+
 }  // namespace lpd

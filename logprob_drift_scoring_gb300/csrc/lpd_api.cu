@@ -366,4 +366,47 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
 }
 
+size_t lpd_fused_workspace_size(int64_t n_rows, int64_t hidden, int64_t vocab) {
+    if (n_rows < 0 || n_rows > kMaxRows || hidden <= 0 || hidden % 64 != 0 || vocab <= 0 || vocab > kMaxVocab)
+        return 0;
+    return fused_layout(n_rows, hidden, vocab).total;
+}
+
+int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const void *W, int64_t n_rows,
+                    int64_t hidden, int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask,
+                    double clip_lo, double clip_hi, float *out_logp_train, float *out_logp_rollout,
+                    float *out_dlogp, lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    int rc = check_rows_vocab(n_rows, vocab);
+    if (rc) return rc;
+    if (hidden <= 0) return LPD_ERR_BAD_SIZE;
+    if (hidden % 64 != 0 || hidden > (1 << 20)) return LPD_ERR_ALIGNMENT;
+    if (!out_metrics || !W || ((!token_ids || !action_mask || !hidden_train || !hidden_rollout) && n_rows > 0))
+        return LPD_ERR_NULL_POINTER;
+    if (!aligned16(hidden_train) || !aligned16(hidden_rollout) || !aligned16(W)) return LPD_ERR_ALIGNMENT;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_fused_workspace_size(n_rows, hidden, vocab))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FusedCall c{};
+    c.layout = fused_layout(n_rows, hidden, vocab);
+    c.workspace = workspace;
+    c.hidden_train = hidden_train;
+    c.hidden_rollout = hidden_rollout;
+    c.weight = W;
+    c.n_rows = n_rows;
+    c.hidden = hidden;
+    c.vocab = vocab;
+    c.out_lt = out_logp_train;
+    c.out_lr = out_logp_rollout;
+    c.out_d = out_dlogp;
+    c.status = &out_metrics->status;
+    const Ws w = carve(workspace, n_rows, 0);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    if ((rc = cuda_status(launch_fused(c, s)))) return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
 }  // extern "C"

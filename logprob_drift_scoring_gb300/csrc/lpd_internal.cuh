@@ -106,6 +106,29 @@ struct FinArgs {
     uint32_t *status;
 };
 
+// ---------------------------------------------------------------- fused head
+// Workspace of the fused LM-head path: the common regions (with no per-warp
+// states) followed by the dense active hidden rows of both sides and the
+// per-(row, vocab tile) partial states.
+struct FusedLayout {
+    WsLayout base;
+    size_t hidden_t, hidden_r, part_a, part_b, total;
+    int64_t a_pad;     // rows padded to the 128-row tile
+    int n_tiles_n;     // vocab tiles of 256 columns
+};
+
+struct FusedCall {
+    FusedLayout layout;
+    void *workspace;
+    const void *hidden_train, *hidden_rollout, *weight;
+    int64_t n_rows, hidden, vocab;
+    float *out_lt, *out_lr, *out_d;
+    uint32_t *status;
+};
+
+FusedLayout fused_layout(int64_t n_rows, int64_t hidden, int64_t vocab);
+cudaError_t launch_fused(const FusedCall &c, cudaStream_t stream);
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int32_t *ids,
                                  float *out_lt, float *out_lr, float *out_d,

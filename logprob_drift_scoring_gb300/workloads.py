@@ -22,6 +22,9 @@ shapes, dtypes, vocab sizes, padding layouts and masks stand in for it:
   sharded  B=1 x T=32768, V=151936 as 4 contiguous vocab shards of 37984
            columns per side, bf16 N(0, 3^2); rollout = bf16(train + N(0,
            2e-3^2)); all rows active; ids uniform.
+  fused    LM head: hidden [16384, 4096] bf16 N(0, 1), W [151936, 4096] bf16
+           N(0, 0.02^2), rollout hidden = bf16(hidden + N(0, 1e-3^2)); all
+           rows active; ids uniform.
 
 Noise scales are standard deviations.  Generation runs on the target device
 with a seeded torch.Generator; large tensors are generated in row chunks.
@@ -178,3 +181,49 @@ def sharded(seed: int = 3, device="cuda", seq: int = 32768, n_shards: int = 4, v
     v_ranges = [(k * width, (k + 1) * width) for k in range(n_shards)]
     return Workload("vocab-sharded-tp4", ts, rs, ids, mask, vocab, v_ranges=v_ranges,
                     meta={"B": 1, "T": seq, "seed": seed, "n_shards": n_shards})
+
+
+@dataclass
+class HeadWorkload:
+    name: str
+    hidden_train: torch.Tensor   # [R, H] bf16
+    hidden_rollout: torch.Tensor
+    weight: torch.Tensor         # [V, H] bf16
+    token_ids: torch.Tensor
+    action_mask: torch.Tensor
+    clip: tuple = CLIP
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.token_ids.shape[0])
+
+    @property
+    def vocab(self) -> int:
+        return int(self.weight.shape[0])
+
+    @property
+    def hidden(self) -> int:
+        return int(self.weight.shape[1])
+
+
+def head(n_rows: int, hidden: int, vocab: int, *, seed: int = 4, device="cuda", w_sigma: float = 0.02,
+         rollout_noise: float = 1e-3, active_prob: float = 1.0) -> HeadWorkload:
+    """LM-head case: hidden N(0, 1), W N(0, w_sigma^2), rollout hidden = bf16(hidden + noise)."""
+    g = _gen(device, seed)
+    ht = torch.randn((n_rows, hidden), generator=g, device=device).to(torch.bfloat16)
+    hr = _fill_noisy(ht.float(), rollout_noise, g, torch.bfloat16)
+    W = torch.empty((vocab, hidden), dtype=torch.bfloat16, device=device)
+    step = _chunk_rows(hidden)
+    for c in range(0, vocab, step):
+        n = min(step, vocab - c)
+        W[c:c + n] = (w_sigma * torch.randn((n, hidden), generator=g, device=device)).to(torch.bfloat16)
+    ids = torch.randint(0, vocab, (n_rows,), generator=g, device=device, dtype=torch.int32)
+    mask = (torch.rand(n_rows, generator=g, device=device) < active_prob).to(torch.uint8)
+    return HeadWorkload("head", ht, hr, W, ids, mask, meta={"seed": seed})
+
+
+def fused(seed: int = 4, device="cuda", rows: int = 16384) -> HeadWorkload:
+    w = head(rows, 4096, 151936, seed=seed, device=device)
+    w.name = "fused-lm-head"
+    return w

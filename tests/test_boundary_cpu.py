@@ -147,3 +147,32 @@ def test_stage_entry_points_validate():
     t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 10)
     assert lib.lpd_token_logp(ctypes.byref(t), ctypes.byref(t), 4, 11, None, None, None, FAKE, WS_OK, 1 << 20,
                               None) == B.LPD_ERR_BAD_STRIDE
+
+
+def _call_fused(ht=FAKE, hr=FAKE, W=FAKE, n_rows=8, hidden=128, vocab=100, ws=WS_OK, ws_bytes=1 << 30, lo=0.8):
+    return B.lib().lpd_score_fused(ht, hr, W, n_rows, hidden, vocab, FAKE, FAKE, lo, 1.2, None, None, None, FAKE,
+                                   ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(hidden=0), B.LPD_ERR_BAD_SIZE),
+    (dict(hidden=100), B.LPD_ERR_ALIGNMENT),
+    (dict(ht=FAKE + 8), B.LPD_ERR_ALIGNMENT),
+    (dict(W=FAKE + 2), B.LPD_ERR_ALIGNMENT),
+    (dict(W=None), B.LPD_ERR_NULL_POINTER),
+    (dict(hr=None), B.LPD_ERR_NULL_POINTER),
+    (dict(vocab=0), B.LPD_ERR_BAD_SIZE),
+    (dict(n_rows=-3), B.LPD_ERR_BAD_SIZE),
+    (dict(lo=-1.0), B.LPD_ERR_BAD_CLIP),
+    (dict(ws_bytes=1024), B.LPD_ERR_WORKSPACE),
+])
+def test_fused_rejects_invalid_arguments(kwargs, code):
+    assert _call_fused(**kwargs) == code
+
+
+def test_fused_workspace_size():
+    assert B.lpd_fused_workspace_size(100, 100, 1000) == 0          # hidden not a multiple of 64
+    small = B.lpd_fused_workspace_size(100, 128, 1000)
+    assert small > 0 and small % 256 == 0
+    # dense hidden copies dominate: 2 sides x 128 padded rows x 4096 x 2 B
+    assert B.lpd_fused_workspace_size(128, 4096, 1000) >= 2 * 128 * 4096 * 2
