@@ -241,14 +241,19 @@ __global__ void __launch_bounds__(kFinThreads) terms_kernel(double ln_clip_lo, d
 // One CTA: merge the finalise blocks' partials (thread tid < 256 folds blocks
 // tid, tid+256, ... in order, then a fixed tree), then nearest-rank p95 and
 // p99 of |dlogp| by a most-significant-digit radix select over the fp32 bit
-// patterns of |dlogp| (monotone for non-negative floats), 8 bits per pass,
-// both ranks in the same passes.  The maximum comes exact from the partials.
+// patterns of |dlogp| (monotone for non-negative floats; the sign bit is always
+// 0), in three passes of 11, 10 and 10 bits, both ranks in the same passes.
+// The first digit covers the exponent and four mantissa bits, so keys that
+// share an order of magnitude still spread over several histogram bins.  The
+// maximum comes exact from the partials.
+constexpr int kSelBins = 2048;
+
 __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, const WsHeader *hdr,
                                                               const uint32_t *keys, const BlockPartial *bp,
                                                               lpd_metrics *out) {
     constexpr int kFold = 256;  // threads that fold block partials
     __shared__ Part sh[kFold];
-    __shared__ uint32_t hist[2][256];
+    __shared__ uint32_t hist[2][kSelBins];
     __shared__ uint32_t prefix[2];
     __shared__ long long rank[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -275,38 +280,28 @@ __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, 
     block_tree<kFold>(sh);
 
     if (n_active > 0) {
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
-            if (tid < 512) (&hist[0][0])[tid] = 0;
+        const int shifts[3] = {20, 10, 0};
+        const int widths[3] = {11, 10, 10};
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = shifts[pass];
+            const uint32_t dmask = (1u << widths[pass]) - 1u;
+            const int nbins = 1 << widths[pass];
+            const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (shift + widths[pass]));
+            for (int b = tid; b < 2 * kSelBins; b += kSelThreads) (&hist[0][0])[b] = 0;
             __syncthreads();
             const uint32_t p0 = prefix[0], p1 = prefix[1];
-            // |dlogp| keys crowd into few digits, so lanes of a warp that hold
-            // the same digit are counted together (one shared atomic per group)
-            for (int64_t base = 0; base < n_active; base += kSelThreads) {
-                const int64_t i = base + tid;
-                const bool valid = i < n_active;
-                const uint32_t key = valid ? keys[i] : 0u;
-                const uint32_t dig = (key >> shift) & 255u;
-#pragma unroll
-                for (int tgt = 0; tgt < 2; ++tgt) {
-                    const bool in = valid && (key & hi_mask) == (tgt == 0 ? p0 : p1);
-                    const unsigned members = __ballot_sync(0xffffffffu, in);
-                    if (in) {
-                        const unsigned grp = __match_any_sync(members, dig);
-                        if (lane == __ffs(grp) - 1) atomicAdd(&hist[tgt][dig], static_cast<uint32_t>(__popc(grp)));
-                    }
-                }
+            for (int64_t i = tid; i < n_active; i += kSelThreads) {
+                const uint32_t key = keys[i];
+                const uint32_t dig = (key >> shift) & dmask;
+                if ((key & hi_mask) == p0) atomicAdd(&hist[0][dig], 1u);
+                if ((key & hi_mask) == p1) atomicAdd(&hist[1][dig], 1u);
             }
             __syncthreads();
             if (warp < 2) {
-                uint32_t c[8];
+                // lane l owns bins [l * per, (l + 1) * per)
+                const int per = nbins / 32;
                 uint32_t tot = 0;
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    c[b] = hist[warp][8 * lane + b];
-                    tot += c[b];
-                }
+                for (int b = 0; b < per; ++b) tot += hist[warp][lane * per + b];
                 uint32_t incl = tot;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -317,18 +312,15 @@ __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, 
                 const long long before = static_cast<long long>(incl - tot);
                 if (before < k && k <= static_cast<long long>(incl)) {
                     long long acc = before;
-                    int digit = -1;
-                    long long newk = 0;
-#pragma unroll
-                    for (int b = 0; b < 8; ++b) {
-                        if (digit < 0 && acc + c[b] >= k) {
-                            digit = 8 * lane + b;
-                            newk = k - acc;
+                    for (int b = 0; b < per; ++b) {
+                        const uint32_t c = hist[warp][lane * per + b];
+                        if (acc + c >= k) {
+                            prefix[warp] |= static_cast<uint32_t>(lane * per + b) << shift;
+                            rank[warp] = k - acc;
+                            break;
                         }
-                        acc += c[b];
+                        acc += c;
                     }
-                    prefix[warp] |= static_cast<uint32_t>(digit) << shift;
-                    rank[warp] = newk;
                 }
             }
             __syncthreads();
