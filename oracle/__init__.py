@@ -64,6 +64,25 @@ class Shard(ctypes.Structure):
     ]
 
 
+OP_SCALE, OP_SOFTCAP = 1, 2
+
+
+class Transform(ctypes.Structure):
+    _fields_ = [("n_ops", ctypes.c_int32), ("kind", ctypes.c_int32 * 4), ("param", ctypes.c_float * 4)]
+
+
+def transform(ops) -> Transform | None:
+    """ops: list of (kind, param) applied in order; None or [] is the identity."""
+    if not ops:
+        return None
+    t = Transform()
+    t.n_ops = len(ops)
+    for i, (k, p) in enumerate(ops):
+        t.kind[i] = k
+        t.param[i] = p
+    return t
+
+
 def compile_oracle(source: Path | str = SOURCE, out: Path | None = None) -> Path:
     """Compile the oracle C source to a shared object (gcc -O2, no fast-math)."""
     source = Path(source)
@@ -101,6 +120,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.lpdo_score_sharded.argtypes = [P, P, ctypes.c_int, P, I64, I64, P, P, D, D, P, P, P, P]
     lib.lpdo_head_logits.restype = None
     lib.lpdo_head_logits.argtypes = [P, P, I64, I64, P]
+    lib.lpdo_score_transformed.restype = U32
+    lib.lpdo_score_transformed.argtypes = [P, I32, I64, P, I32, I64, P, P, I64, I64, P, P, D, D, P, P, P, P]
     lib.lpdo_score_head_rows.restype = U32
     lib.lpdo_score_head_rows.argtypes = [P, P, P, I64, I64, P, P, I64, P, P, P]
     return lib
@@ -277,3 +298,22 @@ def score_head_rows(hidden_t, hidden_r, W, token_ids, rows, lib=None) -> Result:
     st = lib.lpdo_score_head_rows(_ptr(ht), _ptr(hr), _ptr(W), W.shape[1], W.shape[0], _ptr(ids),
                                   _ptr(sel), n, _ptr(lt), _ptr(lr), _ptr(d))
     return Result(lt, lr, d, int(st))
+
+
+def score_transformed(train, rollout, token_ids, mask, train_ops=None, rollout_ops=None, clip_lo=0.8,
+                      clip_hi=1.2, lib=None) -> Result:
+    """score() with an ordered chain of logit transforms per side."""
+    lib = lib or load()
+    t, tc, ts = _logits_arg(train)
+    r, rc, rs = _logits_arg(rollout)
+    n_rows, vocab = t.shape[0], t.shape[1]
+    ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+    m8 = np.ascontiguousarray(mask, dtype=np.uint8)
+    ct, cr = transform(train_ops), transform(rollout_ops)
+    lt, lr, d = (np.zeros(n_rows) for _ in range(3))
+    met = Metrics()
+    st = lib.lpdo_score_transformed(_ptr(t), tc, ts, _ptr(r), rc, rs,
+                                    ctypes.addressof(ct) if ct else None, ctypes.addressof(cr) if cr else None,
+                                    n_rows, vocab, _ptr(ids), _ptr(m8), float(clip_lo), float(clip_hi),
+                                    _ptr(lt), _ptr(lr), _ptr(d), ctypes.addressof(met))
+    return Result(lt, lr, d, int(st), met.as_dict())

@@ -23,6 +23,8 @@
  *         per-shard partial logsumexp merged in global vocab-shard order, and
  *         the single-owner selected-logit gather on pre-shifted rows.
  *   [HD]  same table, rows 9-10: the LM-head GEMM that produces the logits.
+ *   [TC]  same table, row 7: an ordered chain of logit transforms (temperature,
+ *         soft-cap, logit scale) applied to every logit before the softmax.
  *
  * Readings where the pages are silent (each is also listed with the design
  * notes): percentiles are nearest-rank (1-based rank ceil(p*A/100) of the
@@ -381,5 +383,87 @@ uint32_t lpdo_score_head_rows(const uint16_t *hidden_t, const uint16_t *hidden_r
         dlogp[i] = logp_train[i] - logp_rollout[i];
     }
     free(x);
+    return status;
+}
+
+/* ---- logit transform chain [TC] ----------------------------------------- */
+
+#define LPDO_OP_SCALE 1   /* x <- x * p          (temperature 1/T, logit scale) */
+#define LPDO_OP_SOFTCAP 2 /* x <- p * tanh(x / p) */
+
+typedef struct {
+    int32_t n_ops;
+    int32_t kind[4];
+    float param[4];
+} lpdo_transform;
+
+/* The chain applied to one logit, in order, in double. */
+static double apply_chain(const lpdo_transform *c, double x)
+{
+    if (!c)
+        return x;
+    for (int k = 0; k < c->n_ops; ++k) {
+        double p = (double)c->param[k];
+        if (c->kind[k] == LPDO_OP_SCALE)
+            x = x * p;
+        else if (c->kind[k] == LPDO_OP_SOFTCAP)
+            x = p * tanh(x / p);
+    }
+    return x;
+}
+
+/* Selected-token logp of one row after the chain: every logit (the selected
+ * one included) is transformed, then the plain definition is applied. */
+static uint32_t row_logp_chain(const void *row, int dtype, int64_t vocab, int64_t id,
+                               const lpdo_transform *c, double *logp_out)
+{
+    if (id < 0 || id >= vocab) {
+        *logp_out = NAN;
+        return LPDO_STATUS_TOKEN_OOB;
+    }
+    double m = -INFINITY;
+    int has_nan = 0;
+    for (int64_t j = 0; j < vocab; ++j) {
+        double x = apply_chain(c, logit_at(row, dtype, j));
+        if (x > m)
+            m = x;
+        if (isnan(x))
+            has_nan = 1;
+    }
+    double s = 0.0;
+    if (m != -INFINITY)
+        for (int64_t j = 0; j < vocab; ++j)
+            s += exp(apply_chain(c, logit_at(row, dtype, j)) - m);
+    if (has_nan)
+        s = NAN;
+    double lse = lse_of(m, s);
+    double xs = apply_chain(c, logit_at(row, dtype, id));
+    *logp_out = xs - lse;
+    return (isfinite(lse) && isfinite(xs)) ? 0u : LPDO_STATUS_NONFINITE;
+}
+
+uint32_t lpdo_score_transformed(const void *train, int train_dtype, int64_t train_stride,
+                                const void *rollout, int rollout_dtype, int64_t rollout_stride,
+                                const lpdo_transform *train_chain, const lpdo_transform *rollout_chain,
+                                int64_t n_rows, int64_t vocab, const int32_t *token_ids,
+                                const uint8_t *mask, double clip_lo, double clip_hi,
+                                double *logp_train, double *logp_rollout, double *dlogp,
+                                lpdo_metrics *metrics)
+{
+    uint32_t status = 0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        logp_train[r] = logp_rollout[r] = dlogp[r] = 0.0;
+        if (!mask[r])
+            continue;
+        status |= row_logp_chain(row_ptr(train, train_dtype, train_stride, r), train_dtype, vocab,
+                                 token_ids[r], train_chain, &logp_train[r]);
+        status |= row_logp_chain(row_ptr(rollout, rollout_dtype, rollout_stride, r), rollout_dtype,
+                                 vocab, token_ids[r], rollout_chain, &logp_rollout[r]);
+        dlogp[r] = logp_train[r] - logp_rollout[r];
+    }
+    if (metrics) {
+        lpdo_metrics_from_dlogp(dlogp, mask, n_rows, clip_lo, clip_hi, metrics);
+        metrics->status = status;
+    }
     return status;
 }

@@ -412,3 +412,78 @@ def pin_head_logits_matmul(lib):
 
 
 ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+# ----------------------------------------------------- transform-chain pins
+
+def _dec_tanh(y: Decimal) -> Decimal:
+    e = (2 * y).exp()
+    return (e - 1) / (e + 1)
+
+
+def _dec_chain(x, ops):
+    v = Decimal(float(x))
+    for kind, p in ops:
+        p = Decimal(float(np.float32(p)))
+        v = v * p if kind == oracle.OP_SCALE else p * _dec_tanh(v / p)
+    return v
+
+
+def _dec_logp_chain(row, idx, ops):
+    vals = [_dec_chain(x, ops) for x in row]
+    total = sum((v.exp() for v in vals), Decimal(0))
+    return vals[idx] - total.ln()
+
+
+def pin_transform_identity_is_plain(lib):
+    t, r, ids, mask = _case(25, 40, 61, dtype="f32")
+    a = oracle.score(t, r, ids, mask, lib=lib)
+    b = oracle.score_transformed(t, r, ids, mask, [], None, lib=lib)
+    assert np.array_equal(a.dlogp, b.dlogp) and a.metrics == b.metrics
+
+
+def pin_transform_scale_closed_form(lib):
+    rng = np.random.default_rng(62)
+    for s in (0.5, 1.25, 2.0):
+        x = rng.normal(0, 3, size=(6, 2)).astype(np.float32)
+        ids = np.zeros(6, np.int32)
+        res = oracle.score_transformed(x, x, ids, np.ones(6, np.uint8), [(oracle.OP_SCALE, s)], None, lib=lib)
+        for i in range(6):
+            want = -math.log1p(math.exp(s * (float(x[i, 1]) - float(x[i, 0]))))
+            _close(res.logp_train[i], want, 1e-13, "scaled V=2")
+            _close(res.logp_rollout[i], float(dec_logp(x[i], 0)), 1e-13, "unscaled side")
+    u = np.full((2, 500), 1.75, np.float32)
+    res = oracle.score_transformed(u, u, np.array([3, 7], np.int32), np.ones(2, np.uint8),
+                                   [(oracle.OP_SCALE, 1 / 0.7)], None, lib=lib)
+    _close(res.logp_train[0], -math.log(500), 1e-13, "temperature on uniform")
+
+
+def pin_transform_softcap_and_order_decimal(lib):
+    rng = np.random.default_rng(63)
+    x = (rng.normal(0, 20, size=(4, 12))).astype(np.float32)
+    x[0, 3] = 1e4
+    x[1, 5] = -1e4
+    ids = rng.integers(0, 12, size=4).astype(np.int32)
+    chains = ([(oracle.OP_SOFTCAP, 30.0)], [(oracle.OP_SCALE, 2.0), (oracle.OP_SOFTCAP, 15.0)],
+              [(oracle.OP_SOFTCAP, 15.0), (oracle.OP_SCALE, 2.0)])
+    got = []
+    for ops in chains:
+        res = oracle.score_transformed(x, x, ids, np.ones(4, np.uint8), ops, None, lib=lib)
+        for i in range(4):
+            _close(res.logp_train[i], float(_dec_logp_chain(x[i], int(ids[i]), ops)), 1e-12, f"chain {ops}")
+        got.append(res.logp_train.copy())
+    assert not np.allclose(got[1], got[2]), "chain order must matter"
+
+
+def pin_transform_per_side(lib):
+    rng = np.random.default_rng(64)
+    x = rng.normal(0, 3, size=(5, 9)).astype(np.float32)
+    ids = rng.integers(0, 9, size=5).astype(np.int32)
+    ops = [(oracle.OP_SCALE, 1 / 0.7)]
+    res = oracle.score_transformed(x, x, ids, np.ones(5, np.uint8), None, ops, lib=lib)
+    for i in range(5):
+        want = dec_logp(x[i], int(ids[i])) - _dec_logp_chain(x[i], int(ids[i]), ops)
+        _close(res.dlogp[i], float(want), 1e-12, "train plain, rollout tempered")
+
+
+ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}

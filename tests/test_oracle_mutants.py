@@ -47,6 +47,13 @@ MUTANTS = {
                         "const uint16_t *w = W + (size_t)v;"),
     "oob_unchecked": ("    if (id < 0 || id >= vocab) {\n        *logp_out = NAN;\n        return LPDO_STATUS_TOKEN_OOB;\n    }\n    double m, s;",
                       "    double m, s;"),
+    "chain_scale_divides": ("x = x * p;", "x = x / p;"),
+    "chain_softcap_no_outer": ("x = p * tanh(x / p);", "x = tanh(x / p);"),
+    "chain_reversed": ("for (int k = 0; k < c->n_ops; ++k) {\n        double p = (double)c->param[k];",
+                       "for (int k = c->n_ops - 1; k >= 0; --k) {\n        double p = (double)c->param[k];"),
+    "chain_skips_selected": ("double xs = apply_chain(c, logit_at(row, dtype, id));",
+                             "double xs = logit_at(row, dtype, id);"),
+    "chain_wrong_side": ("token_ids[r], rollout_chain, &logp_rollout[r]);", "token_ids[r], train_chain, &logp_rollout[r]);"),
     "nonfinite_unflagged": ("return (isfinite(lse) && isfinite(xs)) ? 0u : LPDO_STATUS_NONFINITE;\n}\n\nstatic int",
                             "return 0u;\n}\n\nstatic int"),
 }
