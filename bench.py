@@ -200,12 +200,21 @@ class Runner:
             ws = B.lpd_workspace_size(B.LPD_KIND_SCORE, n)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.launches_per_step = 5 if n > 0 else 2
+        self.chain = None
 
     def step(self, ev=None):
         """One pass of the path; with ev = (e0, e1, e2, e3) records events
         around stage 1, stage 2 and stage 3 on the current stream."""
         B, w = self.B, self.w
         lt, lr, d = self.outs
+        if self.chain is not None:
+            if ev:
+                ev[0].record()
+            B.lpd_score_transformed(w.train, w.rollout, self.chain, self.chain, w.token_ids, w.action_mask,
+                                    *w.clip, lt, lr, d, self.met, self.ws)
+            if ev:
+                ev[3].record()
+            return
         if self.sharded:
             if ev:
                 ev[0].record()
@@ -343,6 +352,18 @@ def run_fused(args, w, world, rank):
     return out
 
 
+def parse_chain(text: str):
+    """'softcap:30,scale:1.4286' -> [(LPD_OP_SOFTCAP, 30.0), (LPD_OP_SCALE, 1.4286)]."""
+    from logprob_drift_scoring_gb300 import binding as B
+
+    kinds = {"scale": B.LPD_OP_SCALE, "softcap": B.LPD_OP_SOFTCAP}
+    out = []
+    for item in text.split(","):
+        name, val = item.split(":")
+        out.append((kinds[name.strip()], float(val)))
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -365,6 +386,8 @@ def run_ours(args):
             dist.destroy_process_group()
         return out
     runner = Runner(w)
+    if args.transform:
+        runner.chain = parse_chain(args.transform)
     n_active = int(w.action_mask.sum().item())
     bpt = bytes_per_active_token(w)
 
@@ -389,7 +412,7 @@ def run_ours(args):
     ms_step = total_ms / K
     value = world * n_active / (ms_step / 1e3)
 
-    if runner.sharded:
+    if runner.sharded or runner.chain is not None:
         stage2 = sum(e[0].elapsed_time(e[3]) for e in evs) / K
         stage_ms = {"whole_call": stage2}
     else:
@@ -404,7 +427,8 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": f"{peaks['source']} copy bandwidth (burst)",
-                "span": "stage 2: row kernel + per-row finalise" if not runner.sharded else "whole call",
+                "span": "whole call" if (runner.sharded or runner.chain is not None)
+                else "stage 2: row kernel + per-row finalise",
                 "algorithmic_bytes_per_launch": n_active * bpt}
 
     e2e = None
@@ -419,8 +443,9 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": CONFIGS[args.config]["workload"] if not (args.batch or args.seq)
-                       else f"{args.config} reduced B={args.batch} T={args.seq}",
+            "config": {"workload": (CONFIGS[args.config]["workload"] if not (args.batch or args.seq)
+                                    else f"{args.config} reduced B={args.batch} T={args.seq}")
+                       + (f" + transform {args.transform}" if args.transform else ""),
                        "rows": w.n_rows, "active_tokens": n_active,
                        "vocab": w.vocab, "logits_bytes": w.logits_bytes(), "l2": "inputs exceed L2 (no flush)",
                        "parallelism": f"replicas x{world}", "input_dtypes": _dtypes(w)},
@@ -551,6 +576,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--transform", default=None,
+                    help="logit transform chain on both sides, e.g. softcap:30,scale:1.4286")
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")
     ap.add_argument("--seq", type=int, default=None, help="override T (small profiling cases only)")
     args = ap.parse_args(argv)

@@ -71,6 +71,7 @@ extern "C" {
 #define LPD_ERR_CUDA (-8)         /* a CUDA runtime call failed (launch, attribute) */
 #define LPD_ERR_ALIGNMENT (-9)    /* a pointer or stride breaks a stated alignment rule */
 #define LPD_ERR_UNSUPPORTED (-10) /* a size outside what this build supports */
+#define LPD_ERR_BAD_TRANSFORM (-11) /* transform chain: bad op count, kind or parameter */
 
 /* ---- device-reported status bits (lpd_metrics.status) ------------------ */
 #define LPD_STATUS_TOKEN_OOB 1u /* an active row's token id is outside [0, vocab) */
@@ -141,6 +142,20 @@ typedef struct {
     char fingerprint[96];  /* compiler version and build date */
 } lpd_backend_info_t;
 
+/* Logit transform chain of one side ("[WS2] Framework for ablation
+ * experiment", LogProb knobs table, row 7): ops applied in order to every logit
+ * before the softmax.  LPD_OP_SCALE: x <- x * param (temperature T is param =
+ * 1/T; logit scale); LPD_OP_SOFTCAP: x <- param * tanh(x / param).  Parameters
+ * must be finite and > 0.  n_ops = 0 is the identity. */
+#define LPD_OP_SCALE 1
+#define LPD_OP_SOFTCAP 2
+#define LPD_MAX_TRANSFORM_OPS 4
+typedef struct {
+    int32_t n_ops;
+    int32_t kind[LPD_MAX_TRANSFORM_OPS];
+    float param[LPD_MAX_TRANSFORM_OPS];
+} lpd_transform;
+
 /* ---- sizing and introspection ----------------------------------------- */
 
 /* Bytes of device workspace that a call of the given kind needs for n_rows
@@ -206,6 +221,19 @@ int lpd_token_logp(const lpd_logits *train, const lpd_logits *rollout, int64_t n
 int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi,
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
+
+/* lpd_score with a logit transform chain per side (each may be NULL for the
+ * identity).  The chains are part of what is compared: different chains on the
+ * two sides show up as drift, which the pages treat as a correctness bug rather
+ * than noise.  Same workspace kind and outputs as lpd_score; a chain that is
+ * not valid returns LPD_ERR_BAD_TRANSFORM before any launch. */
+int lpd_score_transformed(const lpd_logits *train, const lpd_logits *rollout,
+                          const lpd_transform *train_chain, const lpd_transform *rollout_chain,
+                          int64_t n_rows, int64_t vocab, const int32_t *token_ids,
+                          const uint8_t *action_mask, double clip_lo, double clip_hi,
+                          float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
+                          lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                          void *stream);
 
 /* Vocab-sharded scoring ("[WS2] Framework for ablation experiment", LogProb
  * knobs table, rows 3-5 and 8).  Each side's vocabulary arrives as n_shards

@@ -25,6 +25,8 @@ LPD_ERR_WORKSPACE = -7
 LPD_ERR_CUDA = -8
 LPD_ERR_ALIGNMENT = -9
 LPD_ERR_UNSUPPORTED = -10
+LPD_ERR_BAD_TRANSFORM = -11
+LPD_OP_SCALE, LPD_OP_SOFTCAP = 1, 2
 LPD_STATUS_TOKEN_OOB = 1
 LPD_STATUS_NONFINITE = 2
 LPD_STATUS_TIMEOUT = 4
@@ -40,6 +42,22 @@ class LpdLogits(ctypes.Structure):
 class LpdShard(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("row_stride", ctypes.c_int64), ("v_start", ctypes.c_int64), ("v_end", ctypes.c_int64)]
+
+
+class LpdTransform(ctypes.Structure):
+    _fields_ = [("n_ops", ctypes.c_int32), ("kind", ctypes.c_int32 * 4), ("param", ctypes.c_float * 4)]
+
+
+def transform_struct(ops):
+    """lpd_transform from [(kind, param), ...] applied in order; None for the identity."""
+    if ops is None:
+        return None
+    t = LpdTransform()
+    t.n_ops = len(ops)
+    for i, (k, p) in enumerate(ops):
+        t.kind[i] = k
+        t.param[i] = p
+    return t
 
 
 class LpdMetrics(ctypes.Structure):
@@ -65,7 +83,7 @@ METRICS_BYTES = ctypes.sizeof(LpdMetrics)
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
-            "lpd_fused_workspace_size", "lpd_score_fused")
+            "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed")
 LPD_NOALLOC_MAX_ROWS = 32768
 
 
@@ -105,6 +123,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_fused_workspace_size.argtypes = [I64, I64, I64]
         L.lpd_score_fused.restype = ctypes.c_int
         L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
+        L.lpd_score_transformed.restype = ctypes.c_int
+        L.lpd_score_transformed.argtypes = [P, P, P, P, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
         _LIB = L
@@ -184,6 +204,18 @@ def lpd_score(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp
                          _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics), _ptr(workspace),
                          workspace.numel() if workspace is not None else 0, _stream(stream))
     _check(rc, "lpd_score")
+
+
+def lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, action_mask, clip_lo, clip_hi,
+                          out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace, stream=None) -> None:
+    t, r = logits_struct(train), logits_struct(rollout)
+    ct, cr = transform_struct(train_ops), transform_struct(rollout_ops)
+    rc = lib().lpd_score_transformed(ctypes.byref(t), ctypes.byref(r), ctypes.byref(ct) if ct else None,
+                                     ctypes.byref(cr) if cr else None, train.shape[0], train.shape[1],
+                                     _ptr(token_ids), _ptr(action_mask), float(clip_lo), float(clip_hi),
+                                     _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics),
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "lpd_score_transformed")
 
 
 def lpd_select_active(token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace,
@@ -281,9 +313,11 @@ class ScoreResult:
     metrics: dict
 
 
-def score(train, rollout, token_ids, action_mask, clip=(0.8, 1.2), stream=None) -> ScoreResult:
+def score(train, rollout, token_ids, action_mask, clip=(0.8, 1.2), stream=None, train_ops=None,
+          rollout_ops=None) -> ScoreResult:
     """Allocate outputs and workspace with torch on the logits' device, run
-    lpd_score, and return per-token tensors plus the metrics as a dict."""
+    lpd_score (or lpd_score_transformed when a chain is given), and return
+    per-token tensors plus the metrics as a dict."""
     import torch
 
     dev = train.device
@@ -291,5 +325,9 @@ def score(train, rollout, token_ids, action_mask, clip=(0.8, 1.2), stream=None) 
     outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
     met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
     ws = torch.empty(lpd_workspace_size(LPD_KIND_SCORE, n), dtype=torch.uint8, device=dev)
-    lpd_score(train, rollout, token_ids, action_mask, clip[0], clip[1], *outs, met, ws, stream=stream)
+    if train_ops is None and rollout_ops is None:
+        lpd_score(train, rollout, token_ids, action_mask, clip[0], clip[1], *outs, met, ws, stream=stream)
+    else:
+        lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, action_mask, clip[0], clip[1],
+                              *outs, met, ws, stream=stream)
     return ScoreResult(outs[0], outs[1], outs[2], read_metrics(met))

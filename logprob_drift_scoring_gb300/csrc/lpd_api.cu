@@ -98,9 +98,13 @@ int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *l
 // Stage 2: the streaming row pass, then the per-row finalise.
 int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, const int32_t *perm, int n_perm,
              int64_t n_rows, int64_t vocab, float *lt, float *lr, float *d, float *plt, float *plr,
-             lpd_metrics *met, const Ws &w, cudaStream_t s) {
+             lpd_metrics *met, const Ws &w, cudaStream_t s, const Xform *xform = nullptr) {
     if (n_rows == 0) return LPD_OK;
     RowArgs a{};
+    if (xform) {
+        a.xt = xform[0];
+        a.xr = xform[1];
+    }
     for (int k = 0; k < n_seg; ++k) a.seg[k] = segs[k];
     a.n_seg = n_seg;
     a.vocab = vocab;
@@ -109,7 +113,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     a.part = w.part;
     a.pick = w.pick;
     a.status = &met->status;
-    int rc = cuda_status(launch_rows(a, dt, dr, tma, s));
+    int rc = cuda_status(launch_rows(a, dt, dr, tma, xform != nullptr, s));
     if (rc) return rc;
     FinArgs f{};
     f.n_seg = n_seg;
@@ -154,6 +158,21 @@ Segment whole_vocab(const lpd_logits *t, const lpd_logits *r, int64_t vocab) {
     sg.v_start = 0;
     sg.len = vocab;
     return sg;
+}
+
+// A side's chain as the kernel's copy; NULL is the identity.
+int to_xform(const lpd_transform *c, Xform *out) {
+    *out = Xform{};
+    if (!c) return LPD_OK;
+    if (c->n_ops < 0 || c->n_ops > LPD_MAX_TRANSFORM_OPS) return LPD_ERR_BAD_TRANSFORM;
+    out->n_ops = c->n_ops;
+    for (int k = 0; k < c->n_ops; ++k) {
+        if (c->kind[k] != LPD_OP_SCALE && c->kind[k] != LPD_OP_SOFTCAP) return LPD_ERR_BAD_TRANSFORM;
+        if (!std::isfinite(c->param[k]) || !(c->param[k] > 0.f)) return LPD_ERR_BAD_TRANSFORM;
+        out->kind[k] = c->kind[k];
+        out->param[k] = c->param[k];
+    }
+    return LPD_OK;
 }
 
 // Exact tiling of [0, vocab) by the shard ranges, in any array order ("fail
@@ -233,6 +252,7 @@ const char *lpd_strerror(int code) {
         case LPD_ERR_CUDA: return "a CUDA runtime call failed";
         case LPD_ERR_ALIGNMENT: return "a pointer or stride breaks an alignment rule";
         case LPD_ERR_UNSUPPORTED: return "size outside what this build supports";
+        case LPD_ERR_BAD_TRANSFORM: return "transform chain: bad op count, kind or parameter";
         case static_cast<int>(LPD_STATUS_TOKEN_OOB): return "status: active token id outside [0, vocab)";
         case static_cast<int>(LPD_STATUS_NONFINITE): return "status: non-finite log-sum-exp or selected logit";
         case static_cast<int>(LPD_STATUS_TIMEOUT): return "status: an internal pipeline wait gave up";
@@ -302,6 +322,34 @@ int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows
         return rc;
     if ((rc = run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
                        out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s)))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+int lpd_score_transformed(const lpd_logits *train, const lpd_logits *rollout, const lpd_transform *train_chain,
+                          const lpd_transform *rollout_chain, int64_t n_rows, int64_t vocab, const int32_t *token_ids,
+                          const uint8_t *action_mask, double clip_lo, double clip_hi, float *out_logp_train,
+                          float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    int rc = validate_pair(train, rollout, n_rows, vocab);
+    if (rc) return rc;
+    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    Xform xf[2];
+    if ((rc = to_xform(train_chain, &xf[0])) || (rc = to_xform(rollout_chain, &xf[1]))) return rc;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Ws w = carve(workspace, n_rows, 1);
+    const Segment sg = whole_vocab(train, rollout, vocab);
+    const bool tma = rows_aligned(train->ptr, train->row_stride, train->dtype) &&
+                     rows_aligned(rollout->ptr, rollout->row_stride, rollout->dtype);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    const bool any = xf[0].n_ops > 0 || xf[1].n_ops > 0;
+    if ((rc = run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
+                       out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s, any ? xf : nullptr)))
         return rc;
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
 }

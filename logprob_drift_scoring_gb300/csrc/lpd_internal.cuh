@@ -79,7 +79,15 @@ struct Segment {
     int64_t len;        // columns in this segment
 };
 
+// Logit transform chain of one side, applied in order to every logit.
+struct Xform {
+    int n_ops;
+    int kind[LPD_MAX_TRANSFORM_OPS];
+    float param[LPD_MAX_TRANSFORM_OPS];
+};
+
 struct RowArgs {
+    Xform xt, xr;  // train and rollout chains (used by the transforming instantiation only)
     Segment seg[kMaxSegments];
     int n_seg;
     int64_t vocab;
@@ -134,7 +142,7 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lt, float *out_lr, float *out_d,
                                  lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
                                  cudaStream_t stream);
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma,
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, bool use_xform,
                         cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,

@@ -118,17 +118,6 @@ __device__ __forceinline__ float ldg_elem<F32>(const char *p) {
     return __ldg(reinterpret_cast<const float *>(p));
 }
 
-template <class D>
-__device__ __forceinline__ float lds_elem(const char *stage, int col);
-template <>
-__device__ __forceinline__ float lds_elem<Bf16>(const char *stage, int col) {
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(stage + 2 * col)) << 16);
-}
-template <>
-__device__ __forceinline__ float lds_elem<F32>(const char *stage, int col) {
-    return *reinterpret_cast<const float *>(stage + 4 * col);
-}
-
 // Four consecutive columns starting at `col` (a multiple of 4) of a stage, as
 // two packed pairs.
 template <class D>
@@ -146,6 +135,23 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
     v[1] = f2(w.z, w.w);
 }
 
+// The logit transform chain ("[WS2] Framework for ablation experiment", LogProb
+// knobs table, row 7), applied in order to one logit in fp32: scale x * p
+// (temperature 1/T or logit scale) or soft-cap p * tanh(x / p).  Only real
+// columns are transformed; masked tail columns stay -inf.
+__device__ __forceinline__ float xform1(float x, const Xform &c) {
+    for (int k = 0; k < c.n_ops; ++k) {
+        const float p = c.param[k];
+        x = c.kind[k] == LPD_OP_SCALE ? __fmul_rn(x, p) : __fmul_rn(p, tanhf(__fdiv_rn(x, p)));
+    }
+    return x;
+}
+
+__device__ __forceinline__ void xform16(f2_t *v, const Xform &c) {
+#pragma unroll
+    for (int p = 0; p < 8; ++p) v[p] = f2(xform1(f2_lo(v[p]), c), xform1(f2_hi(v[p]), c));
+}
+
 // Column of slot q (0..15) of consumer thread t within a tile.
 __device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroupCols + 4 * t + (q & 3); }
 
@@ -158,7 +164,7 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
     return x;
 }
 
-template <class DT, class DR, bool kTma>
+template <class DT, class DR, bool kTma, bool kXform>
 __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     extern __shared__ __align__(1024) char smem[];
     __shared__ int abort_flag;
@@ -270,26 +276,43 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
                             lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
                         }
+                        if (kXform) {
+                            xform16(vt, a.xt);
+                            xform16(vr, a.xr);
+                        }
                     } else {
-                        // ragged last tile: the bulk copy moved whole 16-byte
-                        // units; the few columns after them come from global
+                        // ragged last tile: the same vector loads, then the
+                        // columns the bulk copy did not cover (a few bytes at the
+                        // end of the row) come from global, and columns past the
+                        // segment are -inf
                         const int nbt = static_cast<int>((static_cast<uint32_t>(nv * DT::kBytes) & ~15u) / DT::kBytes);
                         const int nbr = static_cast<int>((static_cast<uint32_t>(nv * DR::kBytes) & ~15u) / DR::kBytes);
 #pragma unroll
-                        for (int p = 0; p < 8; ++p) {
-                            float x[2], y[2];
+                        for (int g = 0; g < 4; ++g) {
+                            lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
+                            lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
+                        }
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int col = slot_col(t, 2 * p + h);
-                                x[h] = col < nbt ? lds_elem<DT>(stg, col)
-                                     : col < nv  ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes)
-                                                 : -INFINITY;
-                                y[h] = col < nbr ? lds_elem<DR>(stg + kStageT, col)
-                                     : col < nv  ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes)
-                                                 : -INFINITY;
+                        for (int p = 0; p < 8; ++p) {
+                            const int col0 = slot_col(t, 2 * p);  // the pair is col0, col0 + 1
+                            if (col0 + 1 >= min(nbt, nbr)) {
+                                float x[2] = {f2_lo(vt[p]), f2_hi(vt[p])}, y[2] = {f2_lo(vr[p]), f2_hi(vr[p])};
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int col = col0 + h;
+                                    if (col >= nbt) x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
+                                    if (col >= nbr) y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
+                                    if (kXform && col < nv) {
+                                        x[h] = xform1(x[h], a.xt);
+                                        y[h] = xform1(y[h], a.xr);
+                                    }
+                                }
+                                vt[p] = f2(x[0], x[1]);
+                                vr[p] = f2(y[0], y[1]);
+                            } else if (kXform) {
+                                vt[p] = f2(xform1(f2_lo(vt[p]), a.xt), xform1(f2_hi(vt[p]), a.xt));
+                                vr[p] = f2(xform1(f2_lo(vr[p]), a.xr), xform1(f2_hi(vr[p]), a.xr));
                             }
-                            vt[p] = f2(x[0], x[1]);
-                            vr[p] = f2(y[0], y[1]);
                         }
                     }
                     __syncwarp();
@@ -304,6 +327,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             const int col = slot_col(t, 2 * p + h);
                             x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                             y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
+                            if (kXform && col < nv) {
+                                x[h] = xform1(x[h], a.xt);
+                                y[h] = xform1(y[h], a.xr);
+                            }
                         }
                         vt[p] = f2(x[0], x[1]);
                         vr[p] = f2(y[0], y[1]);
@@ -334,12 +361,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
     }
 }
 
-template <class DT, class DR, bool kTma>
+template <class DT, class DR, bool kTma, bool kXform>
 cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     const int stage_bytes = kTile * (DT::kBytes + DR::kBytes);
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
-    auto kern = row_kernel<DT, DR, kTma>;
+    auto kern = row_kernel<DT, DR, kTma, kXform>;
     static int configured_device = -1;  // attribute is per device; cheap to repeat
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -353,18 +380,23 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool kTma>
+template <bool kTma, bool kXform>
 cudaError_t dispatch(const RowArgs &a, int dt, int dr, cudaStream_t stream) {
-    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma>(a, stream);
-    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma>(a, stream);
-    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma>(a, stream);
-    return launch_typed<F32, F32, kTma>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kXform>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kXform>(a, stream);
+    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kXform>(a, stream);
+    return launch_typed<F32, F32, kTma, kXform>(a, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, cudaStream_t stream) {
-    return use_tma ? dispatch<true>(a, dtype_t, dtype_r, stream) : dispatch<false>(a, dtype_t, dtype_r, stream);
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, bool use_xform,
+                        cudaStream_t stream) {
+    if (use_xform)
+        return use_tma ? dispatch<true, true>(a, dtype_t, dtype_r, stream)
+                       : dispatch<false, true>(a, dtype_t, dtype_r, stream);
+    return use_tma ? dispatch<true, false>(a, dtype_t, dtype_r, stream)
+                   : dispatch<false, false>(a, dtype_t, dtype_r, stream);
 }
 
 }  // namespace lpd

@@ -176,3 +176,27 @@ def test_fused_workspace_size():
     assert small > 0 and small % 256 == 0
     # dense hidden copies dominate: 2 sides x 128 padded rows x 4096 x 2 B
     assert B.lpd_fused_workspace_size(128, 4096, 1000) >= 2 * 128 * 4096 * 2
+
+
+@pytest.mark.parametrize("ops", [
+    [(3, 1.0)],                      # unknown kind
+    [(B.LPD_OP_SCALE, 0.0)],         # non-positive
+    [(B.LPD_OP_SCALE, -2.0)],
+    [(B.LPD_OP_SOFTCAP, float("inf"))],
+    [(B.LPD_OP_SOFTCAP, float("nan"))],
+])
+def test_transform_chain_rejected(ops):
+    t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 16)
+    c = B.transform_struct(ops)
+    rc = B.lib().lpd_score_transformed(ctypes.byref(t), ctypes.byref(t), None, ctypes.byref(c), 8, 16, FAKE, FAKE,
+                                       0.8, 1.2, None, None, None, FAKE, WS_OK, 1 << 20, None)
+    assert rc == B.LPD_ERR_BAD_TRANSFORM
+
+
+def test_transform_chain_too_long():
+    t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 16)
+    c = B.transform_struct([(B.LPD_OP_SCALE, 1.0)] * 4)
+    c.n_ops = 5
+    rc = B.lib().lpd_score_transformed(ctypes.byref(t), ctypes.byref(t), ctypes.byref(c), None, 8, 16, FAKE, FAKE,
+                                       0.8, 1.2, None, None, None, FAKE, WS_OK, 1 << 20, None)
+    assert rc == B.LPD_ERR_BAD_TRANSFORM

@@ -1,0 +1,86 @@
+"""Vocab padding policies and the logit transform chain ("[WS2] Framework
+for ablation experiment", LogProb knobs table, rows 2 and 7) against the
+float64 oracle (needs a GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from logprob_drift_scoring_gb300 import binding as B
+from logprob_drift_scoring_gb300 import workloads as W
+from tests.helpers import LOGP_ATOL, assert_metrics_match, to_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SCALE, SOFTCAP = B.LPD_OP_SCALE, B.LPD_OP_SOFTCAP
+
+
+def _check(w, train_ops, rollout_ops, train=None, rollout=None):
+    train = w.train if train is None else train
+    rollout = w.rollout if rollout is None else rollout
+    res = B.score(train, rollout, w.token_ids, w.action_mask, w.clip, train_ops=train_ops, rollout_ops=rollout_ops)
+    torch.cuda.synchronize()
+    mask = w.action_mask.cpu().numpy()
+    ref = oracle.score_transformed(to_oracle(train), to_oracle(rollout), w.token_ids.cpu().numpy(), mask,
+                                   train_ops, rollout_ops, *w.clip)
+    act = mask != 0
+    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout),
+                      (res.dlogp, ref.dlogp)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g[act] - want[act])) <= LOGP_ATOL
+    assert_metrics_match(res.metrics, ref.metrics, ref.dlogp, mask, w.clip)
+    return res, ref
+
+
+@pytest.mark.parametrize("train_ops,rollout_ops", [
+    ([(SCALE, 1 / 0.7)], [(SCALE, 1 / 0.7)]),                       # same temperature both sides
+    ([(SOFTCAP, 30.0)], [(SOFTCAP, 30.0)]),                         # soft-cap
+    ([(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]),
+    ([], [(SCALE, 1 / 0.7)]),                                       # temperature applied on one side only
+    ([(SCALE, 1 / 0.7), (SOFTCAP, 30.0)], [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]),  # order mismatch
+])
+@pytest.mark.parametrize("shape", [(300, 3 * 8192 + 520, 0), (150, 12805, 3), (200, 5000, 0)])
+def test_transform_chain_vs_oracle(train_ops, rollout_ops, shape):
+    rows, vocab, pad = shape
+    w = W.synthetic(rows, vocab, seed=rows + vocab, device=DEV, row_pad=pad, spike_frac=0.05, spike=40.0)
+    _check(w, train_ops, rollout_ops)
+
+
+def test_identity_chain_is_bitwise_lpd_score():
+    w = W.synthetic(250, 20000, seed=31, device=DEV)
+    plain = B.score(w.train, w.rollout, w.token_ids, w.action_mask)
+    ident = B.score(w.train, w.rollout, w.token_ids, w.action_mask, train_ops=[], rollout_ops=[])
+    torch.cuda.synchronize()
+    for a, b in ((plain.logp_train, ident.logp_train), (plain.dlogp, ident.dlogp)):
+        assert torch.equal(a, b)
+
+
+def test_same_chain_both_sides_keeps_identical_rows_at_zero():
+    w = W.synthetic(120, 9000, seed=32, device=DEV)
+    ops = [(SOFTCAP, 20.0), (SCALE, 1.3)]
+    res = B.score(w.train, w.train, w.token_ids, w.action_mask, train_ops=ops, rollout_ops=ops)
+    torch.cuda.synchronize()
+    assert torch.all(res.dlogp == 0) and res.metrics["approx_kl0"] == 0.0
+
+
+@pytest.mark.parametrize("policy", ["mask", "include"])
+def test_vocab_padding_policies(policy):
+    # padded vocab: 12288 columns stored, the first 12000 are the real vocabulary;
+    # "mask" scores with vocab = 12000 and the padding never enters the LSE,
+    # "include" scores all 12288 columns (pad rows initialised to 0 here)
+    real, padded = 12000, 12288
+    base = W.synthetic(160, padded, seed=33, device=DEV)
+    train = base.train.clone()
+    rollout = base.rollout.clone()
+    train[:, real:] = 0.0
+    rollout[:, real:] = 0.0
+    ids = torch.remainder(base.token_ids, real)
+    vocab = real if policy == "mask" else padded
+    w = W.Workload("pad", train[:, :vocab], rollout[:, :vocab], ids, base.action_mask, vocab)
+    res, ref = _check(w, None, None)
+    # the two policies differ by exactly the padding's probability mass
+    if policy == "include":
+        other = oracle.score(to_oracle(train[:, :real]), to_oracle(rollout[:, :real]), ids.cpu().numpy(),
+                             base.action_mask.cpu().numpy())
+        act = base.action_mask.cpu().numpy() != 0
+        assert np.all(ref.logp_train[act] < other.logp_train[act])
