@@ -137,17 +137,38 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
 
 // The logit transform chain ("[WS2] Framework for ablation experiment", LogProb
 // knobs table, row 7), applied in order to one logit in fp32: scale x * p
-// (temperature 1/T or logit scale) or soft-cap p * tanh(x / p).  Only real
-// columns are transformed; masked tail columns stay -inf.
-__device__ __forceinline__ float xform1(float x, const Xform &c) {
-    for (int k = 0; k < c.n_ops; ++k) {
-        const float p = c.param[k];
-        x = c.kind[k] == LPD_OP_SCALE ? __fmul_rn(x, p) : __fmul_rn(p, tanhf(__fdiv_rn(x, p)));
+// (temperature 1/T or logit scale) or soft-cap p * tanh(x * (1/p)).  The chain
+// is copied into registers once per thread (constant indices only, so it never
+// lives in local memory); ops past n are skipped.  Only real columns are
+// transformed; masked tail columns stay -inf.
+struct XformRegs {
+    int n;
+    int kind[LPD_MAX_TRANSFORM_OPS];
+    float p[LPD_MAX_TRANSFORM_OPS], rcp[LPD_MAX_TRANSFORM_OPS];
+};
+
+__device__ __forceinline__ XformRegs xform_regs(const Xform &c) {
+    XformRegs r;
+    r.n = c.n_ops;
+#pragma unroll
+    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
+        r.kind[k] = c.kind[k];
+        r.p[k] = c.param[k];
+        r.rcp[k] = k < c.n_ops ? __frcp_rn(c.param[k]) : 0.f;
+    }
+    return r;
+}
+
+__device__ __forceinline__ float xform1(float x, const XformRegs &c) {
+#pragma unroll
+    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
+        if (k < c.n)
+            x = c.kind[k] == LPD_OP_SCALE ? __fmul_rn(x, c.p[k]) : __fmul_rn(c.p[k], tanhf(__fmul_rn(x, c.rcp[k])));
     }
     return x;
 }
 
-__device__ __forceinline__ void xform16(f2_t *v, const Xform &c) {
+__device__ __forceinline__ void xform16(f2_t *v, const XformRegs &c) {
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = f2(xform1(f2_lo(v[p]), c), xform1(f2_hi(v[p]), c));
 }
@@ -234,6 +255,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
     // ---------------------------------------------------------- consumers
     const int t = threadIdx.x;
+    XformRegs cxt, cxr;
+    if (kXform) {
+        cxt = xform_regs(a.xt);
+        cxr = xform_regs(a.xr);
+    }
     uint32_t it = 0;
     for (int64_t i = blockIdx.x; i < n_active; i += gridDim.x) {
         const int2 rid = a.rowid[i];
@@ -277,8 +303,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
                         }
                         if (kXform) {
-                            xform16(vt, a.xt);
-                            xform16(vr, a.xr);
+                            xform16(vt, cxt);
+                            xform16(vr, cxr);
                         }
                     } else {
                         // ragged last tile: the same vector loads, then the
@@ -303,15 +329,15 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                                     if (col >= nbt) x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                                     if (col >= nbr) y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
                                     if (kXform && col < nv) {
-                                        x[h] = xform1(x[h], a.xt);
-                                        y[h] = xform1(y[h], a.xr);
+                                        x[h] = xform1(x[h], cxt);
+                                        y[h] = xform1(y[h], cxr);
                                     }
                                 }
                                 vt[p] = f2(x[0], x[1]);
                                 vr[p] = f2(y[0], y[1]);
                             } else if (kXform) {
-                                vt[p] = f2(xform1(f2_lo(vt[p]), a.xt), xform1(f2_hi(vt[p]), a.xt));
-                                vr[p] = f2(xform1(f2_lo(vr[p]), a.xr), xform1(f2_hi(vr[p]), a.xr));
+                                vt[p] = f2(xform1(f2_lo(vt[p]), cxt), xform1(f2_hi(vt[p]), cxt));
+                                vr[p] = f2(xform1(f2_lo(vr[p]), cxr), xform1(f2_hi(vr[p]), cxr));
                             }
                         }
                     }
@@ -328,8 +354,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                             y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
                             if (kXform && col < nv) {
-                                x[h] = xform1(x[h], a.xt);
-                                y[h] = xform1(y[h], a.xr);
+                                x[h] = xform1(x[h], cxt);
+                                y[h] = xform1(y[h], cxr);
                             }
                         }
                         vt[p] = f2(x[0], x[1]);
