@@ -122,6 +122,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.lpdo_head_logits.argtypes = [P, P, I64, I64, P]
     lib.lpdo_score_transformed.restype = U32
     lib.lpdo_score_transformed.argtypes = [P, I32, I64, P, I32, I64, P, P, I64, I64, P, P, D, D, P, P, P, P]
+    lib.lpdo_row_entropy.restype = D
+    lib.lpdo_row_entropy.argtypes = [P, I32, I64]
+    lib.lpdo_entropy.restype = None
+    lib.lpdo_entropy.argtypes = [P, I32, I64, P, I32, I64, I64, I64, P, P, P]
+    lib.lpdo_logprob_backward_row.restype = None
+    lib.lpdo_logprob_backward_row.argtypes = [P, I32, I64, I64, D, P]
     lib.lpdo_score_head_rows.restype = U32
     lib.lpdo_score_head_rows.argtypes = [P, P, P, I64, I64, P, P, I64, P, P, P]
     return lib
@@ -317,3 +323,32 @@ def score_transformed(train, rollout, token_ids, mask, train_ops=None, rollout_o
                                     n_rows, vocab, _ptr(ids), _ptr(m8), float(clip_lo), float(clip_hi),
                                     _ptr(lt), _ptr(lr), _ptr(d), ctypes.addressof(met))
     return Result(lt, lr, d, int(st), met.as_dict())
+
+
+def row_entropy(row, lib=None) -> float:
+    """Entropy of the softmax of one 1-D row."""
+    lib = lib or load()
+    row = np.ascontiguousarray(row)
+    code = BF16 if row.dtype == np.uint16 else F32
+    return float(lib.lpdo_row_entropy(_ptr(row), code, row.shape[0]))
+
+
+def entropy(train, rollout, mask, lib=None):
+    """Per-row entropies of both sides (0 where inactive)."""
+    lib = lib or load()
+    t, tc, ts = _logits_arg(train)
+    r, rc, rs = _logits_arg(rollout)
+    m8 = np.ascontiguousarray(mask, dtype=np.uint8)
+    et, er = np.zeros(t.shape[0]), np.zeros(t.shape[0])
+    lib.lpdo_entropy(_ptr(t), tc, ts, _ptr(r), rc, rs, t.shape[0], t.shape[1], _ptr(m8), _ptr(et), _ptr(er))
+    return et, er
+
+
+def logprob_backward_row(row, token_id: int, grad: float, lib=None) -> np.ndarray:
+    """grad * d logp[token_id] / d logits for one 1-D row, in double."""
+    lib = lib or load()
+    row = np.ascontiguousarray(row)
+    code = BF16 if row.dtype == np.uint16 else F32
+    out = np.zeros(row.shape[0])
+    lib.lpdo_logprob_backward_row(_ptr(row), code, row.shape[0], int(token_id), float(grad), _ptr(out))
+    return out

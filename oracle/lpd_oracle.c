@@ -25,6 +25,8 @@
  *   [HD]  same table, rows 9-10: the LM-head GEMM that produces the logits.
  *   [TC]  same table, row 7: an ordered chain of logit transforms (temperature,
  *         soft-cap, logit scale) applied to every logit before the softmax.
+ *   [TS]  same table, row 11: training-only state, i.e. the entropy of the
+ *         softmax and the logprob's gradient with respect to the logits.
  *
  * Readings where the pages are silent (each is also listed with the design
  * notes): percentiles are nearest-rank (1-based rank ceil(p*A/100) of the
@@ -466,4 +468,53 @@ uint32_t lpdo_score_transformed(const void *train, int train_dtype, int64_t trai
         metrics->status = status;
     }
     return status;
+}
+
+/* ---- training-only state [TS] ------------------------------------------- */
+
+/* Entropy of the softmax of one row: H = -sum_j p_j log p_j with
+ * p_j = exp(x_j - lse), written as H = lse - sum_j p_j x_j (serial in j). */
+double lpdo_row_entropy(const void *row, int dtype, int64_t vocab)
+{
+    double m, s;
+    lpdo_partial(row, dtype, 0, vocab, &m, &s);
+    double lse = lse_of(m, s);
+    double px = 0.0;
+    for (int64_t j = 0; j < vocab; ++j) {
+        double x = logit_at(row, dtype, j);
+        double p = exp(x - lse);
+        if (p > 0.0)
+            px += p * x;
+    }
+    return lse - px;
+}
+
+/* Entropies of both sides for every active row (0 where inactive). */
+void lpdo_entropy(const void *train, int train_dtype, int64_t train_stride,
+                  const void *rollout, int rollout_dtype, int64_t rollout_stride,
+                  int64_t n_rows, int64_t vocab, const uint8_t *mask,
+                  double *ent_train, double *ent_rollout)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        ent_train[r] = ent_rollout[r] = 0.0;
+        if (!mask[r])
+            continue;
+        ent_train[r] = lpdo_row_entropy(row_ptr(train, train_dtype, train_stride, r), train_dtype, vocab);
+        ent_rollout[r] = lpdo_row_entropy(row_ptr(rollout, rollout_dtype, rollout_stride, r),
+                                          rollout_dtype, vocab);
+    }
+}
+
+/* Gradient of grad * logp(x)[id] with respect to the row's logits:
+ *   d/dx_j = grad * (1[j == id] - p_j),  p_j = exp(x_j - lse). */
+void lpdo_logprob_backward_row(const void *row, int dtype, int64_t vocab, int64_t id, double grad,
+                               double *out)
+{
+    double m, s;
+    lpdo_partial(row, dtype, 0, vocab, &m, &s);
+    double lse = lse_of(m, s);
+    for (int64_t j = 0; j < vocab; ++j) {
+        double p = exp(logit_at(row, dtype, j) - lse);
+        out[j] = grad * ((j == id ? 1.0 : 0.0) - p);
+    }
 }

@@ -487,3 +487,59 @@ def pin_transform_per_side(lib):
 
 
 ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+# ------------------------------------------------- entropy and backward pins
+
+def pin_entropy_closed_forms(lib):
+    for vocab in (1, 2, 7, 1000):
+        _close(oracle.row_entropy(np.full(vocab, 2.5, np.float32), lib=lib), math.log(vocab), 1e-12, "uniform H")
+    rng = np.random.default_rng(71)
+    for _ in range(10):
+        x = rng.normal(0, 3, size=2).astype(np.float32)
+        p = 1.0 / (1.0 + math.exp(float(x[1]) - float(x[0])))
+        want = -(p * math.log(p) + (1 - p) * math.log(1 - p)) if 0 < p < 1 else 0.0
+        _close(oracle.row_entropy(x, lib=lib), want, 1e-12, "two-token H")
+    peaked = np.zeros(50, np.float32)
+    peaked[7] = 80.0
+    assert 0.0 <= oracle.row_entropy(peaked, lib=lib) < 1e-30
+
+
+def pin_entropy_decimal(lib):
+    rng = np.random.default_rng(72)
+    for vocab in (3, 9, 16):
+        x = rng.normal(0, 3, size=vocab).astype(np.float32)
+        vals = [Decimal(float(v)) for v in x]
+        z = sum((v.exp() for v in vals), Decimal(0))
+        h = -sum(((v.exp() / z) * (v - z.ln()) for v in vals), Decimal(0))
+        _close(oracle.row_entropy(x, lib=lib), float(h), 1e-12, "decimal H")
+
+
+def pin_backward_finite_differences(lib):
+    rng = np.random.default_rng(73)
+    x = rng.normal(0, 2, size=12)
+    idx, grad, eps = 5, -0.75, 1e-6
+
+    def logp(v):
+        return float(dec_logp(v, idx))
+
+    g = oracle.logprob_backward_row(x.astype(np.float32), idx, grad, lib=lib)
+    xf = x.astype(np.float32).astype(np.float64)
+    for j in range(12):
+        hi, lo = xf.copy(), xf.copy()
+        hi[j] += eps
+        lo[j] -= eps
+        fd = grad * (logp(hi) - logp(lo)) / (2 * eps)
+        _close(g[j], fd, 1e-8, f"d logp / d x_{j}")
+    _close(float(np.sum(g)), 0.0, 1e-14, "gradient sums to zero")
+
+
+def pin_backward_uniform(lib):
+    vocab, idx, grad = 40, 3, 2.0
+    g = oracle.logprob_backward_row(np.zeros(vocab, np.float32), idx, grad, lib=lib)
+    for j in range(vocab):
+        want = grad * ((1.0 if j == idx else 0.0) - 1.0 / vocab)
+        _close(g[j], want, 1e-15, "uniform gradient")
+
+
+ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}

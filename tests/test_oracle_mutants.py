@@ -54,6 +54,10 @@ MUTANTS = {
     "chain_skips_selected": ("double xs = apply_chain(c, logit_at(row, dtype, id));",
                              "double xs = logit_at(row, dtype, id);"),
     "chain_wrong_side": ("token_ids[r], rollout_chain, &logp_rollout[r]);", "token_ids[r], train_chain, &logp_rollout[r]);"),
+    "entropy_sign": ("    return lse - px;\n}", "    return px - lse;\n}"),
+    "entropy_drops_lse": ("    return lse - px;\n}", "    return -px;\n}"),
+    "backward_onehot_dropped": ("out[j] = grad * ((j == id ? 1.0 : 0.0) - p);", "out[j] = grad * (0.0 - p);"),
+    "backward_sign": ("out[j] = grad * ((j == id ? 1.0 : 0.0) - p);", "out[j] = grad * (p - (j == id ? 1.0 : 0.0));"),
     "nonfinite_unflagged": ("return (isfinite(lse) && isfinite(xs)) ? 0u : LPDO_STATUS_NONFINITE;\n}\n\nstatic int",
                             "return 0u;\n}\n\nstatic int"),
 }
