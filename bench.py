@@ -201,12 +201,30 @@ class Runner:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.launches_per_step = 5 if n > 0 else 2
         self.chain = None
+        self.entropy = None      # [ent_train, ent_rollout] when timing lpd_score_entropy
+        self.backward = None     # (grad, out_dlogits) when timing lpd_logprob_backward
 
     def step(self, ev=None):
         """One pass of the path; with ev = (e0, e1, e2, e3) records events
         around stage 1, stage 2 and stage 3 on the current stream."""
         B, w = self.B, self.w
         lt, lr, d = self.outs
+        if self.backward is not None:
+            grad, out = self.backward
+            if ev:
+                ev[0].record()
+            B.lpd_logprob_backward(w.train, w.token_ids, w.action_mask, lt, grad, out)
+            if ev:
+                ev[3].record()
+            return
+        if self.entropy is not None:
+            if ev:
+                ev[0].record()
+            B.lpd_score_entropy(w.train, w.rollout, w.token_ids, w.action_mask, *w.clip, lt, lr, d, *self.entropy,
+                                self.met, self.ws)
+            if ev:
+                ev[3].record()
+            return
         if self.chain is not None:
             if ev:
                 ev[0].record()
@@ -386,10 +404,25 @@ def run_ours(args):
             dist.destroy_process_group()
         return out
     runner = Runner(w)
-    if args.transform:
-        runner.chain = parse_chain(args.transform)
     n_active = int(w.action_mask.sum().item())
     bpt = bytes_per_active_token(w)
+    extra_bytes = 0
+    if args.transform:
+        runner.chain = parse_chain(args.transform)
+    if args.entropy:
+        runner.entropy = [torch.empty(w.n_rows, dtype=torch.float32, device=dev) for _ in range(2)]
+        bpt += 8
+    if args.backward:
+        runner.step()  # the forward's logp feeds the backward
+        torch.cuda.synchronize()
+        g = torch.Generator(device=dev).manual_seed(11)
+        grad = torch.randn(w.n_rows, generator=g, device=dev)
+        out = torch.empty((w.n_rows, w.vocab), dtype=torch.bfloat16, device=dev)
+        runner.backward = (grad, out)
+        # one read of the train row and one bf16 write per active row; inactive rows are zero-filled
+        elt = w.train.element_size()
+        bpt = w.vocab * (elt + 2) + 12
+        extra_bytes = (w.n_rows - n_active) * w.vocab * 2
 
     for _ in range(args.warmup):
         runner.step()
@@ -412,7 +445,8 @@ def run_ours(args):
     ms_step = total_ms / K
     value = world * n_active / (ms_step / 1e3)
 
-    if runner.sharded or runner.chain is not None:
+    whole = runner.sharded or runner.chain is not None or runner.entropy is not None or runner.backward is not None
+    if whole:
         stage2 = sum(e[0].elapsed_time(e[3]) for e in evs) / K
         stage_ms = {"whole_call": stage2}
     else:
@@ -422,17 +456,16 @@ def run_ours(args):
         stage_ms = {"select_active": round(s1, 4), "token_logp": round(stage2, 4), "drift_metrics": round(s3, 4)}
 
     peaks = measured_peaks()
-    achieved = n_active * bpt / (stage2 / 1e3) / 1e9
+    achieved = (n_active * bpt + extra_bytes) / (stage2 / 1e3) / 1e9
     traffic = profiled_traffic(args.config)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": f"{peaks['source']} copy bandwidth (burst)",
-                "span": "whole call" if (runner.sharded or runner.chain is not None)
-                else "stage 2: row kernel + per-row finalise",
-                "algorithmic_bytes_per_launch": n_active * bpt}
+                "span": "whole call" if whole else "stage 2: row kernel + per-row finalise",
+                "algorithmic_bytes_per_launch": n_active * bpt + extra_bytes}
 
     e2e = None
-    if not args.no_e2e and not runner.sharded:
+    if not args.no_e2e and not whole:
         e2e = run_e2e(w, args, world)
     out = None
     if rank == 0:
@@ -445,7 +478,8 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": (CONFIGS[args.config]["workload"] if not (args.batch or args.seq)
                                     else f"{args.config} reduced B={args.batch} T={args.seq}")
-                       + (f" + transform {args.transform}" if args.transform else ""),
+                       + (f" + transform {args.transform}" if args.transform else "")
+                       + (" + entropy" if args.entropy else "") + (" [logprob backward, bf16 out]" if args.backward else ""),
                        "rows": w.n_rows, "active_tokens": n_active,
                        "vocab": w.vocab, "logits_bytes": w.logits_bytes(), "l2": "inputs exceed L2 (no flush)",
                        "parallelism": f"replicas x{world}", "input_dtypes": _dtypes(w)},
@@ -453,7 +487,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": runner.launches_per_step * K if not runner.sharded else 5 * K,
+            "gpu_launches": (1 if runner.backward is not None else runner.launches_per_step) * K,
             "clocks": clocks.summary(),
             "impl": "lpd",
         }
@@ -578,6 +612,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--transform", default=None,
                     help="logit transform chain on both sides, e.g. softcap:30,scale:1.4286")
+    ap.add_argument("--entropy", action="store_true", help="time lpd_score_entropy instead of lpd_score")
+    ap.add_argument("--backward", action="store_true", help="time lpd_logprob_backward of the train side")
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")
     ap.add_argument("--seq", type=int, default=None, help="override T (small profiling cases only)")
     args = ap.parse_args(argv)

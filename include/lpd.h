@@ -235,6 +235,34 @@ int lpd_score_transformed(const lpd_logits *train, const lpd_logits *rollout,
                           lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                           void *stream);
 
+/* lpd_score plus the entropy of each side's softmax per active token
+ * ("[WS2] Framework for ablation experiment", LogProb knobs table, row 11:
+ * training-only state), H = -sum_j p_j log p_j, accumulated in the same single
+ * read of each row.  out_entropy_train / out_entropy_rollout are device
+ * float32[n_rows] (at least one non-NULL; inactive rows receive 0). */
+int lpd_score_entropy(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows,
+                      int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask,
+                      double clip_lo, double clip_hi, float *out_logp_train,
+                      float *out_logp_rollout, float *out_dlogp, float *out_entropy_train,
+                      float *out_entropy_rollout, lpd_metrics *out_metrics, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Gradient of the selected-token logprob with respect to the logits, for one
+ * side (row 11 of the same table): for every active row r and column j,
+ *   out[r, j] = grad_logp[r] * (1[j == token_ids[r]] - exp(x[r, j] - lse[r])),
+ * with lse[r] = x[r, token_ids[r]] - logp[r] taken from this row's logp as
+ * returned by the scoring calls; inactive rows receive 0.  One read of the
+ * logits and one write of the gradient.
+ * logits       the side's lpd_logits [n_rows, vocab] (any row stride).
+ * logp         device float32[n_rows], grad_logp device float32[n_rows].
+ * out_dlogits  device [n_rows, out_row_stride] of out_dtype (LPD_BF16 or
+ *              LPD_F32), columns [0, vocab) written.
+ * An active row whose id is outside [0, vocab) receives NaN. */
+int lpd_logprob_backward(const lpd_logits *logits, int64_t n_rows, int64_t vocab,
+                         const int32_t *token_ids, const uint8_t *action_mask, const float *logp,
+                         const float *grad_logp, void *out_dlogits, int32_t out_dtype,
+                         int64_t out_row_stride, void *stream);
+
 /* Vocab-sharded scoring ("[WS2] Framework for ablation experiment", LogProb
  * knobs table, rows 3-5 and 8).  Each side's vocabulary arrives as n_shards
  * tensors whose [v_start, v_end) ranges must tile [0, vocab) exactly, in any

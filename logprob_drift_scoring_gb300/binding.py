@@ -83,7 +83,8 @@ METRICS_BYTES = ctypes.sizeof(LpdMetrics)
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
-            "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed")
+            "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed", "lpd_score_entropy",
+            "lpd_logprob_backward")
 LPD_NOALLOC_MAX_ROWS = 32768
 
 
@@ -125,6 +126,10 @@ def lib() -> ctypes.CDLL:
         L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_transformed.restype = ctypes.c_int
         L.lpd_score_transformed.argtypes = [P, P, P, P, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
+        L.lpd_score_entropy.restype = ctypes.c_int
+        L.lpd_score_entropy.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P, P, P, SZ, P]
+        L.lpd_logprob_backward.restype = ctypes.c_int
+        L.lpd_logprob_backward.argtypes = [P, I64, I64, P, P, P, P, P, I32, I64, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
         _LIB = L
@@ -216,6 +221,27 @@ def lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, act
                                      _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics),
                                      _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "lpd_score_transformed")
+
+
+def lpd_score_entropy(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
+                      out_dlogp, out_entropy_train, out_entropy_rollout, out_metrics, workspace, stream=None) -> None:
+    t, r = logits_struct(train), logits_struct(rollout)
+    rc = lib().lpd_score_entropy(ctypes.byref(t), ctypes.byref(r), train.shape[0], train.shape[1], _ptr(token_ids),
+                                 _ptr(action_mask), float(clip_lo), float(clip_hi), _ptr(out_logp_train),
+                                 _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_entropy_train),
+                                 _ptr(out_entropy_rollout), _ptr(out_metrics), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(rc, "lpd_score_entropy")
+
+
+def lpd_logprob_backward(logits, token_ids, action_mask, logp, grad_logp, out_dlogits, stream=None) -> None:
+    x = logits_struct(logits)
+    if out_dlogits.dim() != 2 or (out_dlogits.shape[1] > 1 and out_dlogits.stride(1) != 1):
+        raise ValueError("out_dlogits must be 2-D with contiguous columns")
+    rc = lib().lpd_logprob_backward(ctypes.byref(x), logits.shape[0], logits.shape[1], _ptr(token_ids),
+                                    _ptr(action_mask), _ptr(logp), _ptr(grad_logp), _ptr(out_dlogits),
+                                    _dtype_code(out_dlogits), out_dlogits.stride(0), _stream(stream))
+    _check(rc, "lpd_logprob_backward")
 
 
 def lpd_select_active(token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace,

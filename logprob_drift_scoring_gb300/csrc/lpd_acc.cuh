@@ -33,16 +33,27 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// ht, hr (entropy variant only, else 0): sum of e_j * a_j per side, where
+// e_j = 2^a_j is the term and a_j = (x_j - m) log2(e) its exponent, so that
+// the softmax entropy is H = ln(s) - ln(2) * h / s.  When the max moves by
+// delta = (m_old - m_new) log2(e) and the terms are scaled by f = 2^delta,
+// h becomes f * (h + delta * s).
 struct Acc {
-    float mt, st, dd, mr, sr;
+    float mt, st, dd, mr, sr, ht, hr;
 };
 
 __device__ __forceinline__ Acc acc_init() {
     Acc a;
     a.mt = -FLT_MAX;
     a.mr = -FLT_MAX;
-    a.st = a.dd = a.sr = 0.f;
+    a.st = a.dd = a.sr = a.ht = a.hr = 0.f;
     return a;
+}
+
+// f * (h + delta * s), with an empty state (s == 0, delta possibly -inf)
+// contributing exactly 0.
+__device__ __forceinline__ float ent_rescale(float h, float s, float f, float delta) {
+    return s == 0.f ? 0.f : __fmul_rn(f, __fmaf_rn(delta, s, h));
 }
 
 // f - g for f = 2^alpha, g = 2^beta, accurate when alpha ~ beta.
@@ -70,6 +81,8 @@ __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
     const float fa = ex2(aa), fb = ex2(ab), ga = ex2(ba), gb = ex2(bb);
     const float xa = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(a.sr, scale_diff(fa, ga, aa, ba)));
     const float xb = __fadd_rn(__fmul_rn(b.dd, fb), __fmul_rn(b.sr, scale_diff(fb, gb, ab, bb)));
+    a.ht = __fadd_rn(ent_rescale(a.ht, a.st, fa, aa), ent_rescale(b.ht, b.st, fb, ab));
+    a.hr = __fadd_rn(ent_rescale(a.hr, a.sr, ga, ba), ent_rescale(b.hr, b.sr, gb, bb));
     a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
     a.sr = __fadd_rn(__fmul_rn(a.sr, ga), __fmul_rn(b.sr, gb));
     a.dd = __fadd_rn(xa, xb);
@@ -105,6 +118,11 @@ __device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+    f2_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 __device__ __forceinline__ f2_t ex2_2(f2_t a) { return f2(ex2(f2_lo(a)), ex2(f2_hi(a))); }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -119,14 +137,14 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // segment.
 struct Acc2 {
     float mt, mr;
-    f2_t st, sr, dd;
+    f2_t st, sr, dd, ht, hr;
 };
 
 __device__ __forceinline__ Acc2 acc2_init() {
     Acc2 a;
     a.mt = -FLT_MAX;
     a.mr = -FLT_MAX;
-    a.st = a.sr = a.dd = f2(0.f, 0.f);
+    a.st = a.sr = a.dd = a.ht = a.hr = f2(0.f, 0.f);
     return a;
 }
 
@@ -137,7 +155,14 @@ __device__ __forceinline__ Acc acc2_fold(const Acc2 &a) {
     r.st = __fadd_rn(f2_lo(a.st), f2_hi(a.st));
     r.sr = __fadd_rn(f2_lo(a.sr), f2_hi(a.sr));
     r.dd = __fadd_rn(f2_lo(a.dd), f2_hi(a.dd));
+    r.ht = __fadd_rn(f2_lo(a.ht), f2_hi(a.ht));
+    r.hr = __fadd_rn(f2_lo(a.hr), f2_hi(a.hr));
     return r;
+}
+
+// packed form of ent_rescale (both halves share f and delta, not s)
+__device__ __forceinline__ f2_t ent_rescale2(f2_t h, f2_t s, float f, float delta) {
+    return f2(ent_rescale(f2_lo(h), f2_lo(s), f, delta), ent_rescale(f2_hi(h), f2_hi(s), f, delta));
 }
 
 __device__ __forceinline__ float max16(const f2_t *v) {
@@ -159,6 +184,7 @@ __device__ __forceinline__ f2_t tree8(const f2_t *e) {
 // rescaled at most once per chunk; the sixteen terms of each sum are added in a
 // fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
 // -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
+template <bool kEntropy = false>
 __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a) {
     const float cmt = max16(vt), cmr = max16(vr);
     if (cmt > a.mt || cmr > a.mr) {
@@ -167,6 +193,10 @@ __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc
         const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), kLog2e);
         const float ft = ex2(at), fr = ex2(ar);
         const float corr = scale_diff(ft, fr, at, ar);
+        if (kEntropy) {
+            a.ht = ent_rescale2(a.ht, a.st, ft, at);
+            a.hr = ent_rescale2(a.hr, a.sr, fr, ar);
+        }
         a.dd = add2(mul2(a.dd, f2(ft, ft)), mul2(a.sr, f2(corr, corr)));
         a.st = mul2(a.st, f2(ft, ft));
         a.sr = mul2(a.sr, f2(fr, fr));
@@ -177,9 +207,15 @@ __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc
     f2_t et[8], er[8], dq[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        et[p] = ex2_2(mul2(sub2(vt[p], mt2), l2));
-        er[p] = ex2_2(mul2(sub2(vr[p], mr2), l2));
+        const f2_t xt = mul2(sub2(vt[p], mt2), l2), xr = mul2(sub2(vr[p], mr2), l2);
+        et[p] = ex2_2(xt);
+        er[p] = ex2_2(xr);
         dq[p] = sub2(et[p], er[p]);
+        if (kEntropy) {
+            // -inf columns give e = 0 and a = -inf: their product must count as 0
+            a.ht = fma2(et[p], f2(f2_lo(et[p]) == 0.f ? 0.f : f2_lo(xt), f2_hi(et[p]) == 0.f ? 0.f : f2_hi(xt)), a.ht);
+            a.hr = fma2(er[p], f2(f2_lo(er[p]) == 0.f ? 0.f : f2_lo(xr), f2_hi(er[p]) == 0.f ? 0.f : f2_hi(xr)), a.hr);
+        }
     }
     a.st = add2(a.st, tree8(et));
     a.sr = add2(a.sr, tree8(er));

@@ -96,14 +96,24 @@ int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *l
 }
 
 // Stage 2: the streaming row pass, then the per-row finalise.
+// Optional extras of the row pass: a transform chain per side, or entropy outputs.
+struct RowExtras {
+    const Xform *xform = nullptr;       // [2]: train, rollout
+    float *ent_t = nullptr, *ent_r = nullptr;
+};
+
 int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, const int32_t *perm, int n_perm,
              int64_t n_rows, int64_t vocab, float *lt, float *lr, float *d, float *plt, float *plr,
-             lpd_metrics *met, const Ws &w, cudaStream_t s, const Xform *xform = nullptr) {
+             lpd_metrics *met, const Ws &w, cudaStream_t s, const RowExtras &ex = RowExtras{}) {
     if (n_rows == 0) return LPD_OK;
     RowArgs a{};
-    if (xform) {
-        a.xt = xform[0];
-        a.xr = xform[1];
+    int mode = kRowPlain;
+    if (ex.xform) {
+        a.xt = ex.xform[0];
+        a.xr = ex.xform[1];
+        mode = kRowTransform;
+    } else if (ex.ent_t || ex.ent_r) {
+        mode = kRowEntropy;
     }
     for (int k = 0; k < n_seg; ++k) a.seg[k] = segs[k];
     a.n_seg = n_seg;
@@ -113,7 +123,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     a.part = w.part;
     a.pick = w.pick;
     a.status = &met->status;
-    int rc = cuda_status(launch_rows(a, dt, dr, tma, xform != nullptr, s));
+    int rc = cuda_status(launch_rows(a, dt, dr, tma, mode, s));
     if (rc) return rc;
     FinArgs f{};
     f.n_seg = n_seg;
@@ -131,6 +141,8 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     f.out_d = d;
     f.out_perm_lt = plt;
     f.out_perm_lr = plr;
+    f.out_ent_t = ex.ent_t;
+    f.out_ent_r = ex.ent_r;
     f.status = &met->status;
     return cuda_status(launch_finalize(f, n_rows, s));
 }
@@ -347,11 +359,64 @@ int lpd_score_transformed(const lpd_logits *train, const lpd_logits *rollout, co
     if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
                          w, s)))
         return rc;
-    const bool any = xf[0].n_ops > 0 || xf[1].n_ops > 0;
+    RowExtras ex;
+    if (xf[0].n_ops > 0 || xf[1].n_ops > 0) ex.xform = xf;
     if ((rc = run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
-                       out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s, any ? xf : nullptr)))
+                       out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s, ex)))
         return rc;
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+int lpd_score_entropy(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab,
+                      const int32_t *token_ids, const uint8_t *action_mask, double clip_lo, double clip_hi,
+                      float *out_logp_train, float *out_logp_rollout, float *out_dlogp, float *out_entropy_train,
+                      float *out_entropy_rollout, lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+    int rc = validate_pair(train, rollout, n_rows, vocab);
+    if (rc) return rc;
+    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    if (!out_entropy_train && !out_entropy_rollout) return LPD_ERR_NULL_POINTER;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Ws w = carve(workspace, n_rows, 1);
+    const Segment sg = whole_vocab(train, rollout, vocab);
+    const bool tma = rows_aligned(train->ptr, train->row_stride, train->dtype) &&
+                     rows_aligned(rollout->ptr, rollout->row_stride, rollout->dtype);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    // inactive rows get entropy 0, like the other per-token outputs
+    if (out_entropy_train && n_rows > 0 &&
+        (rc = cuda_status(cudaMemsetAsync(out_entropy_train, 0, n_rows * sizeof(float), s))))
+        return rc;
+    if (out_entropy_rollout && n_rows > 0 &&
+        (rc = cuda_status(cudaMemsetAsync(out_entropy_rollout, 0, n_rows * sizeof(float), s))))
+        return rc;
+    RowExtras ex;
+    ex.ent_t = out_entropy_train;
+    ex.ent_r = out_entropy_rollout;
+    if ((rc = run_rows(&sg, 1, train->dtype, rollout->dtype, tma, nullptr, 0, n_rows, vocab, out_logp_train,
+                       out_logp_rollout, out_dlogp, nullptr, nullptr, out_metrics, w, s, ex)))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+int lpd_logprob_backward(const lpd_logits *logits, int64_t n_rows, int64_t vocab, const int32_t *token_ids,
+                         const uint8_t *action_mask, const float *logp, const float *grad_logp, void *out_dlogits,
+                         int32_t out_dtype, int64_t out_row_stride, void *stream) {
+    int rc = check_rows_vocab(n_rows, vocab);
+    if (rc) return rc;
+    if ((rc = check_logits(logits, n_rows, vocab))) return rc;
+    if (n_rows > 0 && (!token_ids || !action_mask || !logp || !grad_logp || !out_dlogits))
+        return LPD_ERR_NULL_POINTER;
+    if (!valid_dtype(out_dtype)) return LPD_ERR_BAD_DTYPE;
+    if (out_row_stride < vocab) return LPD_ERR_BAD_STRIDE;
+    if (!elt_aligned(out_dlogits, out_dtype)) return LPD_ERR_ALIGNMENT;
+    return cuda_status(launch_backward(logits->ptr, logits->dtype, logits->row_stride, out_dlogits, out_dtype,
+                                       out_row_stride, n_rows, vocab, token_ids, action_mask, logp, grad_logp,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards, int64_t n_rows,

@@ -1,0 +1,151 @@
+// Gradient of the selected-token logprob with respect to the logits.
+//
+// Method: "[WS2] Framework for ablation experiment", LogProb knobs table, row
+// 11 (training-only state: the logprob's gradient must match between
+// implementations too).  For an active row r with selected id and upstream
+// gradient g = grad_logp[r]:
+//   d(g * logp[r]) / d x[r, j] = g * (1[j == id] - p_j),  p_j = exp(x[r, j] - lse[r]),
+// with lse[r] = x[r, id] - logp[r] recovered from the forward's own output, so
+// this pass reads each logits row once and writes each gradient row once.
+// Inactive rows get a zero gradient; an active row with an out-of-range id
+// gets NaN (fail closed).
+//
+// Layout: blocks of 256 threads cover 2048 columns of one row (8 per thread);
+// grid.x spans the vocabulary, grid.y strides over rows.  Rows whose input and
+// output start on 16-byte boundaries use 16-byte loads and stores.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "lpd_acc.cuh"
+#include "lpd_internal.cuh"
+
+namespace lpd {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdCols = 8 * kBwdThreads;
+
+struct BwdArgs {
+    const char *x;
+    int64_t x_stride;     // bytes
+    char *out;
+    int64_t out_stride;   // bytes
+    int64_t n_rows, vocab;
+    const int32_t *ids;
+    const uint8_t *mask;
+    const float *logp, *grad;
+    int x_bf16, out_bf16;
+    int vec;              // rows of both tensors are 16-byte aligned
+};
+
+__device__ __forceinline__ float load_x(const BwdArgs &a, const char *row, int64_t j) {
+    if (a.x_bf16)
+        return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(row) + j)) << 16);
+    return __ldg(reinterpret_cast<const float *>(row) + j);
+}
+
+__device__ __forceinline__ void store_out(const BwdArgs &a, char *row, int64_t j, float v) {
+    if (a.out_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(row)[j] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float *>(row)[j] = v;
+}
+
+__global__ void __launch_bounds__(kBwdThreads) backward_kernel(const __grid_constant__ BwdArgs a) {
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kBwdCols + 8 * threadIdx.x;
+    if (c0 >= a.vocab) return;
+    const bool full = c0 + 8 <= a.vocab;
+    for (int64_t r = blockIdx.y; r < a.n_rows; r += gridDim.y) {
+        char *orow = a.out + r * a.out_stride;
+        const char *xrow = a.x + r * a.x_stride;
+        float v[8];
+        bool write = true;
+        if (!a.mask[r]) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        } else {
+            const int64_t id = a.ids[r];
+            if (id < 0 || id >= a.vocab) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = CUDART_NAN_F;
+            } else {
+                const float lse = __fsub_rn(load_x(a, xrow, id), a.logp[r]);
+                const float g = a.grad[r];
+                float x[8];
+                if (a.vec && full) {
+                    if (a.x_bf16) {
+                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(xrow + c0 * 2));
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            x[2 * q] = __uint_as_float(ws[q] << 16);
+                            x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
+                        }
+                    } else {
+                        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4));
+                        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4) + 1);
+                        x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
+                        x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) x[q] = c0 + q < a.vocab ? load_x(a, xrow, c0 + q) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float p = ex2(__fmul_rn(__fsub_rn(x[q], lse), kLog2e));
+                    const float onehot = (c0 + q == id) ? 1.f : 0.f;
+                    v[q] = __fmul_rn(g, __fsub_rn(onehot, p));
+                }
+            }
+        }
+        if (!write) continue;
+        if (a.vec && full) {
+            if (a.out_bf16) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+                    w[q] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                *reinterpret_cast<uint4 *>(orow + c0 * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                reinterpret_cast<float4 *>(orow + c0 * 4)[0] = make_float4(v[0], v[1], v[2], v[3]);
+                reinterpret_cast<float4 *>(orow + c0 * 4)[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (c0 + q < a.vocab) store_out(a, orow, c0 + q, v[q]);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, void *out, int out_dtype,
+                            int64_t out_stride_elems, int64_t n_rows, int64_t vocab, const int32_t *ids,
+                            const uint8_t *mask, const float *logp, const float *grad, cudaStream_t stream) {
+    if (n_rows == 0) return cudaSuccess;
+    BwdArgs a{};
+    a.x = static_cast<const char *>(x);
+    a.x_bf16 = x_dtype == LPD_BF16;
+    a.x_stride = x_stride_elems * (a.x_bf16 ? 2 : 4);
+    a.out = static_cast<char *>(out);
+    a.out_bf16 = out_dtype == LPD_BF16;
+    a.out_stride = out_stride_elems * (a.out_bf16 ? 2 : 4);
+    a.n_rows = n_rows;
+    a.vocab = vocab;
+    a.ids = ids;
+    a.mask = mask;
+    a.logp = logp;
+    a.grad = grad;
+    a.vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (a.x_stride % 16 == 0) &&
+            (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (a.out_stride % 16 == 0);
+    const dim3 grid(static_cast<unsigned>((vocab + kBwdCols - 1) / kBwdCols),
+                    static_cast<unsigned>(n_rows < 65535 ? n_rows : 65535));
+    backward_kernel<<<grid, kBwdThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace lpd

@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.dd = p.z;
         o.mr = p.w;
         o.sr = part_b[i * n_n + n];
+        o.ht = o.hr = 0.f;
         merge_acc(acc, o);
     }
 #pragma unroll
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.dd = __shfl_xor_sync(0xffffffffu, acc.dd, off);
         o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
         o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
+        o.ht = o.hr = 0.f;
         merge_acc(acc, o);
     }
     if (lane != 0) return;

@@ -111,6 +111,7 @@ struct FinArgs {
     uint32_t *keys;
     float *out_lt, *out_lr, *out_d;
     float *out_perm_lt, *out_perm_lr;
+    float *out_ent_t, *out_ent_r;  // entropies (entropy mode only)
     uint32_t *status;
 };
 
@@ -142,12 +143,16 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lt, float *out_lr, float *out_d,
                                  lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
                                  cudaStream_t stream);
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, bool use_xform,
-                        cudaStream_t stream);
+constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2;
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
                            const int2 *rowid, const double *dval, const uint32_t *keys,
                            BlockPartial *bp, lpd_metrics *metrics, cudaStream_t stream);
+
+cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, void *out, int out_dtype,
+                            int64_t out_stride_elems, int64_t n_rows, int64_t vocab, const int32_t *ids,
+                            const uint8_t *mask, const float *logp, const float *grad, cudaStream_t stream);
 
 int device_sm_count();
 

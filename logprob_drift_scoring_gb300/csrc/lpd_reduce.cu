@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
         if (a.out_lr) a.out_lr[r] = CUDART_NAN_F;
         if (a.out_perm_lt) a.out_perm_lt[r] = CUDART_NAN_F;
         if (a.out_perm_lr) a.out_perm_lr[r] = CUDART_NAN_F;
+        if (a.out_ent_t) a.out_ent_t[r] = CUDART_NAN_F;
+        if (a.out_ent_r) a.out_ent_r[r] = CUDART_NAN_F;
     } else {
         const float2 xs = a.pick[i];
         Acc seg[kMaxSegments];
@@ -174,6 +176,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
                 o.dd = p0.z;
                 o.mr = p0.w;
                 o.sr = p1.x;
+                o.ht = p1.y;
+                o.hr = p1.z;
                 merge_acc(sk, o);
             }
             seg[k] = sk;
@@ -187,6 +191,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
         if (a.out_lr) a.out_lr[r] = static_cast<float>(xr - lse_r);
+        // entropy H = ln(s) - ln(2) * h / s of each side's softmax
+        if (a.out_ent_t) a.out_ent_t[r] = static_cast<float>(log(st) - 0.6931471805599453 * (double)row.ht / st);
+        if (a.out_ent_r) a.out_ent_r[r] = static_cast<float>(log(sr) - 0.6931471805599453 * (double)row.hr / sr);
         if (a.n_perm) {
             Acc pr = acc_init();
             for (int j = 0; j < a.n_perm; ++j) merge_acc(pr, seg[a.perm[j]]);

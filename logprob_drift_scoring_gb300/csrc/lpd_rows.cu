@@ -185,8 +185,11 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
     return x;
 }
 
-template <class DT, class DR, bool kTma, bool kXform>
+// kMode: 0 plain, 1 with the transform chain, 2 with the entropy sums.
+template <class DT, class DR, bool kTma, int kMode>
 __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
+    constexpr bool kXform = kMode == 1;
+    constexpr bool kEntropy = kMode == 2;
     extern __shared__ __align__(1024) char smem[];
     __shared__ int abort_flag;
     constexpr int kStageT = kTile * DT::kBytes;
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 }
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
                     a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
-                accumulate16(vt, vr, acc2);
+                accumulate16<kEntropy>(vt, vr, acc2);
             }
             Acc acc = acc2_fold(acc2);
             // fixed butterfly over the warp
@@ -376,23 +379,25 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 o.dd = __shfl_xor_sync(0xffffffffu, acc.dd, off);
                 o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
                 o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
+                o.ht = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.ht, off) : 0.f;
+                o.hr = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.hr, off) : 0.f;
                 merge_acc(acc, o);
             }
             if (lane == 0) {
                 float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;
                 dst[0] = make_float4(acc.mt, acc.st, acc.dd, acc.mr);
-                dst[1] = make_float4(acc.sr, 0.f, 0.f, 0.f);
+                dst[1] = make_float4(acc.sr, acc.ht, acc.hr, 0.f);
             }
         }
     }
 }
 
-template <class DT, class DR, bool kTma, bool kXform>
+template <class DT, class DR, bool kTma, int kMode>
 cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     const int stage_bytes = kTile * (DT::kBytes + DR::kBytes);
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
-    auto kern = row_kernel<DT, DR, kTma, kXform>;
+    auto kern = row_kernel<DT, DR, kTma, kMode>;
     static int configured_device = -1;  // attribute is per device; cheap to repeat
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -406,23 +411,25 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool kTma, bool kXform>
+template <bool kTma, int kMode>
 cudaError_t dispatch(const RowArgs &a, int dt, int dr, cudaStream_t stream) {
-    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kXform>(a, stream);
-    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kXform>(a, stream);
-    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kXform>(a, stream);
-    return launch_typed<F32, F32, kTma, kXform>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kMode>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kMode>(a, stream);
+    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kMode>(a, stream);
+    return launch_typed<F32, F32, kTma, kMode>(a, stream);
+}
+
+template <int kMode>
+cudaError_t dispatch_path(const RowArgs &a, int dt, int dr, bool use_tma, cudaStream_t stream) {
+    return use_tma ? dispatch<true, kMode>(a, dt, dr, stream) : dispatch<false, kMode>(a, dt, dr, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, bool use_xform,
-                        cudaStream_t stream) {
-    if (use_xform)
-        return use_tma ? dispatch<true, true>(a, dtype_t, dtype_r, stream)
-                       : dispatch<false, true>(a, dtype_t, dtype_r, stream);
-    return use_tma ? dispatch<true, false>(a, dtype_t, dtype_r, stream)
-                   : dispatch<false, false>(a, dtype_t, dtype_r, stream);
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream) {
+    if (mode == kRowTransform) return dispatch_path<1>(a, dtype_t, dtype_r, use_tma, stream);
+    if (mode == kRowEntropy) return dispatch_path<2>(a, dtype_t, dtype_r, use_tma, stream);
+    return dispatch_path<0>(a, dtype_t, dtype_r, use_tma, stream);
 }
 
 }  // namespace lpd

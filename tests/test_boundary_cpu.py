@@ -200,3 +200,22 @@ def test_transform_chain_too_long():
     rc = B.lib().lpd_score_transformed(ctypes.byref(t), ctypes.byref(t), ctypes.byref(c), None, 8, 16, FAKE, FAKE,
                                        0.8, 1.2, None, None, None, FAKE, WS_OK, 1 << 20, None)
     assert rc == B.LPD_ERR_BAD_TRANSFORM
+
+
+def test_entropy_and_backward_validation():
+    lib = B.lib()
+    t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 16)
+    assert lib.lpd_score_entropy(ctypes.byref(t), ctypes.byref(t), 8, 16, FAKE, FAKE, 0.8, 1.2, None, None, None,
+                                 None, None, FAKE, WS_OK, 1 << 20, None) == B.LPD_ERR_NULL_POINTER
+    args = dict(n=8, v=16, ids=FAKE, mask=FAKE, logp=FAKE, grad=FAKE, out=FAKE, dt=B.LPD_F32, stride=16)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return lib.lpd_logprob_backward(ctypes.byref(t), a["n"], a["v"], a["ids"], a["mask"], a["logp"], a["grad"],
+                                        a["out"], a["dt"], a["stride"], None)
+    assert call(out=None) == B.LPD_ERR_NULL_POINTER
+    assert call(grad=None) == B.LPD_ERR_NULL_POINTER
+    assert call(dt=5) == B.LPD_ERR_BAD_DTYPE
+    assert call(stride=15) == B.LPD_ERR_BAD_STRIDE
+    assert call(out=FAKE + 2) == B.LPD_ERR_ALIGNMENT
+    assert call(v=0) == B.LPD_ERR_BAD_SIZE

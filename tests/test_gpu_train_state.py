@@ -1,0 +1,109 @@
+"""Entropy and the logprob gradient ("[WS2] Framework for ablation
+experiment", LogProb knobs table, row 11) against the float64 oracle (needs a
+GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from logprob_drift_scoring_gb300 import binding as B
+from logprob_drift_scoring_gb300 import workloads as W
+from tests.helpers import to_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ENT_ATOL = 1e-4
+
+
+def score_entropy(w, train=None, rollout=None):
+    train = w.train if train is None else train
+    rollout = w.rollout if rollout is None else rollout
+    n = w.n_rows
+    outs = [torch.empty(n, dtype=torch.float32, device=DEV) for _ in range(5)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, n), dtype=torch.uint8, device=DEV)
+    B.lpd_score_entropy(train, rollout, w.token_ids, w.action_mask, *w.clip, *outs, met, ws)
+    torch.cuda.synchronize()
+    return outs, B.read_metrics(met)
+
+
+@pytest.mark.parametrize("rows,vocab,dr,pad", [
+    (200, 3 * 8192 + 520, torch.bfloat16, 0),
+    (150, 12805, torch.bfloat16, 3),
+    (120, 9000, torch.float32, 0),
+    (60, 151936, torch.bfloat16, 0),
+    (80, 7, torch.bfloat16, 0),
+])
+def test_entropy_vs_oracle(rows, vocab, dr, pad):
+    w = W.synthetic(rows, vocab, seed=rows + vocab, device=DEV, dtype_rollout=dr, row_pad=pad, spike_frac=0.1)
+    (lt, lr, d, et, er), met = score_entropy(w)
+    mask = w.action_mask.cpu().numpy()
+    ref_t, ref_r = oracle.entropy(to_oracle(w.train), to_oracle(w.rollout), mask)
+    act = mask != 0
+    for got, want in ((et, ref_t), (er, ref_r)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(g[act] - want[act])) <= ENT_ATOL
+        assert np.all(g[~act] == 0)
+    # the scoring outputs are the plain pass's, bit for bit
+    plain = B.score(w.train, w.rollout, w.token_ids, w.action_mask, w.clip)
+    torch.cuda.synchronize()
+    for a, b in ((lt, plain.logp_train), (lr, plain.logp_rollout), (d, plain.dlogp)):
+        assert torch.equal(a, b)
+    assert met == plain.metrics
+
+
+def test_entropy_closed_forms():
+    vocab = 5000
+    u = torch.full((40, vocab), 1.5, dtype=torch.bfloat16, device=DEV)
+    ids = torch.zeros(40, dtype=torch.int32, device=DEV)
+    mask = torch.ones(40, dtype=torch.uint8, device=DEV)
+    w = W.Workload("u", u, u, ids, mask, vocab)
+    (_, _, _, et, er), _ = score_entropy(w)
+    assert torch.max(torch.abs(et.double() - np.log(vocab))).item() <= ENT_ATOL
+    assert torch.equal(et, er)
+    peaked = torch.zeros((8, vocab), dtype=torch.float32, device=DEV)
+    peaked[:, 11] = 80.0
+    w2 = W.Workload("p", peaked, peaked, ids[:8], mask[:8], vocab)
+    (_, _, _, e2, _), _ = score_entropy(w2)
+    assert torch.all(e2.abs() <= ENT_ATOL)
+
+
+@pytest.mark.parametrize("rows,vocab,dt,out_dtype,pad", [
+    (64, 3 * 2048 + 40, torch.bfloat16, torch.float32, 0),
+    (64, 5000, torch.float32, torch.float32, 3),
+    (48, 1001, torch.bfloat16, torch.float32, 0),     # rows not 16-byte aligned: scalar path
+    (64, 20000, torch.bfloat16, torch.bfloat16, 0),
+])
+def test_backward_vs_oracle(rows, vocab, dt, out_dtype, pad):
+    w = W.synthetic(rows, vocab, seed=rows * 7 + vocab, device=DEV, dtype_train=dt, row_pad=pad, active_prob=0.8)
+    res = B.score(w.train, w.rollout, w.token_ids, w.action_mask, w.clip)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    grad = torch.randn(rows, generator=g, device=DEV)
+    out = torch.full((rows, vocab), float("nan"), dtype=out_dtype, device=DEV)
+    B.lpd_logprob_backward(w.train, w.token_ids, w.action_mask, res.logp_train, grad, out)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    x = to_oracle(w.train)
+    mask = w.action_mask.cpu().numpy()
+    ids = w.token_ids.cpu().numpy()
+    gr = grad.double().cpu().numpy()
+    for r in range(rows):
+        if not mask[r]:
+            assert np.all(got[r] == 0)
+            continue
+        want = oracle.logprob_backward_row(np.ascontiguousarray(x[r]), int(ids[r]), float(gr[r]))
+        tol = 1e-5 * abs(gr[r]) + (2.0 ** -8 * np.abs(want) if out_dtype == torch.bfloat16 else 0.0)
+        assert np.all(np.abs(got[r] - want) <= tol + 1e-12), r
+        if out_dtype == torch.float32:
+            assert abs(got[r].sum()) <= 1e-4 * abs(gr[r]) + 1e-9
+
+
+def test_backward_oob_id_is_nan():
+    w = W.synthetic(10, 3000, seed=9, device=DEV, active_prob=1.0)
+    res = B.score(w.train, w.rollout, w.token_ids, w.action_mask)
+    ids = w.token_ids.clone()
+    ids[3] = 3000
+    out = torch.zeros((10, 3000), dtype=torch.float32, device=DEV)
+    B.lpd_logprob_backward(w.train, ids, w.action_mask, res.logp_train, torch.ones(10, device=DEV), out)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isnan(out[3])) and not torch.any(torch.isnan(out[2]))
