@@ -212,9 +212,11 @@ __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc
         er[p] = ex2_2(xr);
         dq[p] = sub2(et[p], er[p]);
         if (kEntropy) {
-            // -inf columns give e = 0 and a = -inf: their product must count as 0
-            a.ht = fma2(et[p], f2(f2_lo(et[p]) == 0.f ? 0.f : f2_lo(xt), f2_hi(et[p]) == 0.f ? 0.f : f2_hi(xt)), a.ht);
-            a.hr = fma2(er[p], f2(f2_lo(er[p]) == 0.f ? 0.f : f2_lo(xr), f2_hi(er[p]) == 0.f ? 0.f : f2_hi(xr)), a.hr);
+            // -inf columns give e = 0 and a = -inf; clamping a to a finite
+            // floor makes their product 0 instead of NaN (finite terms are
+            // never below the floor: their e would be 0 anyway)
+            a.ht = fma2(et[p], f2(fmaxf(f2_lo(xt), -1e30f), fmaxf(f2_hi(xt), -1e30f)), a.ht);
+            a.hr = fma2(er[p], f2(fmaxf(f2_lo(xr), -1e30f), fmaxf(f2_hi(xr), -1e30f)), a.hr);
         }
     }
     a.st = add2(a.st, tree8(et));

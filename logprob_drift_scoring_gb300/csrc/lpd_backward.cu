@@ -10,8 +10,9 @@
 // Inactive rows get a zero gradient; an active row with an out-of-range id
 // gets NaN (fail closed).
 //
-// Layout: blocks of 256 threads cover 2048 columns of one row (8 per thread);
-// grid.x spans the vocabulary, grid.y strides over rows.  Rows whose input and
+// Layout: blocks of 256 threads cover 8192 columns of one row (four groups of
+// 8 per thread, all loads issued before the arithmetic); grid.x spans the
+// vocabulary, grid.y strides over rows.  Rows whose input and
 // output start on 16-byte boundaries use 16-byte loads and stores.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -23,7 +24,8 @@ namespace lpd {
 namespace {
 
 constexpr int kBwdThreads = 256;
-constexpr int kBwdCols = 8 * kBwdThreads;
+constexpr int kBwdGroups = 4;                                // 8-column groups per thread
+constexpr int kBwdCols = 8 * kBwdThreads * kBwdGroups;       // 8192 columns per block
 
 struct BwdArgs {
     const char *x;
@@ -51,72 +53,91 @@ __device__ __forceinline__ void store_out(const BwdArgs &a, char *row, int64_t j
         reinterpret_cast<float *>(row)[j] = v;
 }
 
+// One 8-column group: load (vector or scalar), gradient, store.
+__device__ __forceinline__ void bwd_load8(const BwdArgs &a, const char *xrow, int64_t c0, bool vec, float *x) {
+    if (vec) {
+        if (a.x_bf16) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(xrow + c0 * 2));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                x[2 * q] = __uint_as_float(ws[q] << 16);
+                x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
+            }
+        } else {
+            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4));
+            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4) + 1);
+            x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
+            x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = c0 + q < a.vocab ? load_x(a, xrow, c0 + q) : 0.f;
+    }
+}
+
+__device__ __forceinline__ void bwd_store8(const BwdArgs &a, char *orow, int64_t c0, bool vec, const float *v) {
+    if (vec) {
+        if (a.out_bf16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+                w[q] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            *reinterpret_cast<uint4 *>(orow + c0 * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            reinterpret_cast<float4 *>(orow + c0 * 4)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4 *>(orow + c0 * 4)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (c0 + q < a.vocab) store_out(a, orow, c0 + q, v[q]);
+    }
+}
+
+// Thread t of block (bx, by) handles groups g = 0..3 at columns
+// bx * 8192 + g * 2048 + 8 t, for rows by, by + gridDim.y, ...
 __global__ void __launch_bounds__(kBwdThreads) backward_kernel(const __grid_constant__ BwdArgs a) {
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kBwdCols + 8 * threadIdx.x;
-    if (c0 >= a.vocab) return;
-    const bool full = c0 + 8 <= a.vocab;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBwdCols + 8 * threadIdx.x;
     for (int64_t r = blockIdx.y; r < a.n_rows; r += gridDim.y) {
         char *orow = a.out + r * a.out_stride;
         const char *xrow = a.x + r * a.x_stride;
-        float v[8];
-        bool write = true;
-        if (!a.mask[r]) {
+        const bool active = a.mask[r] != 0;
+        const int64_t id = active ? a.ids[r] : 0;
+        const bool ok = active && id >= 0 && id < a.vocab;
+        float lse = 0.f, g = 0.f;
+        if (ok) {
+            lse = __fsub_rn(load_x(a, xrow, id), a.logp[r]);
+            g = a.grad[r];
+        }
+        float x[kBwdGroups][8];
+        if (ok) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = 0.f;
-        } else {
-            const int64_t id = a.ids[r];
-            if (id < 0 || id >= a.vocab) {
+            for (int gi = 0; gi < kBwdGroups; ++gi) {
+                const int64_t c0 = base + gi * (8 * kBwdThreads);
+                if (c0 < a.vocab) bwd_load8(a, xrow, c0, a.vec && c0 + 8 <= a.vocab, x[gi]);
+            }
+        }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = CUDART_NAN_F;
-            } else {
-                const float lse = __fsub_rn(load_x(a, xrow, id), a.logp[r]);
-                const float g = a.grad[r];
-                float x[8];
-                if (a.vec && full) {
-                    if (a.x_bf16) {
-                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(xrow + c0 * 2));
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int gi = 0; gi < kBwdGroups; ++gi) {
+            const int64_t c0 = base + gi * (8 * kBwdThreads);
+            if (c0 >= a.vocab) continue;
+            float v[8];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            x[2 * q] = __uint_as_float(ws[q] << 16);
-                            x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
-                        }
-                    } else {
-                        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4));
-                        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4) + 1);
-                        x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
-                        x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
-                    }
+            for (int q = 0; q < 8; ++q) {
+                if (!active) {
+                    v[q] = 0.f;
+                } else if (!ok) {
+                    v[q] = CUDART_NAN_F;
                 } else {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) x[q] = c0 + q < a.vocab ? load_x(a, xrow, c0 + q) : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float p = ex2(__fmul_rn(__fsub_rn(x[q], lse), kLog2e));
+                    const float p = ex2(__fmul_rn(__fsub_rn(x[gi][q], lse), kLog2e));
                     const float onehot = (c0 + q == id) ? 1.f : 0.f;
                     v[q] = __fmul_rn(g, __fsub_rn(onehot, p));
                 }
             }
-        }
-        if (!write) continue;
-        if (a.vec && full) {
-            if (a.out_bf16) {
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
-                    w[q] = *reinterpret_cast<const uint32_t *>(&h);
-                }
-                *reinterpret_cast<uint4 *>(orow + c0 * 2) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-                reinterpret_cast<float4 *>(orow + c0 * 4)[0] = make_float4(v[0], v[1], v[2], v[3]);
-                reinterpret_cast<float4 *>(orow + c0 * 4)[1] = make_float4(v[4], v[5], v[6], v[7]);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (c0 + q < a.vocab) store_out(a, orow, c0 + q, v[q]);
+            bwd_store8(a, orow, c0, a.vec && c0 + 8 <= a.vocab, v);
         }
     }
 }

@@ -159,18 +159,54 @@ __device__ __forceinline__ XformRegs xform_regs(const Xform &c) {
     return r;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// tanh(y) = 1 - 2 / (1 + e^(2y)), evaluated on the special-function unit.
+// Its absolute error (a few 1e-7) is what matters here: a soft-capped logit
+// p * tanh(x / p) is off by at most p times that.  Large |y| saturate to +-1.
+__device__ __forceinline__ float tanh_sfu(float y) {
+    const float e = ex2(__fmul_rn(y, 2.f * kLog2e));
+    return __fsub_rn(1.f, __fmul_rn(2.f, rcp_approx(__fadd_rn(1.f, e))));
+}
+
+__device__ __forceinline__ float softcap1(float x, float p, float rcp) {
+    return __fmul_rn(p, tanh_sfu(__fmul_rn(x, rcp)));
+}
+
 __device__ __forceinline__ float xform1(float x, const XformRegs &c) {
 #pragma unroll
     for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
-        if (k < c.n)
-            x = c.kind[k] == LPD_OP_SCALE ? __fmul_rn(x, c.p[k]) : __fmul_rn(c.p[k], tanhf(__fmul_rn(x, c.rcp[k])));
+        if (k < c.n) {
+            if (c.kind[k] == LPD_OP_SCALE)
+                x = __fmul_rn(x, c.p[k]);
+            else
+                x = softcap1(x, c.p[k], c.rcp[k]);
+        }
     }
     return x;
 }
 
+// The chain over sixteen values: ops outermost, so each op's kind is decided
+// once per chunk (it is the same for every thread); scale runs packed.
 __device__ __forceinline__ void xform16(f2_t *v, const XformRegs &c) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) v[p] = f2(xform1(f2_lo(v[p]), c), xform1(f2_hi(v[p]), c));
+    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
+        if (k < c.n) {
+            if (c.kind[k] == LPD_OP_SCALE) {
+                const f2_t p2 = f2(c.p[k], c.p[k]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = mul2(v[q], p2);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = f2(softcap1(f2_lo(v[q]), c.p[k], c.rcp[k]), softcap1(f2_hi(v[q]), c.p[k], c.rcp[k]));
+            }
+        }
+    }
 }
 
 // Column of slot q (0..15) of consumer thread t within a tile.

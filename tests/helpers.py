@@ -7,7 +7,9 @@ p95/p99/max |dlogp| within 1e-4 absolute; active counts, token selection and
 the batch-invariance controls bit-exact.  ratio0_mean has no stated bar; it is
 the mean of exp(dlogp) ("Diagnostics": ratio0 = exp(dlogp)), whose error is
 the mean of exp(dlogp) * (error of dlogp), i.e. about 1e-7 of the ratio
-itself, so 1e-6 x max(1, ratio0_mean) is used.  clipfrac0 must match exactly
+itself, so (1e-6 + the largest per-token dlogp error observed against the
+oracle) x max(1, ratio0_mean) is used; the per-token error is itself held to
+the logp bar.  clipfrac0 must match exactly
 except for tokens whose oracle dlogp lies within 1e-9 of ln(lo) or ln(hi),
 where the two sides may legitimately decide differently (1e-6 when the
 reference is the oracle's metric function applied to the GPU's own fp32
@@ -38,7 +40,7 @@ def to_oracle(t) -> np.ndarray:
 
 
 def assert_metrics_match(gpu: dict, ref: dict, ref_dlogp=None, mask=None, clip=(0.8, 1.2),
-                         ambiguity=CLIP_AMBIGUITY):
+                         ambiguity=CLIP_AMBIGUITY, dlogp_err=0.0):
     assert gpu["status"] == ref["status"], (gpu["status"], ref["status"])
     assert gpu["n_active"] == ref["n_active"]
     assert gpu["flags"] == ref["flags"]
@@ -53,8 +55,8 @@ def assert_metrics_match(gpu: dict, ref: dict, ref_dlogp=None, mask=None, clip=(
         assert abs(gpu[k] - ref[k]) <= tol, (k, gpu[k], ref[k], abs(gpu[k] - ref[k]) / max(abs(ref[k]), 1e-300))
     for k in ("p95_abs_dlogp", "p99_abs_dlogp", "max_abs_dlogp"):
         assert abs(gpu[k] - ref[k]) <= PCT_ATOL, (k, gpu[k], ref[k])
-    assert abs(gpu["ratio0_mean"] - ref["ratio0_mean"]) <= RATIO_ATOL * max(1.0, abs(ref["ratio0_mean"])), \
-        (gpu["ratio0_mean"], ref["ratio0_mean"])
+    ratio_tol = (RATIO_ATOL + 1.01 * dlogp_err) * max(1.0, abs(ref["ratio0_mean"]))
+    assert abs(gpu["ratio0_mean"] - ref["ratio0_mean"]) <= ratio_tol, (gpu["ratio0_mean"], ref["ratio0_mean"])
     # clip decisions: exact unless the oracle value sits on a boundary
     n_amb = 0
     if ref_dlogp is not None:
