@@ -99,7 +99,7 @@ __device__ __forceinline__ void bwd_store8(const BwdArgs &a, char *orow, int64_t
 
 // Thread t of block (bx, by) handles groups g = 0..3 at columns
 // bx * 8192 + g * 2048 + 8 t, for rows by, by + gridDim.y, ...
-__global__ void __launch_bounds__(kBwdThreads) backward_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, 4) backward_kernel(const __grid_constant__ BwdArgs a) {
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kBwdCols + 8 * threadIdx.x;
     for (int64_t r = blockIdx.y; r < a.n_rows; r += gridDim.y) {
         char *orow = a.out + r * a.out_stride;
