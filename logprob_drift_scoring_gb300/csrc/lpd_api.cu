@@ -112,6 +112,19 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
         a.xt = ex.xform[0];
         a.xr = ex.xform[1];
         mode = kRowTransform;
+        // chains made only of scales collapse to one multiply per side
+        bool scales_only = true;
+        float prod[2] = {1.f, 1.f};
+        for (int side = 0; side < 2; ++side)
+            for (int k = 0; k < ex.xform[side].n_ops; ++k) {
+                if (ex.xform[side].kind[k] != LPD_OP_SCALE) scales_only = false;
+                prod[side] *= ex.xform[side].param[k];
+            }
+        if (scales_only) {
+            a.st = prod[0];
+            a.sr = prod[1];
+            mode = kRowScale;
+        }
     } else if (ex.ent_t || ex.ent_r) {
         mode = kRowEntropy;
     }

@@ -10,9 +10,8 @@
 // Inactive rows get a zero gradient; an active row with an out-of-range id
 // gets NaN (fail closed).
 //
-// Layout: blocks of 256 threads cover 8192 columns of one row (four groups of
-// 8 per thread, all loads issued before the arithmetic); grid.x spans the
-// vocabulary, grid.y strides over rows.  Rows whose input and
+// Layout: four persistent blocks of 256 threads per SM stride over rows; each
+// row is swept in 8-column groups, four groups per thread in flight.  Rows whose input and
 // output start on 16-byte boundaries use 16-byte loads and stores.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -24,8 +23,7 @@ namespace lpd {
 namespace {
 
 constexpr int kBwdThreads = 256;
-constexpr int kBwdGroups = 4;                                // 8-column groups per thread
-constexpr int kBwdCols = 8 * kBwdThreads * kBwdGroups;       // 8192 columns per block
+constexpr int kBwdGroups = 4;  // 8-column groups per thread in flight
 
 struct BwdArgs {
     const char *x;
@@ -97,11 +95,13 @@ __device__ __forceinline__ void bwd_store8(const BwdArgs &a, char *orow, int64_t
     }
 }
 
-// Thread t of block (bx, by) handles groups g = 0..3 at columns
-// bx * 8192 + g * 2048 + 8 t, for rows by, by + gridDim.y, ...
+// Persistent blocks: block b takes rows b, b + gridDim.x, ...; within a row
+// thread t handles 8-column groups at 8 t + 2048 k, four groups per iteration
+// with all four loads issued before the arithmetic.  The row prologue (mask,
+// id, lse, g) is paid once per row.
 __global__ void __launch_bounds__(kBwdThreads, 4) backward_kernel(const __grid_constant__ BwdArgs a) {
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kBwdCols + 8 * threadIdx.x;
-    for (int64_t r = blockIdx.y; r < a.n_rows; r += gridDim.y) {
+    constexpr int64_t kStep = 8 * kBwdThreads;  // columns between a thread's groups
+    for (int64_t r = blockIdx.x; r < a.n_rows; r += gridDim.x) {
         char *orow = a.out + r * a.out_stride;
         const char *xrow = a.x + r * a.x_stride;
         const bool active = a.mask[r] != 0;
@@ -112,32 +112,34 @@ __global__ void __launch_bounds__(kBwdThreads, 4) backward_kernel(const __grid_c
             lse = __fsub_rn(load_x(a, xrow, id), a.logp[r]);
             g = a.grad[r];
         }
-        float x[kBwdGroups][8];
-        if (ok) {
+        for (int64_t base = 8 * static_cast<int64_t>(threadIdx.x); base < a.vocab; base += kBwdGroups * kStep) {
+            float x[kBwdGroups][8];
+            if (ok) {
 #pragma unroll
-            for (int gi = 0; gi < kBwdGroups; ++gi) {
-                const int64_t c0 = base + gi * (8 * kBwdThreads);
-                if (c0 < a.vocab) bwd_load8(a, xrow, c0, a.vec && c0 + 8 <= a.vocab, x[gi]);
-            }
-        }
-#pragma unroll
-        for (int gi = 0; gi < kBwdGroups; ++gi) {
-            const int64_t c0 = base + gi * (8 * kBwdThreads);
-            if (c0 >= a.vocab) continue;
-            float v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (!active) {
-                    v[q] = 0.f;
-                } else if (!ok) {
-                    v[q] = CUDART_NAN_F;
-                } else {
-                    const float p = ex2(__fmul_rn(__fsub_rn(x[gi][q], lse), kLog2e));
-                    const float onehot = (c0 + q == id) ? 1.f : 0.f;
-                    v[q] = __fmul_rn(g, __fsub_rn(onehot, p));
+                for (int gi = 0; gi < kBwdGroups; ++gi) {
+                    const int64_t c0 = base + gi * kStep;
+                    if (c0 < a.vocab) bwd_load8(a, xrow, c0, a.vec && c0 + 8 <= a.vocab, x[gi]);
                 }
             }
-            bwd_store8(a, orow, c0, a.vec && c0 + 8 <= a.vocab, v);
+#pragma unroll
+            for (int gi = 0; gi < kBwdGroups; ++gi) {
+                const int64_t c0 = base + gi * kStep;
+                if (c0 >= a.vocab) continue;
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (!active) {
+                        v[q] = 0.f;
+                    } else if (!ok) {
+                        v[q] = CUDART_NAN_F;
+                    } else {
+                        const float p = ex2(__fmul_rn(__fsub_rn(x[gi][q], lse), kLog2e));
+                        const float onehot = (c0 + q == id) ? 1.f : 0.f;
+                        v[q] = __fmul_rn(g, __fsub_rn(onehot, p));
+                    }
+                }
+                bwd_store8(a, orow, c0, a.vec && c0 + 8 <= a.vocab, v);
+            }
         }
     }
 }
@@ -163,9 +165,8 @@ cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, 
     a.grad = grad;
     a.vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (a.x_stride % 16 == 0) &&
             (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (a.out_stride % 16 == 0);
-    const dim3 grid(static_cast<unsigned>((vocab + kBwdCols - 1) / kBwdCols),
-                    static_cast<unsigned>(n_rows < 65535 ? n_rows : 65535));
-    backward_kernel<<<grid, kBwdThreads, 0, stream>>>(a);
+    const int64_t blocks = static_cast<int64_t>(device_sm_count()) * 4;
+    backward_kernel<<<static_cast<unsigned>(n_rows < blocks ? n_rows : blocks), kBwdThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

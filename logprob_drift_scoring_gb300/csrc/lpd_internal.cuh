@@ -87,7 +87,8 @@ struct Xform {
 };
 
 struct RowArgs {
-    Xform xt, xr;  // train and rollout chains (used by the transforming instantiation only)
+    Xform xt, xr;    // train and rollout chains (transform mode only)
+    float st, sr;    // product of each side's scales (scale-only chains)
     Segment seg[kMaxSegments];
     int n_seg;
     int64_t vocab;
@@ -143,7 +144,7 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lt, float *out_lr, float *out_d,
                                  lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
                                  cudaStream_t stream);
-constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2;
+constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3;
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,

@@ -210,11 +210,14 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
     return x;
 }
 
-// kMode: 0 plain, 1 with the transform chain, 2 with the entropy sums.
+// kMode: 0 plain, 1 with a general transform chain, 2 with the entropy sums,
+// 3 with a scale-only chain (one packed multiply by the side's product of
+// scales, so no tanh code sits in this instantiation).
 template <class DT, class DR, bool kTma, int kMode>
 __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     constexpr bool kXform = kMode == 1;
     constexpr bool kEntropy = kMode == 2;
+    constexpr bool kScale = kMode == 3;
     extern __shared__ __align__(1024) char smem[];
     __shared__ int abort_flag;
     constexpr int kStageT = kTile * DT::kBytes;
@@ -334,6 +337,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             xform16(vt, cxt);
                             xform16(vr, cxr);
                         }
+                        if (kScale) {
+                            const f2_t s_t = f2(a.st, a.st), s_r = f2(a.sr, a.sr);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                vt[q] = mul2(vt[q], s_t);
+                                vr[q] = mul2(vr[q], s_r);
+                            }
+                        }
                     } else {
                         // ragged last tile: the same vector loads, then the
                         // columns the bulk copy did not cover (a few bytes at the
@@ -360,12 +371,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                                         x[h] = xform1(x[h], cxt);
                                         y[h] = xform1(y[h], cxr);
                                     }
+                                    if (kScale && col < nv) {
+                                        x[h] = __fmul_rn(x[h], a.st);
+                                        y[h] = __fmul_rn(y[h], a.sr);
+                                    }
                                 }
                                 vt[p] = f2(x[0], x[1]);
                                 vr[p] = f2(y[0], y[1]);
                             } else if (kXform) {
                                 vt[p] = f2(xform1(f2_lo(vt[p]), cxt), xform1(f2_hi(vt[p]), cxt));
                                 vr[p] = f2(xform1(f2_lo(vr[p]), cxr), xform1(f2_hi(vr[p]), cxr));
+                            } else if (kScale) {
+                                vt[p] = mul2(vt[p], f2(a.st, a.st));
+                                vr[p] = mul2(vr[p], f2(a.sr, a.sr));
                             }
                         }
                     }
@@ -384,6 +402,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             if (kXform && col < nv) {
                                 x[h] = xform1(x[h], cxt);
                                 y[h] = xform1(y[h], cxr);
+                            }
+                            if (kScale && col < nv) {
+                                x[h] = __fmul_rn(x[h], a.st);
+                                y[h] = __fmul_rn(y[h], a.sr);
                             }
                         }
                         vt[p] = f2(x[0], x[1]);
@@ -454,6 +476,7 @@ cudaError_t dispatch_path(const RowArgs &a, int dt, int dr, bool use_tma, cudaSt
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream) {
     if (mode == kRowTransform) return dispatch_path<1>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowEntropy) return dispatch_path<2>(a, dtype_t, dtype_r, use_tma, stream);
+    if (mode == kRowScale) return dispatch_path<3>(a, dtype_t, dtype_r, use_tma, stream);
     return dispatch_path<0>(a, dtype_t, dtype_r, use_tma, stream);
 }
 
