@@ -128,6 +128,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.lpdo_entropy.argtypes = [P, I32, I64, P, I32, I64, I64, I64, P, P, P]
     lib.lpdo_logprob_backward_row.restype = None
     lib.lpdo_logprob_backward_row.argtypes = [P, I32, I64, I64, D, P]
+    lib.lpdo_attn_merge.restype = None
+    lib.lpdo_attn_merge.argtypes = [P, P, ctypes.c_int, I64, ctypes.c_int, ctypes.c_int, P, P, P]
     lib.lpdo_score_head_rows.restype = U32
     lib.lpdo_score_head_rows.argtypes = [P, P, P, I64, I64, P, P, I64, P, P, P]
     return lib
@@ -352,3 +354,17 @@ def logprob_backward_row(row, token_id: int, grad: float, lib=None) -> np.ndarra
     out = np.zeros(row.shape[0])
     lib.lpdo_logprob_backward_row(_ptr(row), code, row.shape[0], int(token_id), float(grad), _ptr(out))
     return out
+
+
+def attn_merge(out_parts, lse_parts, order=None, lse_base2=False, lib=None):
+    """Merge partial attention results: out_parts [K, n, d] f32, lse_parts
+    [K, n] f32, parts visited in ``order``.  Returns (out [n, d], lse [n])."""
+    lib = lib or load()
+    o = np.ascontiguousarray(out_parts, dtype=np.float32)
+    l = np.ascontiguousarray(lse_parts, dtype=np.float32)
+    K, n, d = o.shape
+    order = np.ascontiguousarray(range(K) if order is None else order, dtype=np.int32)
+    out = np.zeros((n, d))
+    lse = np.zeros(n)
+    lib.lpdo_attn_merge(_ptr(o), _ptr(l), K, n, d, int(bool(lse_base2)), _ptr(order), _ptr(out), _ptr(lse))
+    return out, lse

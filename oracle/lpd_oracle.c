@@ -27,6 +27,10 @@
  *         soft-cap, logit scale) applied to every logit before the softmax.
  *   [TS]  same table, row 11: training-only state, i.e. the entropy of the
  *         softmax and the logprob's gradient with respect to the logits.
+ *   [AM]  "Attention Debug Matrix", row A7 (merge_order), and the Attention
+ *         knobs table of "[WS2] Framework for ablation experiment", rows 6-7:
+ *         split-KV / context-parallel partial results (out_k, lse_k) merged
+ *         into one (out, lse) in a given block order; lse in base e or 2.
  *
  * Readings where the pages are silent (each is also listed with the design
  * notes): percentiles are nearest-rank (1-based rank ceil(p*A/100) of the
@@ -516,5 +520,59 @@ void lpdo_logprob_backward_row(const void *row, int dtype, int64_t vocab, int64_
     for (int64_t j = 0; j < vocab; ++j) {
         double p = exp(logit_at(row, dtype, j) - lse);
         out[j] = grad * ((j == id ? 1.0 : 0.0) - p);
+    }
+}
+
+/* ---- attention partial merge [AM] ---------------------------------------- */
+
+/* Merge K partial attention results for each of n rows, visiting the parts in
+ * `order` (a permutation of 0..K-1):
+ *   lse = log(sum_k exp(lse_k)),  out = sum_k exp(lse_k - lse) * out_k.
+ * out_parts: [K][n][d] (f32), lse_parts: [K][n]; with lse_base2 the lse values
+ * are log2-sum-exp2 and are converted to natural log first (and back for the
+ * merged lse).  A part whose lse is -inf saw no keys for that row: it carries
+ * no weight and its out values are not read (a backend may leave them 0 or
+ * NaN).  A row no part saw merges to out = 0, lse = -inf. */
+void lpdo_attn_merge(const float *out_parts, const float *lse_parts, int K, int64_t n, int d,
+                     int lse_base2, const int32_t *order, double *out, double *out_lse)
+{
+    const double ln2 = log(2.0);
+    for (int64_t i = 0; i < n; ++i) {
+        double *oi = out + (size_t)i * (size_t)d;
+        for (int j = 0; j < d; ++j)
+            oi[j] = 0.0;
+        double m = -INFINITY;
+        for (int k = 0; k < K; ++k) {
+            double l = lse_parts[(size_t)order[k] * (size_t)n + (size_t)i];
+            if (lse_base2)
+                l *= ln2;
+            if (l > m)
+                m = l;
+        }
+        if (m == -INFINITY) {
+            out_lse[i] = -INFINITY;
+            continue;
+        }
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double l = lse_parts[(size_t)order[k] * (size_t)n + (size_t)i];
+            if (lse_base2)
+                l *= ln2;
+            s += exp(l - m);
+        }
+        double lse = m + log(s);
+        for (int k = 0; k < K; ++k) {
+            int kk = order[k];
+            double l = lse_parts[(size_t)kk * (size_t)n + (size_t)i];
+            if (l == -INFINITY)
+                continue;
+            if (lse_base2)
+                l *= ln2;
+            double w = exp(l - lse);
+            const float *o = out_parts + ((size_t)kk * (size_t)n + (size_t)i) * (size_t)d;
+            for (int j = 0; j < d; ++j)
+                oi[j] += w * (double)o[j];
+        }
+        out_lse[i] = lse_base2 ? lse / ln2 : lse;
     }
 }

@@ -543,3 +543,71 @@ def pin_backward_uniform(lib):
 
 
 ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+# ------------------------------------------------------ attention merge pins
+
+def _attention_split(rng, n, d, n_keys, bounds):
+    """Softmax attention of n queries over n_keys keys, computed whole and per
+    key block (each block's own normalised output and natural-log lse)."""
+    q = rng.normal(0, 1, size=(n, d))
+    k = rng.normal(0, 1, size=(n_keys, d))
+    v = rng.normal(0, 1, size=(n_keys, d))
+    s = q @ k.T / math.sqrt(d)
+    full_lse = np.log(np.sum(np.exp(s), axis=1))
+    full_out = np.exp(s - full_lse[:, None]) @ v
+    outs, lses = [], []
+    for a, b in bounds:
+        sb = s[:, a:b]
+        lb = np.log(np.sum(np.exp(sb), axis=1))
+        outs.append(np.exp(sb - lb[:, None]) @ v[a:b])
+        lses.append(lb)
+    return full_out, full_lse, np.array(outs, np.float32), np.array(lses, np.float32)
+
+
+def pin_attn_merge_equals_unsplit_attention(lib):
+    rng = np.random.default_rng(81)
+    full_out, full_lse, outs, lses = _attention_split(rng, 6, 8, 40, [(0, 9), (9, 25), (25, 40)])
+    for order in ([0, 1, 2], [2, 0, 1]):
+        out, lse = oracle.attn_merge(outs, lses, order, lib=lib)
+        np.testing.assert_allclose(out, full_out, rtol=0, atol=2e-6)     # parts are stored in fp32
+        np.testing.assert_allclose(lse, full_lse, rtol=0, atol=2e-6)
+
+
+def pin_attn_merge_closed_forms(lib):
+    rng = np.random.default_rng(82)
+    outs = rng.normal(0, 1, size=(1, 5, 4)).astype(np.float32)
+    lses = rng.normal(0, 1, size=(1, 5)).astype(np.float32)
+    out, lse = oracle.attn_merge(outs, lses, lib=lib)                        # one part: identity
+    assert np.array_equal(out, outs[0].astype(np.float64)) and np.array_equal(lse, lses[0].astype(np.float64))
+    outs = rng.normal(0, 1, size=(4, 3, 2)).astype(np.float32)
+    lses = np.full((4, 3), 1.5, np.float32)
+    out, lse = oracle.attn_merge(outs, lses, lib=lib)                        # equal lse: plain mean
+    np.testing.assert_allclose(out, outs.astype(np.float64).mean(axis=0), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, 1.5 + math.log(4), rtol=0, atol=1e-14)
+    out2, lse2 = oracle.attn_merge(outs, lses / np.float32(math.log(2)), lse_base2=True, lib=lib)
+    np.testing.assert_allclose(out2, out, rtol=0, atol=1e-6)
+    np.testing.assert_allclose(lse2 * math.log(2), lse, rtol=0, atol=1e-6)
+
+
+ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+def pin_attn_merge_masked_parts(lib):
+    # causal split: the last key block lies after every query, so its part saw
+    # no keys (lse -inf, out left as NaN by the backend); merging the remaining
+    # parts must still equal unsplit attention over the keys that exist
+    rng = np.random.default_rng(83)
+    full_out, full_lse, outs, lses = _attention_split(rng, 4, 8, 30, [(0, 12), (12, 30)])
+    outs = np.concatenate([outs, np.full((1, 4, 8), np.nan, np.float32)])
+    lses = np.concatenate([lses, np.full((1, 4), -np.inf, np.float32)])
+    for order in ([0, 1, 2], [2, 1, 0]):
+        out, lse = oracle.attn_merge(outs, lses, order, lib=lib)
+        np.testing.assert_allclose(out, full_out, rtol=0, atol=2e-6)
+        np.testing.assert_allclose(lse, full_lse, rtol=0, atol=2e-6)
+    # a row that no part saw: out 0, lse -inf
+    out, lse = oracle.attn_merge(np.full((2, 1, 3), np.nan, np.float32), np.full((2, 1), -np.inf, np.float32), lib=lib)
+    assert np.array_equal(out, np.zeros((1, 3))) and lse[0] == -np.inf
+
+
+ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}

@@ -58,6 +58,10 @@ MUTANTS = {
     "entropy_drops_lse": ("    return lse - px;\n}", "    return -px;\n}"),
     "backward_onehot_dropped": ("out[j] = grad * ((j == id ? 1.0 : 0.0) - p);", "out[j] = grad * (0.0 - p);"),
     "backward_sign": ("out[j] = grad * ((j == id ? 1.0 : 0.0) - p);", "out[j] = grad * (p - (j == id ? 1.0 : 0.0));"),
+    "attn_weight_sign": ("double w = exp(l - lse);", "double w = exp(lse - l);"),
+    "attn_base2_unconverted": ("            if (lse_base2)\n                l *= ln2;\n            double w", "            double w"),
+    "attn_masked_part_read": ("            if (l == -INFINITY)\n                continue;\n            if (lse_base2)\n                l *= ln2;\n            double w",
+                              "            if (lse_base2)\n                l *= ln2;\n            double w"),
     "nonfinite_unflagged": ("return (isfinite(lse) && isfinite(xs)) ? 0u : LPDO_STATUS_NONFINITE;\n}\n\nstatic int",
                             "return 0u;\n}\n\nstatic int"),
 }
