@@ -43,7 +43,10 @@ CONFIGS = {
     "sharded": dict(workload="vocab-sharded B=1 T=32768 V=151936 (4 shards) bf16/bf16", vocab=151936),
     "tiny": dict(workload="tiny B=2 T=64 V=1024 bf16/bf16", vocab=1024),
     "fused": dict(workload="fused LM head: 16384 tokens x H=4096, W [151936, 4096] bf16", vocab=151936),
+    "attn": dict(workload="CP-8 causal attention partials: T=32768 x 32 heads, head_dim 128, f32", vocab=0),
 }
+ATTN_METRIC = "attention rows merged/sec (token x head, split-KV (out, lse) merge); achieved HBM GB/s"
+ATTN_UNIT = "rows/s"
 METRIC = "active tokens/sec scored; achieved HBM GB/s vs GB300 peak (logp+drift pass)"
 UNIT = "active_tokens/s"
 KERNEL_SOURCES = ["logprob_drift_scoring_gb300/csrc/lpd_rows.cu"]
@@ -167,6 +170,8 @@ def make_workload(config: str, device, seed_offset: int = 0, batch=None, seq=Non
         return W.tiny(seed=0 + seed_offset, device=device)
     if config == "fused":
         return W.fused(seed=4 + seed_offset, device=device, rows=seq or 16384)
+    if config == "attn":
+        return W.attn(seed=5 + seed_offset, device=device, n_tokens=seq or 32768)
     raise SystemExit(f"unknown config {config}")
 
 
@@ -370,6 +375,144 @@ def run_fused(args, w, world, rank):
     return out
 
 
+def attn_bytes(w, drift: bool) -> int:
+    """Algorithmic HBM bytes of one merge: the out chunks of every (row, part)
+    pair that saw keys, every part's lse, the merged out and lse; with the
+    order-drift diagnostic also its two per-row columns."""
+    es = w.out_parts.element_size()
+    n, d, K = w.n_rows, w.head_dim, w.n_parts
+    b = w.keyed_pairs() * d * es + K * n * 4 + n * d * 4 + n * 4
+    return b + (8 * n if drift else 0)
+
+
+def time_cpu_oracle_attn(target_s: float = 12.0, seed: int = 1234):
+    """The float64 oracle merge as it stands, single-threaded, on a shorter
+    sequence of the same recipe (rows per second scale with rows)."""
+    import oracle
+    from logprob_drift_scoring_gb300 import workloads as W
+
+    lib = oracle.load()
+    probe = W.attn_partials(64, 32, 128, 8, seed=seed, device="cpu")
+    t0 = time.perf_counter()
+    oracle.attn_merge(probe.out_parts.numpy(), probe.lse_parts.numpy(), lib=lib)
+    per_row = (time.perf_counter() - t0) / probe.n_rows
+    tokens = int(max(64, min(8192, target_s / max(per_row, 1e-12) / 32)))
+    tokens -= tokens % 8
+    w = W.attn_partials(tokens, 32, 128, 8, seed=seed + 1, device="cpu")
+    parts, lse = w.out_parts.numpy(), w.lse_parts.numpy()
+    t0 = time.perf_counter()
+    oracle.attn_merge(parts, lse, lib=lib)
+    elapsed = time.perf_counter() - t0
+    return {"value": w.n_rows / elapsed, "unit": ATTN_UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{w.n_rows} rows (T={tokens} x 32 heads, K=8 causal, head_dim 128) of the attn recipe, "
+                      f"float64 serial C, {elapsed:.1f} s"}
+
+
+def run_attn(args, w, world, rank):
+    """The split-KV attention merge: one lpd_attn_merge call per step (with
+    --drift, one lpd_attn_merge_order_drift call comparing ascending and
+    descending part order)."""
+    import torch
+    from logprob_drift_scoring_gb300 import binding as B
+
+    dev = w.out_parts.device
+    n, d, K = w.n_rows, w.head_dim, w.n_parts
+    out = torch.empty((n, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((n,), dtype=torch.float32, device=dev)
+    rdo = torch.empty((n,), dtype=torch.float32, device=dev)
+    rdl = torch.empty((n,), dtype=torch.float32, device=dev)
+    drift = torch.empty(B.MERGE_DRIFT_BYTES, dtype=torch.uint8, device=dev)
+    rev = list(range(K))[::-1]
+    stream = torch.cuda.current_stream()
+
+    def step(parts=w.out_parts, lses=w.lse_parts):
+        if args.drift:
+            B.lpd_attn_merge_order_drift(parts, lses, None, rev, out, lse, rdo, rdl, drift, stream=stream)
+        else:
+            B.lpd_attn_merge(parts, lses, None, out, lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = barrier_max(start.elapsed_time(stop) / args.steps, world)
+    nbytes = attn_bytes(w, args.drift)
+    peaks = measured_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        # host partials -> device, merge, merged (out, lse) back to the host
+        pinned = True
+        try:
+            hp = torch.empty(w.out_parts.shape, dtype=w.out_parts.dtype, pin_memory=True)
+            hl = torch.empty(w.lse_parts.shape, dtype=torch.float32, pin_memory=True)
+            ho = torch.empty((n, d), dtype=torch.float32, pin_memory=True)
+            hs = torch.empty((n,), dtype=torch.float32, pin_memory=True)
+        except RuntimeError:
+            hp, hl = torch.empty(w.out_parts.shape, dtype=w.out_parts.dtype), torch.empty(w.lse_parts.shape)
+            ho, hs = torch.empty((n, d)), torch.empty((n,))
+            pinned = False
+        hp.copy_(w.out_parts)
+        hl.copy_(w.lse_parts)
+        dp, dl = torch.empty_like(w.out_parts), torch.empty_like(w.lse_parts)
+
+        def one():
+            dp.copy_(hp, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            step(dp, dl)
+            ho.copy_(out, non_blocking=True)
+            hs.copy_(lse, non_blocking=True)
+
+        one()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            one()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = barrier_max(s0.elapsed_time(s1) / args.e2e_steps, world)
+        e2e = {"value": round(world * n / (ems / 1e3), 1), "unit": ATTN_UNIT,
+               "h2d_bytes_per_step": hp.numel() * hp.element_size() + hl.numel() * 4,
+               "d2h_bytes_per_step": ho.numel() * 4 + hs.numel() * 4, "ms_per_step": round(ems, 3),
+               "pinned": pinned, "steps": args.e2e_steps}
+        del hp, hl, dp, dl
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = time_cpu_oracle_attn(target_s=args.cpu_seconds)
+    wl = CONFIGS["attn"]["workload"] if args.seq is None else f"attn reduced T={args.seq}"
+    res = {
+        "metric": ATTN_METRIC, "value": round(world * n / (ms / 1e3), 1), "unit": ATTN_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl + (" + order drift (ascending vs descending)" if args.drift else ""),
+                   "rows": n, "parts": K, "head_dim": d, "keyed_pairs": w.keyed_pairs(),
+                   "parts_bytes": w.out_parts.numel() * w.out_parts.element_size(),
+                   "l2": "inputs exceed L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{peaks['source']} copy bandwidth (burst)",
+                     "span": "whole call", "algorithmic_bytes_per_launch": nbytes},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (3 if args.drift else 1) * args.steps,
+        "clocks": clocks.summary(), "impl": "lpd",
+    }
+    print(json.dumps(res), flush=True)
+    return res
+
+
 def parse_chain(text: str):
     """'softcap:30,scale:1.4286' -> [(LPD_OP_SOFTCAP, 30.0), (LPD_OP_SCALE, 1.4286)]."""
     from logprob_drift_scoring_gb300 import binding as B
@@ -396,8 +539,8 @@ def run_ours(args):
 
     B.lib()  # fail loudly here if the CUDA library is missing
     w = make_workload(args.config, dev, seed_offset=rank, batch=args.batch, seq=args.seq)
-    if args.config == "fused":
-        out = run_fused(args, w, world, rank)
+    if args.config in ("fused", "attn"):
+        out = (run_fused if args.config == "fused" else run_attn)(args, w, world, rank)
         if world > 1:
             import torch.distributed as dist
 
@@ -565,6 +708,8 @@ def run_reference(args):
     import oracle
     from logprob_drift_scoring_gb300 import workloads as W
 
+    if args.config == "attn":
+        return run_reference_attn(args, world)
     vocab = CONFIGS[args.config]["vocab"]
     dt_r = torch.float32 if args.config == "llama" else torch.bfloat16
     rows_per_step = args.ref_rows
@@ -598,6 +743,36 @@ def run_reference(args):
     return out
 
 
+def run_reference_attn(args, world):
+    import oracle
+    from logprob_drift_scoring_gb300 import workloads as W
+
+    lib = oracle.load()
+    tokens = 1024  # 32768 rows of the recipe per step
+    times = []
+    for k in range(args.warmup + args.steps):
+        w = W.attn_partials(tokens, 32, 128, 8, seed=6000 + k, device="cpu")
+        parts, lse = w.out_parts.numpy(), w.lse_parts.numpy()
+        t0 = time.perf_counter()
+        oracle.attn_merge(parts, lse, lib=lib)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    rows = tokens * 32
+    value = rows / (ms / 1e3)
+    sample = f"{rows} rows per step (T={tokens} x 32 heads, K=8 causal, head_dim 128), float64 serial C"
+    out = {"metric": ATTN_METRIC, "value": round(value, 2), "unit": ATTN_UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": CONFIGS["attn"]["workload"], "sample_rows_per_step": rows},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 2), "unit": ATTN_UNIT, "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 2), "unit": ATTN_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -614,6 +789,8 @@ def main(argv=None):
                     help="logit transform chain on both sides, e.g. softcap:30,scale:1.4286")
     ap.add_argument("--entropy", action="store_true", help="time lpd_score_entropy instead of lpd_score")
     ap.add_argument("--backward", action="store_true", help="time lpd_logprob_backward of the train side")
+    ap.add_argument("--drift", action="store_true",
+                    help="attn config: time lpd_attn_merge_order_drift instead of lpd_attn_merge")
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")
     ap.add_argument("--seq", type=int, default=None, help="override T (small profiling cases only)")
     args = ap.parse_args(argv)

@@ -314,6 +314,78 @@ int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const 
                     lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                     void *stream);
 
+/* ---- attention (out, lse) merge --------------------------------------------- */
+
+/* Split-KV / context-parallel attention partials are merged with the same
+ * online-softmax algebra as the vocab shards above ("Attention Debug Matrix",
+ * row A7 merge_order; "[WS2] Framework for ablation experiment", Attention
+ * knobs table, rows 6-7: LSE domain/base and the CP / split-K merge order).
+ * Part k computed attention of each query row over one block of keys and
+ * returned its normalised output out_k[r, :] and its log-sum-exp lse_k[r].
+ * For every row r the merge gives
+ *
+ *     lse[r] = log(sum_k exp(lse_k[r])),   out[r, :] = sum_k exp(lse_k[r] - lse[r]) out_k[r, :]
+ *
+ * folding the parts one at a time, in `order`, into a running state
+ * (max m, sum s, unnormalised acc): a part above the running max rescales the
+ * state by exp(m - lse_k), the others add exp(lse_k - m) out_k; the result is
+ * acc / s and m + log(s).  Arithmetic is fp32 with a fixed per-row order, so
+ * the result depends on `order` only through rounding: which order is taken is
+ * the A7 diagnostic knob.  A part with lse_k[r] = -inf saw no keys for row r:
+ * it carries no weight and its out values are not read (they may be NaN).  A
+ * row no part saw gets out = 0 and lse = -inf.
+ *
+ * out_parts   device [n_parts][n_rows][head_dim], dense, dtype LPD_F32 or
+ *             LPD_BF16 (a partial state downcast to bf16, Attention knobs row
+ *             8), 16-byte aligned; head_dim * element size must be a multiple
+ *             of 16 bytes (head_dim % 4 == 0 for f32, % 8 for bf16), else
+ *             LPD_ERR_ALIGNMENT.
+ * lse_parts   device float [n_parts][n_rows], dense.
+ * lse_base2   0: lse values are natural-log (log-sum-exp); 1: base 2
+ *             (log2-sum-exp2, as some kernels export).  Inputs and the merged
+ *             lse use the same base.  Other values: LPD_ERR_BAD_SIZE.
+ * order       HOST int32[n_parts], a permutation of 0..n_parts-1 (else
+ *             LPD_ERR_BAD_SHARDS); NULL means ascending global block index
+ *             0, 1, ..., n_parts-1, the fixed order.
+ * out         device float [n_rows][head_dim], 16-byte aligned.
+ * out_lse     device float [n_rows].
+ * 1 <= n_parts <= LPD_ATTN_MAX_PARTS (else LPD_ERR_UNSUPPORTED);
+ * 0 <= n_rows < 2^32 - 1 and head_dim >= 1 (else LPD_ERR_BAD_SIZE).  No
+ * workspace; nothing is allocated. */
+#define LPD_ATTN_MAX_PARTS 64
+
+int lpd_attn_merge(const void *out_parts, int32_t parts_dtype, const float *lse_parts,
+                   int32_t n_parts, int64_t n_rows, int32_t head_dim, int32_t lse_base2,
+                   const int32_t *order, float *out, float *out_lse, void *stream);
+
+/* Summary of an order-drift run.  max_abs_dout is the largest |out_a - out_b|
+ * over all rows and columns, max_abs_dlse the largest |lse_a - lse_b| (0 where
+ * both are -inf); row_dout / row_dlse the lowest row attaining each (NaN ranks
+ * above every number, so a NaN anywhere is what gets reported).  With
+ * n_rows == 0 both maxima are 0 and both rows -1.  `scratch` is working
+ * space of the call; its contents afterwards mean nothing. */
+typedef struct {
+    double max_abs_dout;
+    double max_abs_dlse;
+    int64_t row_dout;
+    int64_t row_dlse;
+    uint64_t scratch[2];
+} lpd_merge_drift;
+
+/* The merge-order diagnostic itself: merges the same partials in order_a and
+ * in order_b in one pass over them and reports how far the two results are
+ * apart.  Arguments are those of lpd_attn_merge; out / out_lse receive the
+ * order_a result (bitwise what lpd_attn_merge gives for order_a), and
+ *   row_dout   device float [n_rows]: max over the row's columns of |out_a - out_b|,
+ *   row_dlse   device float [n_rows]: |lse_a - lse_b| (0 where both are -inf),
+ *   drift      device lpd_merge_drift, the summary above.
+ * order_a and order_b are host permutations; NULL means ascending order. */
+int lpd_attn_merge_order_drift(const void *out_parts, int32_t parts_dtype, const float *lse_parts,
+                               int32_t n_parts, int64_t n_rows, int32_t head_dim,
+                               int32_t lse_base2, const int32_t *order_a, const int32_t *order_b,
+                               float *out, float *out_lse, float *row_dout, float *row_dlse,
+                               lpd_merge_drift *drift, void *stream);
+
 /* ---- scoring without a caller-provided workspace -------------------------- */
 
 /* Largest n_rows lpd_score_noalloc accepts: its built-in scratch is sized for

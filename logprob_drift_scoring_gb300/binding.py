@@ -80,12 +80,25 @@ class LpdBackendInfo(ctypes.Structure):
 
 METRICS_BYTES = ctypes.sizeof(LpdMetrics)
 
+
+class LpdMergeDrift(ctypes.Structure):
+    _fields_ = [("max_abs_dout", ctypes.c_double), ("max_abs_dlse", ctypes.c_double),
+                ("row_dout", ctypes.c_int64), ("row_dlse", ctypes.c_int64), ("scratch", ctypes.c_uint64 * 2)]
+
+    def as_dict(self) -> dict:
+        return {"max_abs_dout": self.max_abs_dout, "max_abs_dlse": self.max_abs_dlse,
+                "row_dout": self.row_dout, "row_dlse": self.row_dlse}
+
+
+MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
+
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed", "lpd_score_entropy",
-            "lpd_logprob_backward")
+            "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift")
 LPD_NOALLOC_MAX_ROWS = 32768
+LPD_ATTN_MAX_PARTS = 64
 
 
 class LpdError(RuntimeError):
@@ -132,6 +145,10 @@ def lib() -> ctypes.CDLL:
         L.lpd_logprob_backward.argtypes = [P, I64, I64, P, P, P, P, P, I32, I64, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
+        L.lpd_attn_merge.restype = ctypes.c_int
+        L.lpd_attn_merge.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P]
+        L.lpd_attn_merge_order_drift.restype = ctypes.c_int
+        L.lpd_attn_merge_order_drift.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P]
         _LIB = L
     return _LIB
 
@@ -309,7 +326,73 @@ def lpd_score_noalloc(train, rollout, token_ids, action_mask, clip_lo, clip_hi, 
     _check(rc, "lpd_score_noalloc")
 
 
+def _order(order, n_parts):
+    if order is None:
+        return None
+    order = [int(k) for k in order]
+    if len(order) != n_parts:
+        raise ValueError(f"order has {len(order)} entries for {n_parts} parts")
+    return (ctypes.c_int32 * n_parts)(*order)
+
+
+def _parts_shape(out_parts, lse_parts):
+    if out_parts.dim() != 3 or not out_parts.is_contiguous() or not lse_parts.is_contiguous():
+        raise ValueError("out_parts must be a dense [K, n_rows, head_dim] tensor and lse_parts dense [K, n_rows]")
+    K, n, d = out_parts.shape
+    if tuple(lse_parts.shape) != (K, n):
+        raise ValueError("lse_parts must be [K, n_rows]")
+    return K, n, d
+
+
+def lpd_attn_merge(out_parts, lse_parts, order, out, out_lse, lse_base2=False, stream=None) -> None:
+    K, n, d = _parts_shape(out_parts, lse_parts)
+    rc = lib().lpd_attn_merge(_ptr(out_parts), _dtype_code(out_parts), _ptr(lse_parts), K, n, d, int(bool(lse_base2)),
+                              _order(order, K), _ptr(out), _ptr(out_lse), _stream(stream))
+    _check(rc, "lpd_attn_merge")
+
+
+def lpd_attn_merge_order_drift(out_parts, lse_parts, order_a, order_b, out, out_lse, row_dout, row_dlse, drift,
+                               lse_base2=False, stream=None) -> None:
+    K, n, d = _parts_shape(out_parts, lse_parts)
+    rc = lib().lpd_attn_merge_order_drift(_ptr(out_parts), _dtype_code(out_parts), _ptr(lse_parts), K, n, d,
+                                          int(bool(lse_base2)), _order(order_a, K), _order(order_b, K), _ptr(out),
+                                          _ptr(out_lse), _ptr(row_dout), _ptr(row_dlse), _ptr(drift), _stream(stream))
+    _check(rc, "lpd_attn_merge_order_drift")
+
+
 # ---- convenience: allocate with torch, call, read back ------------------------
+
+def read_merge_drift(buf) -> dict:
+    """Copy a device lpd_merge_drift record (uint8 tensor) to the host as a dict."""
+    host = buf.detach().to("cpu", copy=True).numpy().tobytes()
+    return LpdMergeDrift.from_buffer_copy(host).as_dict()
+
+
+def attn_merge(out_parts, lse_parts, order=None, lse_base2=False, stream=None):
+    """Merged (out [n, d] f32, lse [n] f32) of K partials, allocated with torch."""
+    import torch
+
+    K, n, d = _parts_shape(out_parts, lse_parts)
+    out = torch.empty((n, d), dtype=torch.float32, device=out_parts.device)
+    lse = torch.empty((n,), dtype=torch.float32, device=out_parts.device)
+    lpd_attn_merge(out_parts, lse_parts, order, out, lse, lse_base2, stream)
+    return out, lse
+
+
+def attn_merge_order_drift(out_parts, lse_parts, order_a=None, order_b=None, lse_base2=False, stream=None):
+    """(out, lse, row_dout, row_dlse, summary dict) of the order_a vs order_b merge."""
+    import torch
+
+    K, n, d = _parts_shape(out_parts, lse_parts)
+    dev = out_parts.device
+    out = torch.empty((n, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((n,), dtype=torch.float32, device=dev)
+    rdo = torch.empty((n,), dtype=torch.float32, device=dev)
+    rdl = torch.empty((n,), dtype=torch.float32, device=dev)
+    drift = torch.empty(MERGE_DRIFT_BYTES, dtype=torch.uint8, device=dev)
+    lpd_attn_merge_order_drift(out_parts, lse_parts, order_a, order_b, out, lse, rdo, rdl, drift, lse_base2, stream)
+    return out, lse, rdo, rdl, read_merge_drift(drift)
+
 
 def read_metrics(buf) -> dict:
     """Copy a device lpd_metrics record (uint8 tensor) to the host as a dict."""

@@ -223,6 +223,57 @@ int check_shards(const lpd_shard *sh, int n, int64_t n_rows, int64_t vocab, int 
     return next == vocab ? LPD_OK : LPD_ERR_BAD_SHARDS;
 }
 
+// Shared by lpd_attn_merge (diag false: no second order, no drift outputs) and
+// lpd_attn_merge_order_drift (diag true: all three drift outputs required).
+int attn_merge_impl(const void *out_parts, int32_t parts_dtype, const float *lse_parts, int32_t n_parts,
+                    int64_t n_rows, int32_t head_dim, int32_t lse_base2, const int32_t *order_a,
+                    const int32_t *order_b, float *out, float *out_lse, float *row_dout, float *row_dlse,
+                    lpd_merge_drift *drift, bool diag, void *stream) {
+    if (n_rows < 0 || n_rows >= 0xffffffffll || head_dim < 1 || (lse_base2 != 0 && lse_base2 != 1))
+        return LPD_ERR_BAD_SIZE;
+    if (n_parts < 1 || n_parts > LPD_ATTN_MAX_PARTS) return LPD_ERR_UNSUPPORTED;
+    if (!valid_dtype(parts_dtype)) return LPD_ERR_BAD_DTYPE;
+    if (diag && (!drift || (n_rows > 0 && (!row_dout || !row_dlse)))) return LPD_ERR_NULL_POINTER;
+    if (n_rows > 0 && (!out_parts || !lse_parts || !out || !out_lse)) return LPD_ERR_NULL_POINTER;
+    const int64_t row_bytes = static_cast<int64_t>(head_dim) * elt_bytes(parts_dtype);
+    if (row_bytes % 16 != 0) return LPD_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(out_parts) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+        reinterpret_cast<uintptr_t>(lse_parts) % 4 || reinterpret_cast<uintptr_t>(out_lse) % 4 ||
+        reinterpret_cast<uintptr_t>(row_dout) % 4 || reinterpret_cast<uintptr_t>(row_dlse) % 4 ||
+        reinterpret_cast<uintptr_t>(drift) % 8)
+        return LPD_ERR_ALIGNMENT;
+    // one block covers 128 chunks; the grid must fit in gridDim.x
+    const int64_t chunks = n_rows * (row_bytes / 16);
+    if (chunks / 128 >= 0x7fffffffll) return LPD_ERR_UNSUPPORTED;
+    int32_t ident[LPD_ATTN_MAX_PARTS];
+    for (int k = 0; k < n_parts; ++k) ident[k] = k;
+    const int32_t *orders[2] = {order_a ? order_a : ident, order_b ? order_b : ident};
+    for (const int32_t *o : orders) {
+        bool seen[LPD_ATTN_MAX_PARTS] = {false};
+        for (int k = 0; k < n_parts; ++k) {
+            if (o[k] < 0 || o[k] >= n_parts || seen[o[k]]) return LPD_ERR_BAD_SHARDS;
+            seen[o[k]] = true;
+        }
+    }
+    AttnMergeCall c{};
+    c.parts = out_parts;
+    c.bf16 = parts_dtype == LPD_BF16;
+    c.lse = lse_parts;
+    c.n_parts = n_parts;
+    c.n_rows = n_rows;
+    c.head_dim = head_dim;
+    c.base2 = lse_base2;
+    c.order_a = orders[0];
+    c.order_b = orders[1];
+    c.out = out;
+    c.out_lse = out_lse;
+    c.diag = diag;
+    c.row_dout = row_dout;
+    c.row_dlse = row_dlse;
+    c.drift = drift;
+    return cuda_status(launch_attn_merge(c, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace lpd
 
@@ -490,6 +541,21 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                        out_perm_logp_rollout, out_metrics, w, s)))
         return rc;
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+int lpd_attn_merge(const void *out_parts, int32_t parts_dtype, const float *lse_parts, int32_t n_parts, int64_t n_rows,
+                   int32_t head_dim, int32_t lse_base2, const int32_t *order, float *out, float *out_lse,
+                   void *stream) {
+    return attn_merge_impl(out_parts, parts_dtype, lse_parts, n_parts, n_rows, head_dim, lse_base2, order, nullptr,
+                           out, out_lse, nullptr, nullptr, nullptr, false, stream);
+}
+
+int lpd_attn_merge_order_drift(const void *out_parts, int32_t parts_dtype, const float *lse_parts, int32_t n_parts,
+                               int64_t n_rows, int32_t head_dim, int32_t lse_base2, const int32_t *order_a,
+                               const int32_t *order_b, float *out, float *out_lse, float *row_dout, float *row_dlse,
+                               lpd_merge_drift *drift, void *stream) {
+    return attn_merge_impl(out_parts, parts_dtype, lse_parts, n_parts, n_rows, head_dim, lse_base2, order_a, order_b,
+                           out, out_lse, row_dout, row_dlse, drift, true, stream);
 }
 
 size_t lpd_fused_workspace_size(int64_t n_rows, int64_t hidden, int64_t vocab) {

@@ -155,6 +155,25 @@ cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, 
                             int64_t out_stride_elems, int64_t n_rows, int64_t vocab, const int32_t *ids,
                             const uint8_t *mask, const float *logp, const float *grad, cudaStream_t stream);
 
+// Attention (out, lse) merge: one call of lpd_attn_merge (diag false) or of
+// lpd_attn_merge_order_drift (diag true).  Orders are validated permutations.
+struct AttnMergeCall {
+    const void *parts;
+    bool bf16;
+    const float *lse;
+    int n_parts;
+    int64_t n_rows;
+    int head_dim;
+    int base2;
+    const int32_t *order_a, *order_b;   // host, n_parts entries each
+    float *out, *out_lse;
+    bool diag;
+    float *row_dout, *row_dlse;
+    lpd_merge_drift *drift;
+};
+size_t attn_merge_smem(int n_parts, int cpr);
+cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace lpd

@@ -25,6 +25,13 @@ shapes, dtypes, vocab sizes, padding layouts and masks stand in for it:
   fused    LM head: hidden [16384, 4096] bf16 N(0, 1), W [151936, 4096] bf16
            N(0, 0.02^2), rollout hidden = bf16(hidden + N(0, 1e-3^2)); all
            rows active; ids uniform.
+  attn     attention partials of a context-parallel causal prefill: T=32768
+           tokens x 32 query heads (Qwen3-8B), head_dim 128, keys split into
+           K=8 contiguous blocks of T/K.  Row = (token t, head h), token-major.
+           Part k saw n_k = |block k intersect [0, t]| keys: lse_k = log(n_k)
+           + N(2, 1^2) when n_k > 0, else -inf (and its out is 0, as many
+           kernels leave it); out_k N(0, 0.5^2) f32.  About (K-1)/2K of the
+           (row, part) pairs have no keys.
 
 Noise scales are standard deviations.  Generation runs on the target device
 with a seeded torch.Generator; large tensors are generated in row chunks.
@@ -226,4 +233,67 @@ def head(n_rows: int, hidden: int, vocab: int, *, seed: int = 4, device="cuda", 
 def fused(seed: int = 4, device="cuda", rows: int = 16384) -> HeadWorkload:
     w = head(rows, 4096, 151936, seed=seed, device=device)
     w.name = "fused-lm-head"
+    return w
+
+
+@dataclass
+class AttnWorkload:
+    name: str
+    out_parts: torch.Tensor   # [K, n_rows, head_dim] f32 or bf16
+    lse_parts: torch.Tensor   # [K, n_rows] f32
+    n_tokens: int
+    n_heads: int
+    lse_base2: bool = False
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n_parts(self) -> int:
+        return int(self.out_parts.shape[0])
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.out_parts.shape[1])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.out_parts.shape[2])
+
+    def keyed_pairs(self) -> int:
+        """(row, part) pairs whose part saw at least one key."""
+        return int(torch.isfinite(self.lse_parts).sum().item())
+
+
+def attn_partials(n_tokens: int, n_heads: int, head_dim: int, n_parts: int, *, seed: int = 5, device="cuda",
+                  dtype=torch.float32, causal: bool = True, lse_base2: bool = False,
+                  masked_fill: float = 0.0, out_sigma: float = 0.5) -> AttnWorkload:
+    """Per-block attention partials of T tokens x H heads over K contiguous key
+    blocks (the attn recipe).  masked_fill is written into the out rows of
+    parts that saw no keys (0, or NaN to prove they are never read)."""
+    g = _gen(device, seed)
+    T, H, K = n_tokens, n_heads, n_parts
+    t = torch.arange(T, device=device)
+    lse = torch.empty((K, T * H), dtype=torch.float32, device=device)
+    out = torch.empty((K, T * H, head_dim), dtype=dtype, device=device)
+    step = _chunk_rows(head_dim)
+    for k in range(K):
+        start, end = k * T // K, (k + 1) * T // K
+        n_k = (torch.clamp(torch.minimum(t + 1, torch.tensor(end, device=device)) - start, min=0) if causal
+               else torch.full((T,), end - start, device=device))
+        base = torch.log(n_k.to(torch.float32)).repeat_interleave(H)          # -inf where n_k == 0
+        lk = base + 2.0 + torch.randn((T * H,), generator=g, device=device)
+        if lse_base2:
+            lk = lk / torch.log(torch.tensor(2.0, device=device))
+        lse[k] = lk
+        for c in range(0, T * H, step):
+            n = min(step, T * H - c)
+            out[k, c:c + n] = (out_sigma * torch.randn((n, head_dim), generator=g, device=device)).to(dtype)
+        dead = ~torch.isfinite(lse[k])
+        out[k][dead] = torch.tensor(masked_fill, dtype=dtype, device=device)
+    return AttnWorkload("attn", out, lse, T, H, lse_base2,
+                        meta={"seed": seed, "causal": causal, "masked_fill": masked_fill})
+
+
+def attn(seed: int = 5, device="cuda", n_tokens: int = 32768, dtype=torch.float32) -> AttnWorkload:
+    w = attn_partials(n_tokens, 32, 128, 8, seed=seed, device=device, dtype=dtype)
+    w.name = "cp8-attention-partials"
     return w

@@ -30,6 +30,7 @@ def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(B.LpdShard) == 40
     assert ctypes.sizeof(B.LpdMetrics) == 80
     assert ctypes.sizeof(B.LpdBackendInfo) == 32 + 48 + 16 + 32 + 16 + 96
+    assert ctypes.sizeof(B.LpdMergeDrift) == 48
 
 
 def test_backend_info():
@@ -219,3 +220,62 @@ def test_entropy_and_backward_validation():
     assert call(stride=15) == B.LPD_ERR_BAD_STRIDE
     assert call(out=FAKE + 2) == B.LPD_ERR_ALIGNMENT
     assert call(v=0) == B.LPD_ERR_BAD_SIZE
+
+
+def _call_merge(parts=FAKE, dtype=B.LPD_F32, lse=FAKE, K=4, n=8, d=128, base2=0, order_a=None, order_b=None,
+                out=FAKE, out_lse=FAKE, rdo=FAKE, rdl=FAKE, drift=FAKE, diag=True):
+    lib = B.lib()
+    oa = None if order_a is None else (ctypes.c_int32 * len(order_a))(*order_a)
+    ob = None if order_b is None else (ctypes.c_int32 * len(order_b))(*order_b)
+    if diag:
+        return lib.lpd_attn_merge_order_drift(parts, dtype, lse, K, n, d, base2, oa, ob, out, out_lse, rdo, rdl,
+                                              drift, None)
+    return lib.lpd_attn_merge(parts, dtype, lse, K, n, d, base2, oa, out, out_lse, None)
+
+
+@pytest.mark.parametrize("diag", [False, True])
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(n=-1), B.LPD_ERR_BAD_SIZE),
+    (dict(n=0xFFFFFFFF), B.LPD_ERR_BAD_SIZE),
+    (dict(d=0), B.LPD_ERR_BAD_SIZE),
+    (dict(base2=2), B.LPD_ERR_BAD_SIZE),
+    (dict(K=0), B.LPD_ERR_UNSUPPORTED),
+    (dict(K=B.LPD_ATTN_MAX_PARTS + 1), B.LPD_ERR_UNSUPPORTED),
+    (dict(dtype=7), B.LPD_ERR_BAD_DTYPE),
+    (dict(parts=None), B.LPD_ERR_NULL_POINTER),
+    (dict(lse=None), B.LPD_ERR_NULL_POINTER),
+    (dict(out=None), B.LPD_ERR_NULL_POINTER),
+    (dict(out_lse=None), B.LPD_ERR_NULL_POINTER),
+    (dict(d=6), B.LPD_ERR_ALIGNMENT),                       # 24-byte rows
+    (dict(dtype=B.LPD_BF16, d=12), B.LPD_ERR_ALIGNMENT),    # 24-byte rows
+    (dict(parts=FAKE + 8), B.LPD_ERR_ALIGNMENT),
+    (dict(out=FAKE + 4), B.LPD_ERR_ALIGNMENT),
+    (dict(lse=FAKE + 2), B.LPD_ERR_ALIGNMENT),
+    (dict(order_a=[0, 1, 1, 3]), B.LPD_ERR_BAD_SHARDS),
+    (dict(order_a=[0, 1, 2, 4]), B.LPD_ERR_BAD_SHARDS),
+    (dict(order_a=[0, 1, 2, -1]), B.LPD_ERR_BAD_SHARDS),
+])
+def test_attn_merge_rejects_invalid_arguments(kwargs, code, diag):
+    assert _call_merge(diag=diag, **kwargs) == code
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(drift=None), B.LPD_ERR_NULL_POINTER),
+    (dict(drift=None, n=0), B.LPD_ERR_NULL_POINTER),
+    (dict(rdo=None), B.LPD_ERR_NULL_POINTER),
+    (dict(rdl=None), B.LPD_ERR_NULL_POINTER),
+    (dict(rdo=FAKE + 2), B.LPD_ERR_ALIGNMENT),
+    (dict(drift=FAKE + 4), B.LPD_ERR_ALIGNMENT),
+    (dict(order_b=[3, 2, 2, 0]), B.LPD_ERR_BAD_SHARDS),
+])
+def test_attn_merge_drift_rejects_invalid_arguments(kwargs, code):
+    assert _call_merge(**kwargs) == code
+
+
+def test_attn_merge_binding_checks_shapes():
+    torch = pytest.importorskip("torch")
+    parts = torch.zeros((2, 3, 8))
+    with pytest.raises(ValueError):
+        B.attn_merge(parts, torch.zeros((3, 2)))
+    with pytest.raises(ValueError):
+        B.attn_merge(parts, torch.zeros((2, 3)), order=[0])
