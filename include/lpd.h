@@ -349,7 +349,8 @@ int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const 
  *             0, 1, ..., n_parts-1, the fixed order.
  * out         device float [n_rows][head_dim], 16-byte aligned.
  * out_lse     device float [n_rows].
- * 1 <= n_parts <= LPD_ATTN_MAX_PARTS (else LPD_ERR_UNSUPPORTED);
+ * 1 <= n_parts <= LPD_ATTN_MAX_PARTS and one part at most 2^32 - 2 16-byte
+ * chunks (n_rows * head_dim * element size < 64 GB), else LPD_ERR_UNSUPPORTED;
  * 0 <= n_rows < 2^32 - 1 and head_dim >= 1 (else LPD_ERR_BAD_SIZE).  No
  * workspace; nothing is allocated. */
 #define LPD_ATTN_MAX_PARTS 64

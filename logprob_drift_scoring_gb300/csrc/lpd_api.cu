@@ -242,9 +242,9 @@ int attn_merge_impl(const void *out_parts, int32_t parts_dtype, const float *lse
         reinterpret_cast<uintptr_t>(row_dout) % 4 || reinterpret_cast<uintptr_t>(row_dlse) % 4 ||
         reinterpret_cast<uintptr_t>(drift) % 8)
         return LPD_ERR_ALIGNMENT;
-    // one block covers 128 chunks; the grid must fit in gridDim.x
+    // chunk indices are 32-bit: at most 2^32 - 1 16-byte chunks (64 GB) per part
     const int64_t chunks = n_rows * (row_bytes / 16);
-    if (chunks / 128 >= 0x7fffffffll) return LPD_ERR_UNSUPPORTED;
+    if (chunks >= 0xffffffffll) return LPD_ERR_UNSUPPORTED;
     int32_t ident[LPD_ATTN_MAX_PARTS];
     for (int k = 0; k < n_parts; ++k) ident[k] = k;
     const int32_t *orders[2] = {order_a ? order_a : ident, order_b ? order_b : ident};

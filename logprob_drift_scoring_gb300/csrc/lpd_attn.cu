@@ -9,8 +9,9 @@
 // folded one part at a time in a caller-given order (the A7 knob).
 //
 // Layout: the merge streams K * n_rows * head_dim values once and writes one
-// n_rows * head_dim result, so it is bound by HBM.  Each thread owns one
-// 16-byte chunk of one row (4 f32 or 8 bf16 columns); a block of 128 threads
+// n_rows * head_dim result, so it is bound by HBM.  Each thread owns one or
+// two adjacent 16-byte chunks of one row (4 or 8 f32 columns, 8 or 16 bf16),
+// so the per-part scalar work of the fold is shared by them; a block of 128 threads
 // copies the lse values of the rows it touches, then the chunks of every part
 // whose lse is finite (a causal split leaves many (row, part) pairs without
 // keys), into shared memory with cp.async (every copy of a thread in flight at
@@ -29,21 +30,27 @@ namespace {
 
 constexpr int kMergeThreads = 128;
 constexpr int kMaxParts = LPD_ATTN_MAX_PARTS;
+constexpr int kSmallParts = 8;  // part counts up to this run fully unrolled
 
+// A thread's unit is kV adjacent 16-byte chunks of one row (kV = 2 when a row
+// has an even number of chunks and the block's staging fits, else 1).
 struct MergeArgs {
-    const char *parts;       // [K][n][d] chunks of 16 bytes
+    const char *parts;       // [K][n][d] as 16-byte chunks
     const float *lse;        // [K][n]
     float *out;              // [n][d]
     float *out_lse;          // [n]
     unsigned *row_dout;      // [n], float bits, zeroed by the caller (drift only)
     float *row_dlse;         // [n] (drift only)
     int64_t n;               // rows
-    int64_t total;           // chunks per part = n * cpr
-    int cpr;                 // 16-byte chunks per row
+    int64_t part_bytes;      // bytes of one part
+    uint32_t units;          // units per part = n * cpr / kV (below 2^32, checked by the caller)
+    uint32_t upr;            // units per row
+    int upr_shift;           // log2(upr) when upr is a power of two, else -1
     int n_parts;
     int nr_max;              // bound on the rows one block touches
     int base2;
     uint8_t order_a[kMaxParts], order_b[kMaxParts];
+    int64_t off_a[kSmallParts];  // order_a[k] * part_bytes for the first parts
 };
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -61,7 +68,7 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <bool kBf16>
-__device__ __forceinline__ void unpack(const uint4 w, float (&v)[kBf16 ? 8 : 4]) {
+__device__ __forceinline__ void unpack(const uint4 w, float *v) {
     if constexpr (kBf16) {
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -77,116 +84,254 @@ __device__ __forceinline__ void unpack(const uint4 w, float (&v)[kBf16 ? 8 : 4])
     }
 }
 
-// One row chunk folded over the parts in `ord`: running max m, running sum s
-// of exp(lse_k - m), unnormalised accumulator acc; a part above the running
-// max rescales the state instead of being scaled itself.  A part with
-// lse = -inf is skipped.  c converts an lse difference to base 2 for ex2.
-template <bool kBf16>
-__device__ __forceinline__ void fold(const uint4 *chunk_s, const float *lse_s, int nr_max, const uint8_t *ord, int K,
-                                     int t, int rl, float c, bool base2, float (&o)[kBf16 ? 8 : 4], float &lse) {
-    constexpr int E = kBf16 ? 8 : 4;
-    float m = -CUDART_INF_F, s = 0.f, acc[E];
+// Staged shared memory of one block: chunk_s[(k * kV + v) * 128 + t] holds
+// chunk v of thread t's unit in part k (consecutive threads, consecutive 16
+// bytes: no bank conflicts); lse_s[rr * kMaxK + k] the lse of the block's
+// row rr in part k; ord_s both orders (the looped kMaxK = 64 form only).
+template <int kV, int kMaxK>
+struct Staged {
+    const uint4 *chunk_s;
+    const float *lse_s;
+    const uint8_t *ord_s;
+};
+
+// Part visited k-th in order A (kB false) or B.  The unrolled form (every k a
+// constant) reads the order straight from the kernel parameters.
+template <int kMaxK, bool kB>
+__device__ __forceinline__ int order_at(const MergeArgs &a, const uint8_t *ord_s, int k) {
+    if constexpr (kMaxK <= kSmallParts)
+        return kB ? a.order_b[k] : a.order_a[k];
+    else
+        return ord_s[(kB ? kMaxParts : 0) + k];
+}
+
+// Running state of one unit's fold: max m, sum s of exp(lse_k - m) and the
+// unnormalised accumulator acc.  A part above the running max rescales the
+// state instead of being scaled itself.  cvt converts an lse difference to
+// base 2 for ex2.
+template <int N>
+struct FoldState {
+    float m, s, acc[N];
+};
+
+template <int N>
+__device__ __forceinline__ void fold_init(FoldState<N> &f) {
+    f.m = -CUDART_INF_F;
+    f.s = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int k = 0; k < K; ++k) {
-        const int p = ord[k];
-        const float l = lse_s[p * nr_max + rl];
-        if (l == -CUDART_INF_F) continue;
-        float v[E];
-        unpack<kBf16>(chunk_s[p * kMergeThreads + t], v);
-        if (l > m) {
-            const float sc = ex2(__fmul_rn(__fsub_rn(m, l), c));  // 0 while m is still -inf
-            s = __fmaf_rn(s, sc, 1.f);
+    for (int e = 0; e < N; ++e) f.acc[e] = 0.f;
+}
+
+template <int N>
+__device__ __forceinline__ void fold_step(FoldState<N> &f, float l, const float *v, float cvt) {
+    if (l > f.m) {
+        const float sc = ex2(__fmul_rn(__fsub_rn(f.m, l), cvt));  // 0 while m is still -inf
+        f.s = __fmaf_rn(f.s, sc, 1.f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(acc[e], sc, v[e]);
-            m = l;
-        } else {
-            const float w = ex2(__fmul_rn(__fsub_rn(l, m), c));
-            s = __fadd_rn(s, w);
+        for (int e = 0; e < N; ++e) f.acc[e] = __fmaf_rn(f.acc[e], sc, v[e]);
+        f.m = l;
+    } else {
+        const float w = ex2(__fmul_rn(__fsub_rn(l, f.m), cvt));
+        f.s = __fadd_rn(f.s, w);
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(w, v[e], acc[e]);
-        }
+        for (int e = 0; e < N; ++e) f.acc[e] = __fmaf_rn(w, v[e], f.acc[e]);
     }
-    if (s > 0.f) {
+}
+
+// out = acc / s and (only where asked: the row's first unit) lse = m + log s;
+// a unit no part saw gives out 0 and lse -inf.
+template <int N>
+__device__ __forceinline__ void fold_finish(const FoldState<N> &f, bool want_lse, bool base2, float *o, float &lse) {
+    if (f.s > 0.f) {
+        const float inv = __frcp_rn(f.s);
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = __fdiv_rn(acc[e], s);
-        lse = __fadd_rn(m, base2 ? log2f(s) : logf(s));
+        for (int e = 0; e < N; ++e) o[e] = __fmul_rn(f.acc[e], inv);
+        if (want_lse) lse = __fadd_rn(f.m, base2 ? log2f(f.s) : logf(f.s));
     } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = 0.f;
+        for (int e = 0; e < N; ++e) o[e] = 0.f;
         lse = -CUDART_INF_F;
     }
 }
 
-template <bool kBf16, bool kDrift>
+// One unit folded over the parts in order A or B, chunks staged by part index.
+// A part with lse = -inf is skipped.
+template <bool kBf16, int kV, int kMaxK, bool kB>
+__device__ __forceinline__ void fold(const MergeArgs &a, const Staged<kV, kMaxK> &st, int K, int t, int rl, float cvt,
+                                     bool want_lse, float *o, float &lse) {
+    constexpr int E = kBf16 ? 8 : 4;
+    FoldState<kV * E> f;
+    fold_init(f);
+#pragma unroll(kMaxK <= kSmallParts ? kMaxK : 1)
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k >= K) break;
+        const int p = order_at<kMaxK, kB>(a, st.ord_s, k);
+        const float l = st.lse_s[rl * kMaxK + p];
+        if (l == -CUDART_INF_F) continue;
+        float v[kV * E];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) unpack<kBf16>(st.chunk_s[(p * kV + u) * kMergeThreads + t], v + u * E);
+        fold_step(f, l, v, cvt);
+    }
+    fold_finish(f, want_lse, a.base2, o, lse);
+}
+
+// The plain merge of up to kSmallParts parts: the row's lse values sit in
+// registers in visiting order and chunk k of the visit is staged in slot k.
+template <bool kBf16>
+__device__ __forceinline__ void fold_seq(const MergeArgs &a, const float (&l)[kSmallParts], const uint4 *chunk_s,
+                                         int t, float cvt, bool want_lse, float *o, float &lse) {
+    constexpr int E = kBf16 ? 8 : 4;
+    FoldState<E> f;
+    fold_init(f);
+#pragma unroll
+    for (int k = 0; k < kSmallParts; ++k) {
+        if (l[k] == -CUDART_INF_F) continue;  // also every k >= K
+        float v[E];
+        unpack<kBf16>(chunk_s[k * kMergeThreads + t], v);
+        fold_step(f, l[k], v, cvt);
+    }
+    fold_finish(f, want_lse, a.base2, o, lse);
+}
+
+// Row of a unit index: a shift for the usual power-of-two head sizes.
+__device__ __forceinline__ uint32_t unit_row(const MergeArgs &a, uint32_t u) {
+    return a.upr_shift >= 0 ? u >> a.upr_shift : u / a.upr;
+}
+
+// A tile is 128 consecutive units: the rows [r0, r0 + nr) it touches.
+struct Tile {
+    uint32_t u0, r0;
+    int nr;
+};
+
+__device__ __forceinline__ Tile tile_at(const MergeArgs &a, uint32_t tile) {
+    Tile g;
+    g.u0 = tile * static_cast<uint32_t>(kMergeThreads);
+    g.r0 = unit_row(a, g.u0);
+    const uint32_t u_last = (a.units - g.u0 > static_cast<uint32_t>(kMergeThreads) ? g.u0 + kMergeThreads : a.units) - 1;
+    g.nr = static_cast<int>(unit_row(a, u_last) - g.r0 + 1);
+    return g;
+}
+
+// Copy the lse of every part for the tile's rows into lse_s[rr * kMaxK + k].
+template <int kMaxK>
+__device__ __forceinline__ void stage_lse(const MergeArgs &a, const Tile &g, float *lse_s, int t, int K) {
+    for (int rr = t; rr < g.nr; rr += kMergeThreads) {
+#pragma unroll(kMaxK <= kSmallParts ? kMaxK : 1)
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            cp_async4(lse_s + rr * kMaxK + k, a.lse + static_cast<int64_t>(k) * a.n + g.r0 + rr);
+        }
+    }
+}
+
+// Persistent blocks walk tiles blockIdx.x, blockIdx.x + gridDim.x, ...  The
+// lse of a block's next tile is copied while the current tile's chunks are in
+// flight, so each tile costs one memory round trip, not two.
+template <bool kBf16, bool kDrift, int kV, int kMaxK>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeArgs a) {
     constexpr int E = kBf16 ? 8 : 4;
+    // plain merge of few parts: visiting order fixed per launch, one chunk per thread
+    constexpr bool kSeq = !kDrift && kMaxK <= kSmallParts && kV == 1;
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = a.n_parts;
-    uint4 *chunk_s = reinterpret_cast<uint4 *>(smem);                                   // [K][128]
-    float *lse_s = reinterpret_cast<float *>(smem + static_cast<size_t>(K) * kMergeThreads * 16);  // [K][nr_max]
-    unsigned *rowmax_s = reinterpret_cast<unsigned *>(lse_s + K * a.nr_max);           // [nr_max]
-    uint8_t *ord_s = reinterpret_cast<uint8_t *>(rowmax_s + a.nr_max);                  // [2][kMaxParts]
+    const int lse_stride = a.nr_max * kMaxK;
+    uint4 *chunk_s = reinterpret_cast<uint4 *>(smem);
+    float *lse_s = reinterpret_cast<float *>(smem + static_cast<size_t>(K) * kV * kMergeThreads * 16);  // [2][lse_stride]
+    unsigned *rowmax_s = reinterpret_cast<unsigned *>(lse_s + 2 * lse_stride);
+    uint8_t *ord_s = reinterpret_cast<uint8_t *>(rowmax_s + a.nr_max);
 
     const int t = threadIdx.x;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kMergeThreads;
-    const int64_t c = c0 + t;
-    const bool live = c < a.total;
-    const int64_t r0 = c0 / a.cpr;
-    const int64_t c_end = c0 + kMergeThreads < a.total ? c0 + kMergeThreads : a.total;
-    const int nr = static_cast<int>((c_end - 1) / a.cpr - r0 + 1);
-
-    // lse of the rows this block touches first: a part with lse = -inf saw no
-    // keys for that row, and its chunk is never copied
-    for (int i = t; i < K * nr; i += kMergeThreads) {
-        const int k = i / nr, rr = i - k * nr;
-        cp_async4(lse_s + k * a.nr_max + rr, a.lse + k * a.n + r0 + rr);
+    const uint32_t n_tiles = static_cast<uint32_t>((static_cast<uint64_t>(a.units) + kMergeThreads - 1) / kMergeThreads);
+    uint32_t tile = blockIdx.x;
+    if (tile >= n_tiles) return;  // whole block
+    if constexpr (kMaxK > kSmallParts) {
+        if (t < K) {
+            ord_s[t] = a.order_a[t];
+            if (kDrift) ord_s[kMaxParts + t] = a.order_b[t];
+        }
     }
-    if (t < K) {
-        ord_s[t] = a.order_a[t];
-        if (kDrift) ord_s[kMaxParts + t] = a.order_b[t];
-    }
-    if (kDrift)
-        for (int i = t; i < nr; i += kMergeThreads) rowmax_s[i] = 0u;
+    Tile g = tile_at(a, tile);
+    stage_lse<kMaxK>(a, g, lse_s, t, K);
     cp_async_wait_all();
     __syncthreads();
 
-    const int64_t row = c / a.cpr;
-    const int rl = static_cast<int>(row - r0);
-    if (live) {
-        const char *src = a.parts + c * 16;
-        const int64_t part_bytes = a.total * 16;
-        for (int k = 0; k < K; ++k)
-            if (lse_s[k * a.nr_max + rl] != -CUDART_INF_F)
-                cp_async16(chunk_s + k * kMergeThreads + t, src + k * part_bytes);
-        cp_async_wait_all();  // each thread reads back only its own chunks
-    }
-
     const float cvt = a.base2 ? 1.f : kLog2e;
-    const bool head = live && row * a.cpr == c;  // first chunk of its row
-    float oa[E], la = 0.f;
-    if (live) {
-        fold<kBf16>(chunk_s, lse_s, a.nr_max, ord_s, K, t, rl, cvt, a.base2, oa, la);
-        float4 *dst = reinterpret_cast<float4 *>(a.out + c * E);
-        dst[0] = make_float4(oa[0], oa[1], oa[2], oa[3]);
-        if constexpr (kBf16) dst[1] = make_float4(oa[4], oa[5], oa[6], oa[7]);
-        if (head) a.out_lse[row] = la;
-    }
-    if constexpr (kDrift) {
-        if (live) {
-            float ob[E], lb;
-            fold<kBf16>(chunk_s, lse_s, a.nr_max, ord_s + kMaxParts, K, t, rl, cvt, a.base2, ob, lb);
-            float dmax = 0.f;
+    int buf = 0;
+    for (;;) {
+        const float *lcur = lse_s + buf * lse_stride;
+        const uint32_t u = g.u0 + t;
+        const bool live = u < a.units;
+        const uint32_t row = unit_row(a, u);
+        const int rl = static_cast<int>(row - g.r0);
+        // a part with lse = -inf saw no keys for this row: its chunks are never copied
+        const char *src = a.parts + static_cast<int64_t>(u) * (16 * kV);
+        float lseq[kSmallParts];  // kSeq: the row's lse in visiting order
+        if constexpr (kSeq) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float d = oa[e] == ob[e] ? 0.f : fabsf(__fsub_rn(oa[e], ob[e]));
-                dmax = (d > dmax || d != d) ? d : dmax;  // NaN wins
+            for (int k = 0; k < kSmallParts; ++k) {
+                lseq[k] = (live && k < K) ? lcur[rl * kMaxK + a.order_a[k]] : -CUDART_INF_F;
+                if (lseq[k] != -CUDART_INF_F) cp_async16(chunk_s + k * kMergeThreads + t, src + a.off_a[k]);
             }
-            atomicMax(rowmax_s + rl, __float_as_uint(dmax));
-            if (head) a.row_dlse[row] = la == lb ? 0.f : fabsf(__fsub_rn(la, lb));
+        } else if (live) {
+#pragma unroll(kMaxK <= kSmallParts ? kMaxK : 1)
+            for (int k = 0; k < kMaxK; ++k) {
+                if (k >= K) break;
+                if (lcur[rl * kMaxK + k] != -CUDART_INF_F) {
+#pragma unroll
+                    for (int v = 0; v < kV; ++v)
+                        cp_async16(chunk_s + (k * kV + v) * kMergeThreads + t, src + k * a.part_bytes + 16 * v);
+                }
+            }
         }
-        __syncthreads();
-        for (int i = t; i < nr; i += kMergeThreads) atomicMax(a.row_dout + r0 + i, rowmax_s[i]);
+        const uint32_t next = tile + gridDim.x;
+        const bool more = next < n_tiles;
+        Tile gn = g;
+        if (more) {
+            gn = tile_at(a, next);
+            stage_lse<kMaxK>(a, gn, lse_s + (buf ^ 1) * lse_stride, t, K);
+        }
+        if (kDrift)
+            for (int i = t; i < g.nr; i += kMergeThreads) rowmax_s[i] = 0u;
+        cp_async_wait_all();
+        __syncthreads();  // the next tile's lse and the zeroed row maxima are visible
+
+        const Staged<kV, kMaxK> st{chunk_s, lcur, ord_s};
+        const bool head = live && row * a.upr == u;  // first unit of its row
+        float oa[kV * E], la = 0.f;
+        if (live) {
+            if constexpr (kSeq)
+                fold_seq<kBf16>(a, lseq, chunk_s, t, cvt, head, oa, la);
+            else
+                fold<kBf16, kV, kMaxK, false>(a, st, K, t, rl, cvt, head, oa, la);
+            float4 *dst = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(u) * (kV * E));
+#pragma unroll
+            for (int q = 0; q < kV * E / 4; ++q)
+                dst[q] = make_float4(oa[4 * q], oa[4 * q + 1], oa[4 * q + 2], oa[4 * q + 3]);
+            if (head) a.out_lse[row] = la;
+        }
+        if constexpr (kDrift) {
+            if (live) {
+                float ob[kV * E], lb;
+                fold<kBf16, kV, kMaxK, true>(a, st, K, t, rl, cvt, head, ob, lb);
+                float dmax = 0.f;
+#pragma unroll
+                for (int e = 0; e < kV * E; ++e) {
+                    const float d = oa[e] == ob[e] ? 0.f : fabsf(__fsub_rn(oa[e], ob[e]));
+                    dmax = (d > dmax || d != d) ? d : dmax;  // NaN wins
+                }
+                atomicMax(rowmax_s + rl, __float_as_uint(dmax));
+                if (head) a.row_dlse[row] = la == lb ? 0.f : fabsf(__fsub_rn(la, lb));
+            }
+            __syncthreads();
+            for (int i = t; i < g.nr; i += kMergeThreads) atomicMax(a.row_dout + g.r0 + i, rowmax_s[i]);
+        }
+        if (!more) break;
+        __syncthreads();  // every thread is done with this tile's lse buffer before it is refilled
+        tile = next;
+        g = gn;
+        buf ^= 1;
     }
 }
 
@@ -246,23 +391,56 @@ __global__ void drift_finalize_kernel(lpd_merge_drift *d, int64_t n) {
     d->row_dlse = static_cast<int64_t>(0xffffffffull - (kl & 0xffffffffull));
 }
 
-template <bool kBf16, bool kDrift>
-cudaError_t launch_merge(const MergeArgs &a, size_t smem, unsigned blocks, cudaStream_t stream) {
-    auto *fn = merge_kernel<kBf16, kDrift>;
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+// Plain merge: a persistent grid, as many blocks as fit on every SM at once,
+// each walking tiles blockIdx.x, blockIdx.x + gridDim.x, ...  Order drift:
+// one block per tile.
+template <bool kBf16, bool kDrift, int kV, int kMaxK>
+cudaError_t launch_merge(const MergeArgs &a, size_t smem, cudaStream_t stream) {
+    auto *fn = merge_kernel<kBf16, kDrift, kV, kMaxK>;
+    cudaError_t e;
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
+            cudaSuccess)
+        return e;
+    const int64_t tiles = (static_cast<int64_t>(a.units) + kMergeThreads - 1) / kMergeThreads;
+    int64_t grid = tiles;
+    if (!kDrift) {
+        // the drift form's second fold and extra barriers leave each block's
+        // memory idle for longer: one block per tile keeps more copies in flight
+        int per_sm = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kMergeThreads, smem)) != cudaSuccess)
+            return e;
+        const int64_t resident = static_cast<int64_t>(device_sm_count()) * (per_sm > 0 ? per_sm : 1);
+        grid = tiles < resident ? tiles : resident;
     }
-    fn<<<blocks, kMergeThreads, smem, stream>>>(a);
+    fn<<<static_cast<unsigned>(grid), kMergeThreads, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <bool kBf16, bool kDrift>
+cudaError_t launch_merge_shape(const MergeArgs &a, int kv, size_t smem, cudaStream_t stream) {
+    if (a.n_parts <= kSmallParts)
+        return kv == 2 ? launch_merge<kBf16, kDrift, 2, kSmallParts>(a, smem, stream)
+                       : launch_merge<kBf16, kDrift, 1, kSmallParts>(a, smem, stream);
+    return kv == 2 ? launch_merge<kBf16, kDrift, 2, kMaxParts>(a, smem, stream)
+                   : launch_merge<kBf16, kDrift, 1, kMaxParts>(a, smem, stream);
+}
+
+// Chunks per thread: one up to kSmallParts parts (more resident blocks beat
+// sharing the per-part scalar work between two chunks); beyond, two when a
+// row has an even number of chunks and the staging of up to 32 parts fits.
+int merge_kv(int n_parts, int cpr) {
+    if (n_parts <= kSmallParts) return 1;
+    return (cpr % 2 == 0 && n_parts <= 32) ? 2 : 1;
 }
 
 }  // namespace
 
 size_t attn_merge_smem(int n_parts, int cpr) {
-    const int nr_max = kMergeThreads / cpr + 2;
-    return static_cast<size_t>(n_parts) * kMergeThreads * 16 + static_cast<size_t>(n_parts) * nr_max * 4 +
+    const int kv = merge_kv(n_parts, cpr);
+    const int max_k = n_parts <= kSmallParts ? kSmallParts : kMaxParts;
+    const int nr_max = kMergeThreads / (cpr / kv) + 2;
+    return static_cast<size_t>(n_parts) * kv * kMergeThreads * 16 + 2 * static_cast<size_t>(nr_max) * max_k * 4 +
            static_cast<size_t>(nr_max) * 4 + 2 * kMaxParts;
 }
 
@@ -276,6 +454,8 @@ cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     if (c.n_rows > 0) {
+        const int kv = merge_kv(c.n_parts, cpr);
+        const int upr = cpr / kv;
         MergeArgs a{};
         a.parts = static_cast<const char *>(c.parts);
         a.lse = c.lse;
@@ -284,22 +464,26 @@ cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream) {
         a.row_dout = reinterpret_cast<unsigned *>(c.row_dout);
         a.row_dlse = c.row_dlse;
         a.n = c.n_rows;
-        a.total = c.n_rows * cpr;
-        a.cpr = cpr;
+        a.part_bytes = c.n_rows * cpr * 16;
+        a.units = static_cast<uint32_t>(c.n_rows * upr);
+        a.upr = static_cast<uint32_t>(upr);
+        a.upr_shift = (upr & (upr - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(upr)) : -1;
         a.n_parts = c.n_parts;
-        a.nr_max = kMergeThreads / cpr + 2;
+        a.nr_max = kMergeThreads / upr + 2;
         a.base2 = c.base2;
         for (int k = 0; k < c.n_parts; ++k) {
             a.order_a[k] = static_cast<uint8_t>(c.order_a[k]);
             a.order_b[k] = static_cast<uint8_t>(drift ? c.order_b[k] : c.order_a[k]);
+            if (k < kSmallParts) a.off_a[k] = static_cast<int64_t>(c.order_a[k]) * a.part_bytes;
         }
         const size_t smem = attn_merge_smem(c.n_parts, cpr);
-        const unsigned blocks = static_cast<unsigned>((a.total + kMergeThreads - 1) / kMergeThreads);
         cudaError_t e;
         if (c.bf16)
-            e = drift ? launch_merge<true, true>(a, smem, blocks, stream) : launch_merge<true, false>(a, smem, blocks, stream);
+            e = drift ? launch_merge_shape<true, true>(a, kv, smem, stream)
+                      : launch_merge_shape<true, false>(a, kv, smem, stream);
         else
-            e = drift ? launch_merge<false, true>(a, smem, blocks, stream) : launch_merge<false, false>(a, smem, blocks, stream);
+            e = drift ? launch_merge_shape<false, true>(a, kv, smem, stream)
+                      : launch_merge_shape<false, false>(a, kv, smem, stream);
         if (e != cudaSuccess) return e;
         if (drift) {
             const int64_t want = (c.n_rows + kReduceThreads - 1) / kReduceThreads;

@@ -411,9 +411,6 @@ def pin_head_logits_matmul(lib):
         _close(res.logp_rollout[k], log_softmax(ref2[i])[ids[i]], 1e-12, "head logp rollout")
 
 
-ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
-
-
 # ----------------------------------------------------- transform-chain pins
 
 def _dec_tanh(y: Decimal) -> Decimal:
@@ -486,9 +483,6 @@ def pin_transform_per_side(lib):
         _close(res.dlogp[i], float(want), 1e-12, "train plain, rollout tempered")
 
 
-ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
-
-
 # ------------------------------------------------- entropy and backward pins
 
 def pin_entropy_closed_forms(lib):
@@ -542,9 +536,6 @@ def pin_backward_uniform(lib):
         _close(g[j], want, 1e-15, "uniform gradient")
 
 
-ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
-
-
 # ------------------------------------------------------ attention merge pins
 
 def _attention_split(rng, n, d, n_keys, bounds):
@@ -588,9 +579,6 @@ def pin_attn_merge_closed_forms(lib):
     out2, lse2 = oracle.attn_merge(outs, lses / np.float32(math.log(2)), lse_base2=True, lib=lib)
     np.testing.assert_allclose(out2, out, rtol=0, atol=1e-6)
     np.testing.assert_allclose(lse2 * math.log(2), lse, rtol=0, atol=1e-6)
-
-
-ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 
 def pin_attn_merge_masked_parts(lib):

@@ -241,6 +241,7 @@ def _call_merge(parts=FAKE, dtype=B.LPD_F32, lse=FAKE, K=4, n=8, d=128, base2=0,
     (dict(base2=2), B.LPD_ERR_BAD_SIZE),
     (dict(K=0), B.LPD_ERR_UNSUPPORTED),
     (dict(K=B.LPD_ATTN_MAX_PARTS + 1), B.LPD_ERR_UNSUPPORTED),
+    (dict(n=1 << 30, d=64), B.LPD_ERR_UNSUPPORTED),           # 2^34 chunks in one part
     (dict(dtype=7), B.LPD_ERR_BAD_DTYPE),
     (dict(parts=None), B.LPD_ERR_NULL_POINTER),
     (dict(lse=None), B.LPD_ERR_NULL_POINTER),

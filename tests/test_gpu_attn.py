@@ -69,6 +69,11 @@ def _assert_close(w, got_out, got_lse, order=None, rows=None):
     (40, 2, 128, 6, torch.float32, True),       # base-2 lse
     (33, 2, 4, 1, torch.float32, False),        # one part
     (130, 1, 16, 64, torch.float32, False),     # the most parts
+    (11, 2, 16, 20, torch.float32, False),      # looped part count, two chunks per thread
+    (7, 1, 16, 32, torch.bfloat16, False),      # the most parts with two chunks per thread
+    (9, 3, 8, 33, torch.bfloat16, True),        # one chunk per row, looped part count
+    (4000, 16, 128, 8, torch.float32, False),   # more tiles than resident blocks: persistent loop
+    (3000, 8, 64, 12, torch.bfloat16, False),   # the same with a looped part count
 ])
 def test_merge_matches_oracle(T, H, d, K, dtype, base2):
     w = W.attn_partials(T, H, d, K, seed=T + K, device=DEV, dtype=dtype, lse_base2=base2,
@@ -146,6 +151,9 @@ def _summary(rdo, rdl):
     (61, 2, 80, 7, torch.float32),
     (50, 4, 64, 8, torch.bfloat16),
     (130, 1, 16, 64, torch.float32),
+    (11, 2, 16, 20, torch.float32),
+    (300, 2, 8, 3, torch.bfloat16),
+    (4000, 16, 128, 8, torch.float32),
 ])
 def test_order_drift_is_the_difference_of_the_two_merges(T, H, d, K, dtype):
     w = W.attn_partials(T, H, d, K, seed=T * K, device=DEV, dtype=dtype, masked_fill=float("nan"))
