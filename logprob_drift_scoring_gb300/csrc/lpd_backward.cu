@@ -10,9 +10,13 @@
 // Inactive rows get a zero gradient; an active row with an out-of-range id
 // gets NaN (fail closed).
 //
-// Layout: four persistent blocks of 256 threads per SM stride over rows; each
-// row is swept in 8-column groups, four groups per thread in flight.  Rows whose input and
-// output start on 16-byte boundaries use 16-byte loads and stores.
+// Layout: four persistent blocks of 256 threads per SM stride over rows.
+// Rows whose input and output start on 16-byte boundaries are swept in
+// 8-column groups with 16-byte loads and stores, 32 registers of raw input per
+// thread in flight (eight groups of bf16 or four of fp32); the one-hot term is
+// applied only in the group that holds the id.  Inactive and out-of-range rows
+// are a fill.  Other rows take a plain per-element loop with the same
+// arithmetic.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -23,7 +27,7 @@ namespace lpd {
 namespace {
 
 constexpr int kBwdThreads = 256;
-constexpr int kBwdGroups = 4;  // 8-column groups per thread in flight
+constexpr uint32_t kBwdStep = 8 * kBwdThreads;  // columns between a thread's groups
 
 struct BwdArgs {
     const char *x;
@@ -34,111 +38,146 @@ struct BwdArgs {
     const int32_t *ids;
     const uint8_t *mask;
     const float *logp, *grad;
-    int x_bf16, out_bf16;
     int vec;              // rows of both tensors are 16-byte aligned
 };
 
-__device__ __forceinline__ float load_x(const BwdArgs &a, const char *row, int64_t j) {
-    if (a.x_bf16)
+template <bool kXBf16>
+__device__ __forceinline__ float load_x(const char *row, int64_t j) {
+    if constexpr (kXBf16)
         return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(row) + j)) << 16);
-    return __ldg(reinterpret_cast<const float *>(row) + j);
+    else
+        return __ldg(reinterpret_cast<const float *>(row) + j);
 }
 
-__device__ __forceinline__ void store_out(const BwdArgs &a, char *row, int64_t j, float v) {
-    if (a.out_bf16)
+template <bool kOBf16>
+__device__ __forceinline__ void store_out(char *row, int64_t j, float v) {
+    if constexpr (kOBf16)
         reinterpret_cast<__nv_bfloat16 *>(row)[j] = __float2bfloat16_rn(v);
     else
         reinterpret_cast<float *>(row)[j] = v;
 }
 
-// One 8-column group: load (vector or scalar), gradient, store.
-__device__ __forceinline__ void bwd_load8(const BwdArgs &a, const char *xrow, int64_t c0, bool vec, float *x) {
-    if (vec) {
-        if (a.x_bf16) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(xrow + c0 * 2));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+// 8 consecutive columns as raw 16-byte words: one for bf16, two for fp32.
+template <bool kXBf16>
+struct Raw8 {
+    uint4 w[kXBf16 ? 1 : 2];
+};
+
+// Columns are 32-bit: vocab < 2^31, so a column plus a few sweeps stays below 2^32.
+template <bool kXBf16>
+__device__ __forceinline__ void load8(const char *xrow, uint32_t c0, Raw8<kXBf16> &r) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(xrow + static_cast<size_t>(c0) * (kXBf16 ? 2 : 4));
+    r.w[0] = __ldcs(p);
+    if constexpr (!kXBf16) r.w[1] = __ldcs(p + 1);
+}
+
+template <bool kXBf16>
+__device__ __forceinline__ void unpack8(const Raw8<kXBf16> &r, float *x) {
+    if constexpr (kXBf16) {
+        const uint32_t ws[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                x[2 * q] = __uint_as_float(ws[q] << 16);
-                x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
-            }
-        } else {
-            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4));
-            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(xrow + c0 * 4) + 1);
-            x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
-            x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
+        for (int q = 0; q < 4; ++q) {
+            x[2 * q] = __uint_as_float(ws[q] << 16);
+            x[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
         }
     } else {
+        const uint32_t ws[8] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w, r.w[1].x, r.w[1].y, r.w[1].z, r.w[1].w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = c0 + q < a.vocab ? load_x(a, xrow, c0 + q) : 0.f;
+        for (int q = 0; q < 8; ++q) x[q] = __uint_as_float(ws[q]);
     }
 }
 
-__device__ __forceinline__ void bwd_store8(const BwdArgs &a, char *orow, int64_t c0, bool vec, const float *v) {
-    if (vec) {
-        if (a.out_bf16) {
-            uint32_t w[4];
+template <bool kOBf16>
+__device__ __forceinline__ void store8(char *orow, uint32_t c0, const float *v) {
+    if constexpr (kOBf16) {
+        uint32_t w[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
-                w[q] = *reinterpret_cast<const uint32_t *>(&h);
-            }
-            *reinterpret_cast<uint4 *>(orow + c0 * 2) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            reinterpret_cast<float4 *>(orow + c0 * 4)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4 *>(orow + c0 * 4)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+            w[q] = *reinterpret_cast<const uint32_t *>(&h);
         }
+        __stcs(reinterpret_cast<uint4 *>(orow + static_cast<size_t>(c0) * 2), make_uint4(w[0], w[1], w[2], w[3]));
     } else {
+        float4 *p = reinterpret_cast<float4 *>(orow + static_cast<size_t>(c0) * 4);
+        __stcs(p, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(p + 1, make_float4(v[4], v[5], v[6], v[7]));
+    }
+}
+
+// g * (1[j == id] - p_j), p_j = 2^((x_j - lse) log2 e): the one-hot term only
+// where the group holds the id.
+__device__ __forceinline__ void grad8(const float *x, uint32_t c0, uint32_t id, float lse, float g, float *v) {
+    float p[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        p[q] = ex2(__fmul_rn(__fsub_rn(x[q], lse), kLog2e));
+        v[q] = __fmul_rn(g, -p[q]);
+    }
+    const uint32_t j = id - c0;  // wraps for id < c0
+    if (j < 8u) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            if (c0 + q < a.vocab) store_out(a, orow, c0 + q, v[q]);
+            if (q == j) v[q] = __fmul_rn(g, __fsub_rn(1.f, p[q]));
     }
 }
 
-// Persistent blocks: block b takes rows b, b + gridDim.x, ...; within a row
-// thread t handles 8-column groups at 8 t + 2048 k, four groups per iteration
-// with all four loads issued before the arithmetic.  The row prologue (mask,
-// id, lse, g) is paid once per row.
+template <bool kXBf16, bool kOBf16>
 __global__ void __launch_bounds__(kBwdThreads, 4) backward_kernel(const __grid_constant__ BwdArgs a) {
-    constexpr int64_t kStep = 8 * kBwdThreads;  // columns between a thread's groups
+    constexpr int kGroups = kXBf16 ? 8 : 4;  // groups in flight: 32 registers of raw input
+    const int t = threadIdx.x;
     for (int64_t r = blockIdx.x; r < a.n_rows; r += gridDim.x) {
         char *orow = a.out + r * a.out_stride;
         const char *xrow = a.x + r * a.x_stride;
         const bool active = a.mask[r] != 0;
         const int64_t id = active ? a.ids[r] : 0;
-        const bool ok = active && id >= 0 && id < a.vocab;
-        float lse = 0.f, g = 0.f;
-        if (ok) {
-            lse = __fsub_rn(load_x(a, xrow, id), a.logp[r]);
-            g = a.grad[r];
-        }
-        for (int64_t base = 8 * static_cast<int64_t>(threadIdx.x); base < a.vocab; base += kBwdGroups * kStep) {
-            float x[kBwdGroups][8];
-            if (ok) {
+        if (!(active && id >= 0 && id < a.vocab)) {
+            // inactive rows: 0; an active row with an out-of-range id: NaN
+            const float fill = active ? CUDART_NAN_F : 0.f;
+            float v[8];
 #pragma unroll
-                for (int gi = 0; gi < kBwdGroups; ++gi) {
-                    const int64_t c0 = base + gi * kStep;
-                    if (c0 < a.vocab) bwd_load8(a, xrow, c0, a.vec && c0 + 8 <= a.vocab, x[gi]);
+            for (int q = 0; q < 8; ++q) v[q] = fill;
+            for (int64_t c0 = 8 * t; c0 < a.vocab; c0 += static_cast<int64_t>(kBwdStep)) {
+                if (a.vec && c0 + 8 <= a.vocab) {
+                    store8<kOBf16>(orow, c0, v);
+                } else {
+                    for (int q = 0; q < 8 && c0 + q < a.vocab; ++q) store_out<kOBf16>(orow, c0 + q, fill);
                 }
             }
+            continue;
+        }
+        const float lse = __fsub_rn(load_x<kXBf16>(xrow, id), a.logp[r]);
+        const float g = a.grad[r];
+        const uint32_t V = static_cast<uint32_t>(a.vocab), uid = static_cast<uint32_t>(id);
+        if (!a.vec) {
+            for (int64_t j = t; j < a.vocab; j += kBwdThreads) {
+                const float p = ex2(__fmul_rn(__fsub_rn(load_x<kXBf16>(xrow, j), lse), kLog2e));
+                store_out<kOBf16>(orow, j, j == id ? __fmul_rn(g, __fsub_rn(1.f, p)) : __fmul_rn(g, -p));
+            }
+            continue;
+        }
+        for (uint32_t base = 8 * t; base < V; base += kGroups * kBwdStep) {
+            Raw8<kXBf16> raw[kGroups];
 #pragma unroll
-            for (int gi = 0; gi < kBwdGroups; ++gi) {
-                const int64_t c0 = base + gi * kStep;
-                if (c0 >= a.vocab) continue;
-                float v[8];
+            for (int gi = 0; gi < kGroups; ++gi) {
+                const uint32_t c0 = base + gi * kBwdStep;
+                if (c0 + 8 <= V) load8<kXBf16>(xrow, c0, raw[gi]);
+            }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (!active) {
-                        v[q] = 0.f;
-                    } else if (!ok) {
-                        v[q] = CUDART_NAN_F;
-                    } else {
-                        const float p = ex2(__fmul_rn(__fsub_rn(x[gi][q], lse), kLog2e));
-                        const float onehot = (c0 + q == id) ? 1.f : 0.f;
-                        v[q] = __fmul_rn(g, __fsub_rn(onehot, p));
-                    }
+            for (int gi = 0; gi < kGroups; ++gi) {
+                const uint32_t c0 = base + gi * kBwdStep;
+                if (c0 >= V) break;
+                float x[8], v[8];
+                if (c0 + 8 <= V) {
+                    unpack8<kXBf16>(raw[gi], x);
+                    grad8(x, c0, uid, lse, g, v);
+                    store8<kOBf16>(orow, c0, v);
+                } else {
+                    // the row's last, partial group
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) x[q] = c0 + q < V ? load_x<kXBf16>(xrow, c0 + q) : 0.f;
+                    grad8(x, c0, uid, lse, g, v);
+                    for (uint32_t q = 0; q < 8 && c0 + q < V; ++q) store_out<kOBf16>(orow, c0 + q, v[q]);
                 }
-                bwd_store8(a, orow, c0, a.vec && c0 + 8 <= a.vocab, v);
             }
         }
     }
@@ -151,12 +190,11 @@ cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, 
                             const uint8_t *mask, const float *logp, const float *grad, cudaStream_t stream) {
     if (n_rows == 0) return cudaSuccess;
     BwdArgs a{};
+    const bool xb = x_dtype == LPD_BF16, ob = out_dtype == LPD_BF16;
     a.x = static_cast<const char *>(x);
-    a.x_bf16 = x_dtype == LPD_BF16;
-    a.x_stride = x_stride_elems * (a.x_bf16 ? 2 : 4);
+    a.x_stride = x_stride_elems * (xb ? 2 : 4);
     a.out = static_cast<char *>(out);
-    a.out_bf16 = out_dtype == LPD_BF16;
-    a.out_stride = out_stride_elems * (a.out_bf16 ? 2 : 4);
+    a.out_stride = out_stride_elems * (ob ? 2 : 4);
     a.n_rows = n_rows;
     a.vocab = vocab;
     a.ids = ids;
@@ -166,7 +204,13 @@ cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, 
     a.vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (a.x_stride % 16 == 0) &&
             (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (a.out_stride % 16 == 0);
     const int64_t blocks = static_cast<int64_t>(device_sm_count()) * 4;
-    backward_kernel<<<static_cast<unsigned>(n_rows < blocks ? n_rows : blocks), kBwdThreads, 0, stream>>>(a);
+    const unsigned grid = static_cast<unsigned>(n_rows < blocks ? n_rows : blocks);
+    if (xb)
+        ob ? backward_kernel<true, true><<<grid, kBwdThreads, 0, stream>>>(a)
+           : backward_kernel<true, false><<<grid, kBwdThreads, 0, stream>>>(a);
+    else
+        ob ? backward_kernel<false, true><<<grid, kBwdThreads, 0, stream>>>(a)
+           : backward_kernel<false, false><<<grid, kBwdThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
