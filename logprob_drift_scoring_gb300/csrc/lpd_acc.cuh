@@ -74,6 +74,9 @@ __device__ __forceinline__ float scale_diff(float f, float g, float alpha, float
 
 // Merge state b into a.  Symmetric in a and b bit for bit (max and IEEE
 // addition commute), so a butterfly leaves every lane with the same value.
+// Without kEntropy the entropy sums are left alone (they are not carried);
+// the other fields are the same either way.
+template <bool kEntropy = true>
 __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
     const float mt = fmaxf(a.mt, b.mt), mr = fmaxf(a.mr, b.mr);
     const float aa = __fmul_rn(__fsub_rn(a.mt, mt), kLog2e), ab = __fmul_rn(__fsub_rn(b.mt, mt), kLog2e);
@@ -81,8 +84,10 @@ __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
     const float fa = ex2(aa), fb = ex2(ab), ga = ex2(ba), gb = ex2(bb);
     const float xa = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(a.sr, scale_diff(fa, ga, aa, ba)));
     const float xb = __fadd_rn(__fmul_rn(b.dd, fb), __fmul_rn(b.sr, scale_diff(fb, gb, ab, bb)));
-    a.ht = __fadd_rn(ent_rescale(a.ht, a.st, fa, aa), ent_rescale(b.ht, b.st, fb, ab));
-    a.hr = __fadd_rn(ent_rescale(a.hr, a.sr, ga, ba), ent_rescale(b.hr, b.sr, gb, bb));
+    if (kEntropy) {
+        a.ht = __fadd_rn(ent_rescale(a.ht, a.st, fa, aa), ent_rescale(b.ht, b.st, fb, ab));
+        a.hr = __fadd_rn(ent_rescale(a.hr, a.sr, ga, ba), ent_rescale(b.hr, b.sr, gb, bb));
+    }
     a.st = __fadd_rn(__fmul_rn(a.st, fa), __fmul_rn(b.st, fb));
     a.sr = __fadd_rn(__fmul_rn(a.sr, ga), __fmul_rn(b.sr, gb));
     a.dd = __fadd_rn(xa, xb);

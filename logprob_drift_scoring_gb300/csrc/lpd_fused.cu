@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.mr = p.w;
         o.sr = part_b[i * n_n + n];
         o.ht = o.hr = 0.f;
-        merge_acc(acc, o);
+        merge_acc<false>(acc, o);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
         o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
         o.ht = o.hr = 0.f;
-        merge_acc(acc, o);
+        merge_acc<false>(acc, o);
     }
     if (lane != 0) return;
     const int2 rid = rowid[i];

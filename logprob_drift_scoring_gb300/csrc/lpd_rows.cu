@@ -141,59 +141,122 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
 // is copied into registers once per thread (constant indices only, so it never
 // lives in local memory); ops past n are skipped.  Only real columns are
 // transformed; masked tail columns stay -inf.
-struct XformRegs {
+// A side's chain as the consumers read it: one {kind, p, 1/p} entry per op in
+// a shared-memory table (dynamic indexing stays cheap there), walked by a real
+// loop so each op body is emitted once per call site.
+struct XformView {
+    const float4 *ops;  // x: kind (as int bits), y: p, z: 1/p
     int n;
-    int kind[LPD_MAX_TRANSFORM_OPS];
-    float p[LPD_MAX_TRANSFORM_OPS], rcp[LPD_MAX_TRANSFORM_OPS];
 };
 
-__device__ __forceinline__ XformRegs xform_regs(const Xform &c) {
-    XformRegs r;
-    r.n = c.n_ops;
-#pragma unroll
-    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
-        r.kind[k] = c.kind[k];
-        r.p[k] = c.param[k];
-        r.rcp[k] = k < c.n_ops ? __frcp_rn(c.param[k]) : 0.f;
-    }
+__device__ __forceinline__ void xform_table(const Xform &c, float4 *ops) {
+    for (int k = 0; k < c.n_ops; ++k)
+        ops[k] = make_float4(__int_as_float(c.kind[k]), c.param[k], __frcp_rn(c.param[k]), 0.f);
+}
+
+// ---- soft-cap p * tanh(x / p) ---------------------------------------------
+// Near-identical logits on the two sides must get near-identical transformed
+// values, so tanh has to stay at the level of fp32 rounding (the hardware
+// tanh.approx, about 2^-11 relative, does not).  Own tanh, from its series
+// and its exponential form:
+//   z = y^2 < 0.49:  tanh(y) = y (1 + z P(z)), P of degree 6 fitted to
+//                    (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: within 0.69 ulp
+//                    of tanh in float32 Horner evaluation);
+//   otherwise:       tanh(y) = sign(y) (1 - 2 / (1 + 2^(2|y| log2 e))), with
+//                    ex2.approx and rcp.approx (a few ulp where |y| >= 0.7,
+//                    exactly +-1 once the power overflows; NaN stays NaN).
+// Every path takes the same per-element decision on the same rounded z, and
+// the packed path rounds each half like the scalar one, so a column's value
+// does not depend on which load path or lane handled it.
+constexpr float kTanhZMax = 0.49f;
+__host__ __device__ constexpr float tanh_c(int k) {
+    return k == 0 ? -3.333333135e-01f : k == 1 ? 1.333329082e-01f : k == 2 ? -5.396154150e-02f
+         : k == 3 ? 2.181738243e-02f : k == 4 ? -8.638928644e-03f : k == 5 ? 3.035830799e-03f : -6.726949941e-04f;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 
-// Soft-cap p * tanh(x / p) with CUDA's tanhf: near-identical logits on the two
-// sides must get near-identical transformed values, so the tanh error has to
-// stay at the level of fp32 rounding.
-__device__ __forceinline__ float softcap1(float x, float p, float rcp) {
-    return __fmul_rn(p, tanhf(__fmul_rn(x, rcp)));
+__device__ __forceinline__ float tanh_poly(float y, float z) {
+    float p = tanh_c(6);
+#pragma unroll
+    for (int k = 5; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
+    return __fmaf_rn(y, __fmul_rn(z, p), y);
 }
 
-__device__ __forceinline__ float xform1(float x, const XformRegs &c) {
+__device__ __forceinline__ float tanh_exp(float y) {
+    const float e = ex2(__fmul_rn(fabsf(y), 2.8853900817779268f));  // 2^(2|y| log2 e)
+    const float t = __fmaf_rn(-2.f, rcp_approx(__fadd_rn(1.f, e)), 1.f);
+    return copysignf(t, y);
+}
+
+__device__ __forceinline__ float tanh_own(float y) {
+    const float z = __fmul_rn(y, y);
+    return z < kTanhZMax ? tanh_poly(y, z) : tanh_exp(y);
+}
+
+__device__ __forceinline__ float softcap1(float x, float p, float rcp) {
+    return __fmul_rn(p, tanh_own(__fmul_rn(x, rcp)));
+}
+
+// Sixteen values in place.  When no value of the warp needs the exponential
+// form (the usual case: |x| < 0.7 p everywhere) only the packed polynomial runs.
+__device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
+    const f2_t r2 = f2(rcp, rcp), p2 = f2(p, p);
+    f2_t y[8], z[8];
 #pragma unroll
-    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
-        if (k < c.n) {
-            if (c.kind[k] == LPD_OP_SCALE)
-                x = __fmul_rn(x, c.p[k]);
-            else
-                x = softcap1(x, c.p[k], c.rcp[k]);
+    for (int q = 0; q < 8; ++q) {
+        y[q] = mul2(v[q], r2);
+        z[q] = mul2(y[q], y[q]);
+    }
+    const float zmax = max16(z);
+    f2_t t[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        f2_t pp = f2(tanh_c(6), tanh_c(6));
+#pragma unroll
+        for (int k = 5; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
+        t[q] = fma2(y[q], mul2(z[q], pp), y[q]);
+    }
+    if (__any_sync(0xffffffffu, !(zmax < kTanhZMax))) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float lo = f2_lo(z[q]) < kTanhZMax ? f2_lo(t[q]) : tanh_exp(f2_lo(y[q]));
+            const float hi = f2_hi(z[q]) < kTanhZMax ? f2_hi(t[q]) : tanh_exp(f2_hi(y[q]));
+            t[q] = f2(lo, hi);
         }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = mul2(p2, t[q]);
+}
+
+__device__ __forceinline__ float xform1(float x, const XformView &c) {
+#pragma unroll 1
+    for (int k = 0; k < c.n; ++k) {
+        const float4 op = c.ops[k];
+        if (__float_as_int(op.x) == LPD_OP_SCALE)
+            x = __fmul_rn(x, op.y);
+        else
+            x = softcap1(x, op.y, op.z);
     }
     return x;
 }
 
 // The chain over sixteen values: ops outermost, so each op's kind is decided
-// once per chunk (it is the same for every thread); scale runs packed.
-__device__ __forceinline__ void xform16(f2_t *v, const XformRegs &c) {
+// once per chunk (it is the same for every thread); both ops run packed.
+__device__ __forceinline__ void xform16(f2_t *v, const XformView &c) {
+#pragma unroll 1
+    for (int k = 0; k < c.n; ++k) {
+        const float4 op = c.ops[k];
+        if (__float_as_int(op.x) == LPD_OP_SCALE) {
+            const f2_t p2 = f2(op.y, op.y);
 #pragma unroll
-    for (int k = 0; k < LPD_MAX_TRANSFORM_OPS; ++k) {
-        if (k < c.n) {
-            if (c.kind[k] == LPD_OP_SCALE) {
-                const f2_t p2 = f2(c.p[k], c.p[k]);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = mul2(v[q], p2);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    v[q] = f2(softcap1(f2_lo(v[q]), c.p[k], c.rcp[k]), softcap1(f2_hi(v[q]), c.p[k], c.rcp[k]));
-            }
+            for (int q = 0; q < 8; ++q) v[q] = mul2(v[q], p2);
+        } else {
+            softcap16(v, op.y, op.z);
         }
     }
 }
@@ -220,6 +283,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
     constexpr bool kScale = kMode == 3;
     extern __shared__ __align__(1024) char smem[];
     __shared__ int abort_flag;
+    __shared__ float4 xf_ops[kXform ? 2 * LPD_MAX_TRANSFORM_OPS : 1];
     constexpr int kStageT = kTile * DT::kBytes;
     constexpr int kStageR = kTile * DR::kBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -231,6 +295,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        if (kXform) {
+            xform_table(a.xt, xf_ops);
+            xform_table(a.xr, xf_ops + LPD_MAX_TRANSFORM_OPS);
+        }
         if (kTma) {
             for (int s = 0; s < n_stages; ++s) {
                 mbar_init(&full[s], 1);
@@ -286,11 +354,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
     // ---------------------------------------------------------- consumers
     const int t = threadIdx.x;
-    XformRegs cxt, cxr;
-    if (kXform) {
-        cxt = xform_regs(a.xt);
-        cxr = xform_regs(a.xr);
-    }
+    const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0}, cxr{xf_ops + (kXform ? LPD_MAX_TRANSFORM_OPS : 0),
+                                                              kXform ? a.xr.n_ops : 0};
     uint32_t it = 0;
     for (int64_t i = blockIdx.x; i < n_active; i += gridDim.x) {
         const int2 rid = a.rowid[i];
@@ -360,7 +425,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 #pragma unroll
                         for (int p = 0; p < 8; ++p) {
                             const int col0 = slot_col(t, 2 * p);  // the pair is col0, col0 + 1
-                            if (col0 + 1 >= min(nbt, nbr)) {
+                            if (col0 >= nv) {
+                                vt[p] = vr[p] = f2(-INFINITY, -INFINITY);  // wholly past the segment
+                            } else if (col0 + 1 >= min(nbt, nbr)) {
                                 float x[2] = {f2_lo(vt[p]), f2_hi(vt[p])}, y[2] = {f2_lo(vr[p]), f2_hi(vr[p])};
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
@@ -428,7 +495,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
                 o.ht = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.ht, off) : 0.f;
                 o.hr = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.hr, off) : 0.f;
-                merge_acc(acc, o);
+                merge_acc<kEntropy>(acc, o);
             }
             if (lane == 0) {
                 float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;

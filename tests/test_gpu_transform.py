@@ -87,3 +87,46 @@ def test_vocab_padding_policies(policy):
                              base.action_mask.cpu().numpy())
         act = base.action_mask.cpu().numpy() != 0
         assert np.all(ref.logp_train[act] < other.logp_train[act])
+
+
+def test_softcap_tanh_accuracy_per_value():
+    """Rows [a, 0] under soft-cap 30: logp of column 0 is -log(1 + exp(-f(a)))
+    with f(a) = 30 tanh(a / 30), whose sensitivity to f is at most 1.  The
+    kernel's own tanh must keep f within a few ulp: the bar is 8 ulp of
+    max(1, |f|) plus the float32 rounding of logp itself.  The values cover
+    both forms of the tanh (|a| < 21 and beyond), the switch point, tiny and
+    saturating arguments and +-inf."""
+    a = np.concatenate([np.linspace(-200, 200, 4001), 21 + np.linspace(-1e-3, 1e-3, 201),
+                        -21 + np.linspace(-1e-3, 1e-3, 201), [1e-30, -1e-30, 1e-7, 3e3, -3e3, np.inf, -np.inf]])
+    a = a.astype(np.float32)
+    n = a.size
+    x = np.zeros((n, 2), np.float32)
+    x[:, 0] = a
+    t = torch.from_numpy(x).to(DEV)
+    ids = torch.zeros(n, dtype=torch.int32, device=DEV)
+    mask = torch.ones(n, dtype=torch.uint8, device=DEV)
+    ops = [(SOFTCAP, 30.0)]
+    res = B.score(t, t, ids, mask, train_ops=ops, rollout_ops=ops)
+    torch.cuda.synchronize()
+    ref = oracle.score_transformed(x, x, np.zeros(n, np.int32), np.ones(n, np.uint8), ops, ops, 0.8, 1.2)
+    got = res.logp_train.cpu().numpy().astype(np.float64)
+    f = 30.0 * np.tanh(a.astype(np.float64) / 30.0)
+    tol = 8 * 2.0 ** -24 * np.maximum(1.0, np.abs(f)) + 2.0 ** -24 * np.maximum(1.0, np.abs(ref.logp_train))
+    err = np.abs(got - ref.logp_train)
+    assert np.all(err <= tol), (float(a[np.argmax(err - tol)]), float(np.max(err - tol)))
+
+
+def test_softcap_load_paths_agree_bitwise():
+    # logits spread over both forms of the tanh within the same warps, stored
+    # with 16-byte aligned rows (bulk-copy ring) and with an odd row stride
+    # (plain loads): identical bits
+    base = W.synthetic(40, 3 * 4096 + 517, seed=19, device=DEV, row_pad=3, active_prob=1.0, sigma=20.0)
+    ops = [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]
+    aligned = B.score(base.train, base.rollout, base.token_ids, base.action_mask, train_ops=ops, rollout_ops=ops)
+    t2, r2 = base.train.contiguous(), base.rollout.contiguous()
+    assert (t2.stride(0) * 2) % 16 != 0
+    generic = B.score(t2, r2, base.token_ids, base.action_mask, train_ops=ops, rollout_ops=ops)
+    torch.cuda.synchronize()
+    for a, b in ((aligned.logp_train, generic.logp_train), (aligned.logp_rollout, generic.logp_rollout),
+                 (aligned.dlogp, generic.dlogp)):
+        assert torch.equal(a, b)
