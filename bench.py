@@ -208,6 +208,14 @@ class Runner:
         self.chain = None
         self.entropy = None      # [ent_train, ent_rollout] when timing lpd_score_entropy
         self.backward = None     # (grad, out_dlogits) when timing lpd_logprob_backward
+        self.topology = None     # reduction-topology arm when timing lpd_score_sharded_topology
+
+    def use_topology(self, topo: int):
+        B, w, torch = self.B, self.w, self.torch
+        self.topology = topo
+        need = B.lpd_topology_workspace_size(topo, w.n_rows, w.vocab, len(w.v_ranges),
+                                             B._dtype_code(w.train[0]), B._dtype_code(w.rollout[0]))
+        self.ws = torch.empty(need, dtype=torch.uint8, device=w.token_ids.device)
 
     def step(self, ev=None):
         """One pass of the path; with ev = (e0, e1, e2, e3) records events
@@ -235,6 +243,14 @@ class Runner:
                 ev[0].record()
             B.lpd_score_transformed(w.train, w.rollout, self.chain, self.chain, w.token_ids, w.action_mask,
                                     *w.clip, lt, lr, d, self.met, self.ws)
+            if ev:
+                ev[3].record()
+            return
+        if self.sharded and self.topology is not None:
+            if ev:
+                ev[0].record()
+            B.lpd_score_sharded_topology(w.train, w.rollout, w.v_ranges, w.token_ids, w.action_mask, *w.clip,
+                                         self.topology, None, lt, lr, d, self.met, self.ws)
             if ev:
                 ev[3].record()
             return
@@ -552,6 +568,16 @@ def run_ours(args):
     extra_bytes = 0
     if args.transform:
         runner.chain = parse_chain(args.transform)
+    if args.topology:
+        if not runner.sharded:
+            raise SystemExit("--topology needs --config sharded")
+        runner.use_topology(B.TOPOLOGIES[args.topology])
+        if args.topology == "allgather_logits":
+            runner.launches_per_step += 1  # the gather kernel
+        if args.topology == "allgather_logits":
+            # the all-gather reads every row of every shard and writes the full
+            # rows once before the scoring pass reads the active ones
+            extra_bytes = 2 * w.logits_bytes()
     if args.entropy:
         runner.entropy = [torch.empty(w.n_rows, dtype=torch.float32, device=dev) for _ in range(2)]
         bpt += 8
@@ -588,7 +614,7 @@ def run_ours(args):
     ms_step = total_ms / K
     value = world * n_active / (ms_step / 1e3)
 
-    whole = runner.sharded or runner.chain is not None or runner.entropy is not None or runner.backward is not None
+    whole = (runner.sharded or runner.chain is not None or runner.entropy is not None or runner.backward is not None)
     if whole:
         stage2 = sum(e[0].elapsed_time(e[3]) for e in evs) / K
         stage_ms = {"whole_call": stage2}
@@ -622,7 +648,8 @@ def run_ours(args):
             "config": {"workload": (CONFIGS[args.config]["workload"] if not (args.batch or args.seq)
                                     else f"{args.config} reduced B={args.batch} T={args.seq}")
                        + (f" + transform {args.transform}" if args.transform else "")
-                       + (" + entropy" if args.entropy else "") + (" [logprob backward, bf16 out]" if args.backward else ""),
+                       + (" + entropy" if args.entropy else "") + (" [logprob backward, bf16 out]" if args.backward else "")
+                       + (f" [reduce: {args.topology}]" if args.topology else ""),
                        "rows": w.n_rows, "active_tokens": n_active,
                        "vocab": w.vocab, "logits_bytes": w.logits_bytes(), "l2": "inputs exceed L2 (no flush)",
                        "parallelism": f"replicas x{world}", "input_dtypes": _dtypes(w)},
@@ -631,6 +658,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": (1 if runner.backward is not None else runner.launches_per_step) * K,
+
             "clocks": clocks.summary(),
             "impl": "lpd",
         }
@@ -789,6 +817,9 @@ def main(argv=None):
                     help="logit transform chain on both sides, e.g. softcap:30,scale:1.4286")
     ap.add_argument("--entropy", action="store_true", help="time lpd_score_entropy instead of lpd_score")
     ap.add_argument("--backward", action="store_true", help="time lpd_logprob_backward of the train side")
+    ap.add_argument("--topology", choices=["allgather_partials_fixed_merge", "allreduce_partials",
+                                           "allgather_logits"], default=None,
+                    help="sharded config: time lpd_score_sharded_topology with this reduction arm")
     ap.add_argument("--drift", action="store_true",
                     help="attn config: time lpd_attn_merge_order_drift instead of lpd_attn_merge")
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")

@@ -289,6 +289,50 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* ---- reduction topology arms ------------------------------------------------- */
+
+/* The three ways a vocab-parallel logprob can combine its shards
+ * ("[WS2] Framework for ablation experiment", LogProb knobs table, row 4:
+ * reduction topology), run on the same shards so that their drift against
+ * each other is pure arithmetic.  All three compute the same logp exactly; they
+ * differ in rounding only.
+ *   LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE  every shard's (m, s) partial,
+ *       merged pairwise (online softmax) in shard order or `reduce_order`:
+ *       the main result of lpd_score_sharded.
+ *   LPD_TOPO_ALLREDUCE_PARTIALS  a max reduction M = max_k m_k, then a sum
+ *       reduction S = sum_k s_k exp(m_k - M) in fp32, in shard order or
+ *       `reduce_order` (the order an all-reduce adds in); lse = M + log S per
+ *       side, and dlogp is the difference of the two sides' logp.
+ *   LPD_TOPO_ALLGATHER_LOGITS  the shards gathered into full rows in the
+ *       workspace (a copy kernel), then one pass over each row: bitwise what
+ *       lpd_score gives on the concatenated logits.
+ *       `reduce_order` is ignored. */
+#define LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE 0
+#define LPD_TOPO_ALLREDUCE_PARTIALS 1
+#define LPD_TOPO_ALLGATHER_LOGITS 2
+
+/* Workspace bytes for lpd_score_sharded_topology (0 for invalid arguments).
+ * The gather arm also holds both sides' gathered logits: n_rows rows of
+ * vocab elements of each side's dtype, each row padded to 16 bytes. */
+size_t lpd_topology_workspace_size(int32_t topology, int64_t n_rows, int64_t vocab,
+                                   int32_t n_shards, int32_t dtype_train,
+                                   int32_t dtype_rollout);
+
+/* lpd_score_sharded with a chosen reduction topology.  Arguments, outputs,
+ * status and errors are those of lpd_score_sharded without its permuted-merge
+ * outputs; `reduce_order` is a HOST int32[n_shards] permutation (else
+ * LPD_ERR_BAD_SHARDS) or NULL for ascending shard order.  An unknown topology
+ * returns LPD_ERR_UNSUPPORTED.  workspace: lpd_topology_workspace_size(...)
+ * bytes with the shards' dtypes, 256-byte aligned. */
+int lpd_score_sharded_topology(const lpd_shard *train, const lpd_shard *rollout,
+                               int32_t n_shards, int64_t n_rows, int64_t vocab,
+                               const int32_t *token_ids, const uint8_t *action_mask,
+                               double clip_lo, double clip_hi, int32_t topology,
+                               const int32_t *reduce_order, float *out_logp_train,
+                               float *out_logp_rollout, float *out_dlogp,
+                               lpd_metrics *out_metrics, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
 /* Fused LM-head scoring ("[WS2] Framework for ablation experiment", LogProb
  * knobs table, rows 9-10: the head GEMM and its fusion tiling).  The logits
  * x_side[r, v] = sum_k hidden_side[r, k] * W[v, k] are formed tile by tile on

@@ -32,6 +32,8 @@ LPD_STATUS_NONFINITE = 2
 LPD_STATUS_TIMEOUT = 4
 LPD_FLAG_NO_ACTIVE = 1
 LPD_KIND_SCORE, LPD_KIND_SHARDED = 0, 1
+LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE, LPD_TOPO_ALLREDUCE_PARTIALS, LPD_TOPO_ALLGATHER_LOGITS = 0, 1, 2
+TOPOLOGIES = {"allgather_partials_fixed_merge": 0, "allreduce_partials": 1, "allgather_logits": 2}
 
 
 class LpdLogits(ctypes.Structure):
@@ -96,7 +98,8 @@ MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed", "lpd_score_entropy",
-            "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift")
+            "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
+            "lpd_topology_workspace_size", "lpd_score_sharded_topology")
 LPD_NOALLOC_MAX_ROWS = 32768
 LPD_ATTN_MAX_PARTS = 64
 
@@ -145,6 +148,10 @@ def lib() -> ctypes.CDLL:
         L.lpd_logprob_backward.argtypes = [P, I64, I64, P, P, P, P, P, I32, I64, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
+        L.lpd_topology_workspace_size.restype = SZ
+        L.lpd_topology_workspace_size.argtypes = [I32, I64, I64, I32, I32, I32]
+        L.lpd_score_sharded_topology.restype = ctypes.c_int
+        L.lpd_score_sharded_topology.argtypes = [P, P, I32, I64, I64, P, P, D, D, I32, P, P, P, P, P, P, SZ, P]
         L.lpd_attn_merge.restype = ctypes.c_int
         L.lpd_attn_merge.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P]
         L.lpd_attn_merge_order_drift.restype = ctypes.c_int
@@ -301,6 +308,27 @@ def lpd_score_sharded(train_shards, rollout_shards, v_ranges, token_ids, action_
     _check(rc, "lpd_score_sharded")
 
 
+def lpd_topology_workspace_size(topology: int, n_rows: int, vocab: int, n_shards: int, dtype_train: int,
+                                dtype_rollout: int) -> int:
+    return int(lib().lpd_topology_workspace_size(topology, n_rows, vocab, n_shards, dtype_train, dtype_rollout))
+
+
+def lpd_score_sharded_topology(train_shards, rollout_shards, v_ranges, token_ids, action_mask, clip_lo, clip_hi,
+                               topology, reduce_order, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                               workspace, stream=None) -> None:
+    ts, rs = shard_array(train_shards, v_ranges), shard_array(rollout_shards, v_ranges)
+    n_rows = train_shards[0].shape[0]
+    vocab = max(v1 for _, v1 in v_ranges)
+    order = None
+    if reduce_order is not None:
+        order = (ctypes.c_int32 * len(reduce_order))(*[int(k) for k in reduce_order])
+    rc = lib().lpd_score_sharded_topology(ts, rs, len(train_shards), n_rows, vocab, _ptr(token_ids),
+                                          _ptr(action_mask), float(clip_lo), float(clip_hi), int(topology), order,
+                                          _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp),
+                                          _ptr(out_metrics), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "lpd_score_sharded_topology")
+
+
 def lpd_fused_workspace_size(n_rows: int, hidden: int, vocab: int) -> int:
     return int(lib().lpd_fused_workspace_size(n_rows, hidden, vocab))
 
@@ -440,3 +468,21 @@ def score(train, rollout, token_ids, action_mask, clip=(0.8, 1.2), stream=None, 
         lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, action_mask, clip[0], clip[1],
                               *outs, met, ws, stream=stream)
     return ScoreResult(outs[0], outs[1], outs[2], read_metrics(met))
+
+
+def score_sharded_topology(train_shards, rollout_shards, v_ranges, token_ids, action_mask, topology,
+                           reduce_order=None, clip=(0.8, 1.2), stream=None) -> ScoreResult:
+    """lpd_score_sharded_topology with torch-allocated outputs and workspace."""
+    import torch
+
+    dev = token_ids.device
+    n = token_ids.shape[0]
+    vocab = max(v1 for _, v1 in v_ranges)
+    outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
+    nbytes = lpd_topology_workspace_size(topology, n, vocab, len(train_shards), _dtype_code(train_shards[0]),
+                                         _dtype_code(rollout_shards[0]))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    lpd_score_sharded_topology(train_shards, rollout_shards, v_ranges, token_ids, action_mask, clip[0], clip[1],
+                               topology, reduce_order, *outs, met, ws, stream)
+    return ScoreResult(*outs, read_metrics(met))

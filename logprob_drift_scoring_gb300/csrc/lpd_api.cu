@@ -100,6 +100,8 @@ int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *l
 struct RowExtras {
     const Xform *xform = nullptr;       // [2]: train, rollout
     float *ent_t = nullptr, *ent_r = nullptr;
+    int topo = LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE;  // how the finalise reduces the segments
+    const int32_t *order = nullptr;     // host, n_seg entries: segment reduction order
 };
 
 int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, const int32_t *perm, int n_perm,
@@ -156,6 +158,11 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     f.out_perm_lr = plr;
     f.out_ent_t = ex.ent_t;
     f.out_ent_r = ex.ent_r;
+    f.topo = ex.topo;
+    if (ex.order) {
+        f.n_order = n_seg;
+        for (int j = 0; j < n_seg; ++j) f.order[j] = static_cast<int8_t>(ex.order[j]);
+    }
     f.status = &met->status;
     return cuda_status(launch_finalize(f, n_rows, s));
 }
@@ -272,6 +279,67 @@ int attn_merge_impl(const void *out_parts, int32_t parts_dtype, const float *lse
     c.row_dlse = row_dlse;
     c.drift = drift;
     return cuda_status(launch_attn_merge(c, static_cast<cudaStream_t>(stream)));
+}
+
+// Shared validation of the sharded entry points: sizes, pointers, both
+// sides' shard maps (the same split on each side), and the per-shard segments
+// in global vocab order with whether every row can use the bulk-copy ring.
+int prepare_shards(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards, int64_t n_rows,
+                   int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask, const lpd_metrics *met,
+                   Segment *segs, bool *tma) {
+    int rc = check_rows_vocab(n_rows, vocab);
+    if (rc) return rc;
+    if (n_shards < 1 || n_shards > kMaxSegments) return LPD_ERR_UNSUPPORTED;
+    if (!met || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
+    int ot[kMaxSegments], orr[kMaxSegments];
+    if ((rc = check_shards(train, n_shards, n_rows, vocab, ot))) return rc;
+    if ((rc = check_shards(rollout, n_shards, n_rows, vocab, orr))) return rc;
+    // both sides must use the same split: shard j (in vocab order) covers the
+    // same range on each side
+    for (int j = 0; j < n_shards; ++j)
+        if (train[ot[j]].v_start != rollout[orr[j]].v_start || train[ot[j]].v_end != rollout[orr[j]].v_end)
+            return LPD_ERR_BAD_SHARDS;
+    *tma = true;
+    for (int j = 0; j < n_shards; ++j) {
+        const lpd_shard &a = train[ot[j]], &b = rollout[orr[j]];
+        segs[j].t = static_cast<const char *>(a.ptr);
+        segs[j].r = static_cast<const char *>(b.ptr);
+        segs[j].t_stride = a.row_stride * elt_bytes(a.dtype);
+        segs[j].r_stride = b.row_stride * elt_bytes(b.dtype);
+        segs[j].v_start = a.v_start;
+        segs[j].len = a.v_end - a.v_start;
+        *tma = *tma && rows_aligned(a.ptr, a.row_stride, a.dtype) && rows_aligned(b.ptr, b.row_stride, b.dtype);
+    }
+    return LPD_OK;
+}
+
+// A host permutation of 0..n-1 (or NULL).
+int check_order(const int32_t *order, int n) {
+    if (!order) return LPD_OK;
+    bool seen[kMaxSegments] = {false};
+    for (int j = 0; j < n; ++j) {
+        const int k = order[j];
+        if (k < 0 || k >= n || seen[k]) return LPD_ERR_BAD_SHARDS;
+        seen[k] = true;
+    }
+    return LPD_OK;
+}
+
+// Workspace of the all-gather arm: the single-segment scoring regions, then
+// each side's gathered logits with rows padded to 16 bytes.
+struct GatherLayout {
+    size_t logits_t, logits_r, total;
+    int64_t pitch_t, pitch_r;  // bytes
+};
+
+GatherLayout gather_layout(int64_t n_rows, int64_t vocab, int32_t dt, int32_t dr) {
+    GatherLayout g;
+    g.pitch_t = (vocab * elt_bytes(dt) + 15) / 16 * 16;
+    g.pitch_r = (vocab * elt_bytes(dr) + 15) / 16 * 16;
+    g.logits_t = align256(ws_layout(n_rows, 1).total);
+    g.logits_r = align256(g.logits_t + static_cast<size_t>(n_rows) * g.pitch_t);
+    g.total = align256(g.logits_r + static_cast<size_t>(n_rows) * g.pitch_r);
+    return g;
 }
 
 }  // namespace
@@ -488,42 +556,15 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                       double clip_hi, const int32_t *merge_perm, float *out_logp_train, float *out_logp_rollout,
                       float *out_dlogp, float *out_perm_logp_train, float *out_perm_logp_rollout,
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes, void *stream) {
-    int rc = check_rows_vocab(n_rows, vocab);
+    Segment segs[kMaxSegments];
+    bool tma = true;
+    int rc = prepare_shards(train, rollout, n_shards, n_rows, vocab, token_ids, action_mask, out_metrics, segs, &tma);
     if (rc) return rc;
-    if (n_shards < 1 || n_shards > kMaxSegments) return LPD_ERR_UNSUPPORTED;
-    if (!out_metrics || ((!token_ids || !action_mask) && n_rows > 0)) return LPD_ERR_NULL_POINTER;
-    int ot[kMaxSegments], orr[kMaxSegments];
-    if ((rc = check_shards(train, n_shards, n_rows, vocab, ot))) return rc;
-    if ((rc = check_shards(rollout, n_shards, n_rows, vocab, orr))) return rc;
-    // both sides must use the same split: shard j (in vocab order) covers the
-    // same range on each side
-    for (int j = 0; j < n_shards; ++j)
-        if (train[ot[j]].v_start != rollout[orr[j]].v_start || train[ot[j]].v_end != rollout[orr[j]].v_end)
-            return LPD_ERR_BAD_SHARDS;
     if ((rc = check_clip(clip_lo, clip_hi))) return rc;
-    if (merge_perm) {
-        bool seen[kMaxSegments] = {false};
-        for (int j = 0; j < n_shards; ++j) {
-            const int k = merge_perm[j];
-            if (k < 0 || k >= n_shards || seen[k]) return LPD_ERR_BAD_SHARDS;
-            seen[k] = true;
-        }
-    }
+    if ((rc = check_order(merge_perm, n_shards))) return rc;
     if ((rc = check_workspace(workspace, workspace_bytes,
                               lpd_workspace_size(LPD_KIND_SHARDED, n_rows, vocab, n_shards))))
         return rc;
-    Segment segs[kMaxSegments];
-    bool tma = true;
-    for (int j = 0; j < n_shards; ++j) {
-        const lpd_shard &a = train[ot[j]], &b = rollout[orr[j]];
-        segs[j].t = static_cast<const char *>(a.ptr);
-        segs[j].r = static_cast<const char *>(b.ptr);
-        segs[j].t_stride = a.row_stride * elt_bytes(a.dtype);
-        segs[j].r_stride = b.row_stride * elt_bytes(b.dtype);
-        segs[j].v_start = a.v_start;
-        segs[j].len = a.v_end - a.v_start;
-        tma = tma && rows_aligned(a.ptr, a.row_stride, a.dtype) && rows_aligned(b.ptr, b.row_stride, b.dtype);
-    }
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Ws w = carve(workspace, n_rows, n_shards);
     if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
@@ -539,6 +580,80 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
     if ((rc = run_rows(segs, n_shards, train[0].dtype, rollout[0].dtype, tma, merge_perm, merge_perm ? n_shards : 0,
                        n_rows, vocab, out_logp_train, out_logp_rollout, out_dlogp, out_perm_logp_train,
                        out_perm_logp_rollout, out_metrics, w, s)))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
+size_t lpd_topology_workspace_size(int32_t topology, int64_t n_rows, int64_t vocab, int32_t n_shards,
+                                   int32_t dtype_train, int32_t dtype_rollout) {
+    if (n_rows < 0 || n_rows > kMaxRows || vocab <= 0 || vocab > kMaxVocab || n_shards < 1 ||
+        n_shards > kMaxSegments || !valid_dtype(dtype_train) || !valid_dtype(dtype_rollout))
+        return 0;
+    switch (topology) {
+        case LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE:
+        case LPD_TOPO_ALLREDUCE_PARTIALS:
+            return ws_layout(n_rows, n_shards).total;
+        case LPD_TOPO_ALLGATHER_LOGITS: {
+            const GatherLayout g = gather_layout(n_rows, vocab, dtype_train, dtype_rollout);
+            return g.total;
+        }
+        default:
+            return 0;
+    }
+}
+
+int lpd_score_sharded_topology(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards, int64_t n_rows,
+                               int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask, double clip_lo,
+                               double clip_hi, int32_t topology, const int32_t *reduce_order, float *out_logp_train,
+                               float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    if (topology != LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE && topology != LPD_TOPO_ALLREDUCE_PARTIALS &&
+        topology != LPD_TOPO_ALLGATHER_LOGITS)
+        return LPD_ERR_UNSUPPORTED;
+    Segment segs[kMaxSegments];
+    bool tma = true;
+    int rc = prepare_shards(train, rollout, n_shards, n_rows, vocab, token_ids, action_mask, out_metrics, segs, &tma);
+    if (rc) return rc;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if (topology != LPD_TOPO_ALLGATHER_LOGITS && (rc = check_order(reduce_order, n_shards))) return rc;
+    const int32_t dt = train[0].dtype, dr = rollout[0].dtype;
+    if ((rc = check_workspace(workspace, workspace_bytes,
+                              lpd_topology_workspace_size(topology, n_rows, vocab, n_shards, dt, dr))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (topology == LPD_TOPO_ALLGATHER_LOGITS) {
+        // the all-gather: every shard's columns of every row into one full row per side
+        const GatherLayout g = gather_layout(n_rows, vocab, dt, dr);
+        char *base = static_cast<char *>(workspace);
+        char *gt = base + g.logits_t, *gr = base + g.logits_r;
+        if ((rc = cuda_status(launch_gather_shards(segs, n_shards, n_rows, gt, g.pitch_t, elt_bytes(dt), gr,
+                                                   g.pitch_r, elt_bytes(dr), s))))
+            return rc;
+        Segment whole{};
+        whole.t = gt;
+        whole.r = gr;
+        whole.t_stride = g.pitch_t;
+        whole.r_stride = g.pitch_r;
+        whole.v_start = 0;
+        whole.len = vocab;
+        const Ws w = carve(workspace, n_rows, 1);
+        if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp,
+                             out_metrics, w, s)))
+            return rc;
+        if ((rc = run_rows(&whole, 1, dt, dr, true, nullptr, 0, n_rows, vocab, out_logp_train, out_logp_rollout,
+                           out_dlogp, nullptr, nullptr, out_metrics, w, s)))
+            return rc;
+        return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+    }
+    const Ws w = carve(workspace, n_rows, n_shards);
+    if ((rc = run_select(n_rows, token_ids, action_mask, out_logp_train, out_logp_rollout, out_dlogp, out_metrics,
+                         w, s)))
+        return rc;
+    RowExtras ex;
+    ex.topo = topology;
+    ex.order = reduce_order;
+    if ((rc = run_rows(segs, n_shards, dt, dr, tma, nullptr, 0, n_rows, vocab, out_logp_train, out_logp_rollout,
+                       out_dlogp, nullptr, nullptr, out_metrics, w, s, ex)))
         return rc;
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
 }

@@ -103,6 +103,9 @@ struct FinArgs {
     int n_seg;
     int n_perm;                    // 0: no merge-order diagnostic
     int8_t perm[kMaxSegments];
+    int topo;                      // LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE or LPD_TOPO_ALLREDUCE_PARTIALS
+    int n_order;                   // 0: segments reduced in index order
+    int8_t order[kMaxSegments];
     int64_t vocab;
     const WsHeader *hdr;
     const int2 *rowid;
@@ -173,6 +176,11 @@ struct AttnMergeCall {
 };
 size_t attn_merge_smem(int n_parts, int cpr);
 cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream);
+
+// The all-gather of the allgather_logits arm: shard pieces of every row into
+// full rows (pitches in bytes).
+cudaError_t launch_gather_shards(const Segment *segs, int n_seg, int64_t n_rows, void *dst_t, int64_t pitch_t,
+                                 int elt_t, void *dst_r, int64_t pitch_r, int elt_r, cudaStream_t stream);
 
 int device_sm_count();
 

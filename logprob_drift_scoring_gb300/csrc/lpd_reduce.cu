@@ -163,7 +163,6 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
     } else {
         const float2 xs = a.pick[i];
         Acc seg[kMaxSegments];
-        Acc row = acc_init();
         for (int k = 0; k < a.n_seg; ++k) {
             Acc sk = acc_init();
             const float4 *pw = a.part + (i * a.n_seg + k) * kConsumerWarps * 2;
@@ -181,19 +180,42 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
                 merge_acc(sk, o);
             }
             seg[k] = sk;
-            merge_acc(row, sk);  // global vocab-shard order
         }
-        const double lse_t = lse_train(row), lse_r = lse_rollout(row);
         const double xt = xs.x, xr = xs.y;
-        const double st = row.st, sr = row.sr, dd = row.dd;
-        const double l_ratio = fabs(dd) < 0.5 * st ? log1p(-dd / st) : log(sr / st);
-        d = ((xt - xr) - (static_cast<double>(row.mt) - static_cast<double>(row.mr))) + l_ratio;
+        Acc row = acc_init();
+        double lse_t, lse_r;
+        if (a.topo == LPD_TOPO_ALLREDUCE_PARTIALS) {
+            // a max reduction, then a sum reduction of s_k 2^((m_k - M) log2 e)
+            // in reduction order, each side on its own
+            float mt = -FLT_MAX, mr = -FLT_MAX;
+            for (int k = 0; k < a.n_seg; ++k) {
+                mt = fmaxf(mt, seg[k].mt);
+                mr = fmaxf(mr, seg[k].mr);
+            }
+            float st = 0.f, sr = 0.f;
+            for (int j = 0; j < a.n_seg; ++j) {
+                const Acc &sk = seg[a.n_order ? a.order[j] : j];
+                st = __fadd_rn(st, __fmul_rn(sk.st, ex2(__fmul_rn(__fsub_rn(sk.mt, mt), kLog2e))));
+                sr = __fadd_rn(sr, __fmul_rn(sk.sr, ex2(__fmul_rn(__fsub_rn(sk.mr, mr), kLog2e))));
+            }
+            lse_t = static_cast<double>(mt) + log(static_cast<double>(st));
+            lse_r = static_cast<double>(mr) + log(static_cast<double>(sr));
+            d = (xt - lse_t) - (xr - lse_r);
+        } else {
+            // online pairwise merge in global vocab-shard order (or the given one)
+            for (int j = 0; j < a.n_seg; ++j) merge_acc(row, seg[a.n_order ? a.order[j] : j]);
+            lse_t = lse_train(row);
+            lse_r = lse_rollout(row);
+            const double st = row.st, sr = row.sr, dd = row.dd;
+            const double l_ratio = fabs(dd) < 0.5 * st ? log1p(-dd / st) : log(sr / st);
+            d = ((xt - xr) - (static_cast<double>(row.mt) - static_cast<double>(row.mr))) + l_ratio;
+        }
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
         if (a.out_lr) a.out_lr[r] = static_cast<float>(xr - lse_r);
         // entropy H = ln(s) - ln(2) * h / s of each side's softmax
-        if (a.out_ent_t) a.out_ent_t[r] = static_cast<float>(log(st) - 0.6931471805599453 * (double)row.ht / st);
-        if (a.out_ent_r) a.out_ent_r[r] = static_cast<float>(log(sr) - 0.6931471805599453 * (double)row.hr / sr);
+        if (a.out_ent_t) a.out_ent_t[r] = static_cast<float>(log((double)row.st) - 0.6931471805599453 * (double)row.ht / row.st);
+        if (a.out_ent_r) a.out_ent_r[r] = static_cast<float>(log((double)row.sr) - 0.6931471805599453 * (double)row.hr / row.sr);
         if (a.n_perm) {
             Acc pr = acc_init();
             for (int j = 0; j < a.n_perm; ++j) merge_acc(pr, seg[a.perm[j]]);

@@ -280,3 +280,50 @@ def test_attn_merge_binding_checks_shapes():
         B.attn_merge(parts, torch.zeros((3, 2)))
     with pytest.raises(ValueError):
         B.attn_merge(parts, torch.zeros((2, 3)), order=[0])
+
+
+def _call_topology(shards_t, shards_r, topology=B.LPD_TOPO_ALLREDUCE_PARTIALS, order=None, n_rows=8, vocab=100,
+                   ws=WS_OK, ws_bytes=1 << 24):
+    lib = B.lib()
+    n = len(shards_t)
+    ts = (B.LpdShard * n)(*shards_t)
+    rs = (B.LpdShard * n)(*shards_r)
+    o = (ctypes.c_int32 * len(order))(*order) if order is not None else None
+    return lib.lpd_score_sharded_topology(ts, rs, n, n_rows, vocab, FAKE, FAKE, 0.8, 1.2, topology, o, None, None,
+                                          None, FAKE, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("topology", [0, 1, 2])
+@pytest.mark.parametrize("t,r,order,code", [
+    ([_sh(0, 50), _sh(51, 100)], [_sh(0, 50), _sh(51, 100)], None, B.LPD_ERR_BAD_SHARDS),        # gap
+    ([_sh(0, 50), _sh(50, 100)], [_sh(0, 40), _sh(40, 100)], None, B.LPD_ERR_BAD_SHARDS),        # sides differ
+    ([_sh(0, 50), _sh(50, 100, B.LPD_F32)], [_sh(0, 50), _sh(50, 100)], None, B.LPD_ERR_BAD_DTYPE),
+    ([_sh(0, 50), _sh(50, 100, stride=49)], [_sh(0, 50), _sh(50, 100)], None, B.LPD_ERR_BAD_STRIDE),
+])
+def test_topology_rejects_bad_maps(t, r, order, code, topology):
+    assert _call_topology(t, r, topology, order) == code
+
+
+def test_topology_rejects_bad_order_topology_and_workspace():
+    t = [_sh(0, 50), _sh(50, 100)]
+    for topo in (0, 1):
+        assert _call_topology(t, t, topo, [1, 1]) == B.LPD_ERR_BAD_SHARDS
+        assert _call_topology(t, t, topo, [0, 2]) == B.LPD_ERR_BAD_SHARDS
+    assert _call_topology(t, t, 3) == B.LPD_ERR_UNSUPPORTED
+    assert _call_topology(t, t, -1) == B.LPD_ERR_UNSUPPORTED
+    need = B.lpd_topology_workspace_size(2, 8, 100, 2, B.LPD_BF16, B.LPD_BF16)
+    assert _call_topology(t, t, 2, ws_bytes=need - 1) == B.LPD_ERR_WORKSPACE
+    assert _call_topology(t, t, 1, ws=WS_OK + 8) == B.LPD_ERR_ALIGNMENT     # not 256-byte aligned
+
+
+def test_topology_workspace_size():
+    part = B.lpd_topology_workspace_size(B.LPD_TOPO_ALLREDUCE_PARTIALS, 100, 1000, 4, B.LPD_BF16, B.LPD_BF16)
+    assert part == B.lpd_workspace_size(B.LPD_KIND_SHARDED, 100, 1000, 4)
+    assert B.lpd_topology_workspace_size(0, 100, 1000, 4, B.LPD_BF16, B.LPD_F32) == part
+    gather = B.lpd_topology_workspace_size(B.LPD_TOPO_ALLGATHER_LOGITS, 100, 1000, 4, B.LPD_BF16, B.LPD_F32)
+    # both sides' rows (padded to 16 bytes) on top of a single-segment scoring workspace
+    assert gather >= B.lpd_workspace_size(B.LPD_KIND_SCORE, 100) + 100 * 2000 + 100 * 4000
+    assert gather % 256 == 0
+    assert B.lpd_topology_workspace_size(5, 100, 1000, 4, B.LPD_BF16, B.LPD_BF16) == 0
+    assert B.lpd_topology_workspace_size(0, 100, 1000, 0, B.LPD_BF16, B.LPD_BF16) == 0
+    assert B.lpd_topology_workspace_size(0, 100, 1000, 4, 9, B.LPD_BF16) == 0
