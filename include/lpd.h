@@ -222,6 +222,19 @@ int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi,
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* Stage 3 over caller-given per-token values: the metrics record of the
+ * rows with action_mask != 0, with d = dlogp[r] (float32, widened exactly) in
+ * place of the scorer's own values.  For data-parallel runs: the ranks'
+ * out_dlogp and masks gathered in rank order give the exact metrics of the
+ * union, percentiles included ("WS2 Cross-Config Logprob Drift Contract",
+ * "Diagnostics": the same metrics globally and per rank).  A non-finite value
+ * on an active row sets LPD_STATUS_NONFINITE.
+ * dlogp        device float32[n_rows]; action_mask device uint8[n_rows].
+ * workspace    lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0) bytes. */
+int lpd_drift_metrics_from_dlogp(int64_t n_rows, const float *dlogp, const uint8_t *action_mask,
+                                 double clip_lo, double clip_hi, lpd_metrics *out_metrics,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* lpd_score with a logit transform chain per side (each may be NULL for the
  * identity).  The chains are part of what is compared: different chains on the
  * two sides show up as drift, which the pages treat as a correctness bug rather

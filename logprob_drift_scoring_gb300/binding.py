@@ -99,7 +99,7 @@ EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed", "lpd_score_entropy",
             "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
-            "lpd_topology_workspace_size", "lpd_score_sharded_topology")
+            "lpd_topology_workspace_size", "lpd_score_sharded_topology", "lpd_drift_metrics_from_dlogp")
 LPD_NOALLOC_MAX_ROWS = 32768
 LPD_ATTN_MAX_PARTS = 64
 
@@ -148,6 +148,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_logprob_backward.argtypes = [P, I64, I64, P, P, P, P, P, I32, I64, P]
         L.lpd_score_noalloc.restype = ctypes.c_int
         L.lpd_score_noalloc.argtypes = [P, P, I64, I64, P, P, D, D, P, P, P, P, P]
+        L.lpd_drift_metrics_from_dlogp.restype = ctypes.c_int
+        L.lpd_drift_metrics_from_dlogp.argtypes = [I64, P, P, D, D, P, P, SZ, P]
         L.lpd_topology_workspace_size.restype = SZ
         L.lpd_topology_workspace_size.argtypes = [I32, I64, I64, I32, I32, I32]
         L.lpd_score_sharded_topology.restype = ctypes.c_int
@@ -306,6 +308,24 @@ def lpd_score_sharded(train_shards, rollout_shards, v_ranges, token_ids, action_
                                  _ptr(out_dlogp), _ptr(out_perm_logp_train), _ptr(out_perm_logp_rollout),
                                  _ptr(out_metrics), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "lpd_score_sharded")
+
+
+def lpd_drift_metrics_from_dlogp(dlogp, action_mask, clip_lo, clip_hi, out_metrics, workspace, stream=None) -> None:
+    rc = lib().lpd_drift_metrics_from_dlogp(dlogp.shape[0], _ptr(dlogp), _ptr(action_mask), float(clip_lo),
+                                            float(clip_hi), _ptr(out_metrics), _ptr(workspace), workspace.numel(),
+                                            _stream(stream))
+    _check(rc, "lpd_drift_metrics_from_dlogp")
+
+
+def drift_metrics_from_dlogp(dlogp, action_mask, clip=(0.8, 1.2), stream=None) -> dict:
+    """The metrics record of given per-token dlogp (float32, device) over the active rows."""
+    import torch
+
+    dev = dlogp.device
+    met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
+    ws = torch.empty(lpd_workspace_size(LPD_KIND_SCORE, dlogp.shape[0]), dtype=torch.uint8, device=dev)
+    lpd_drift_metrics_from_dlogp(dlogp, action_mask, clip[0], clip[1], met, ws, stream)
+    return read_metrics(met)
 
 
 def lpd_topology_workspace_size(topology: int, n_rows: int, vocab: int, n_shards: int, dtype_train: int,

@@ -446,6 +446,26 @@ int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi, lpd_metric
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, static_cast<cudaStream_t>(stream));
 }
 
+int lpd_drift_metrics_from_dlogp(int64_t n_rows, const float *dlogp, const uint8_t *action_mask, double clip_lo,
+                                 double clip_hi, lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    if (n_rows < 0) return LPD_ERR_BAD_SIZE;
+    if (n_rows > kMaxRows) return LPD_ERR_UNSUPPORTED;
+    if (!out_metrics || (n_rows > 0 && (!dlogp || !action_mask))) return LPD_ERR_NULL_POINTER;
+    int rc = check_clip(clip_lo, clip_hi);
+    if (rc) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Ws w = carve(workspace, n_rows, 1);
+    if ((rc = cuda_status(launch_select_active(n_rows, action_mask, nullptr, nullptr, nullptr, nullptr, out_metrics,
+                                               w.hdr, w.rowid, s))))
+        return rc;
+    if ((rc = cuda_status(launch_dlogp_rows(n_rows, dlogp, w.hdr, w.rowid, w.dval, w.keys, &out_metrics->status, s))))
+        return rc;
+    return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
+}
+
 int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab,
               const int32_t *token_ids, const uint8_t *action_mask, double clip_lo, double clip_hi,
               float *out_logp_train, float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,

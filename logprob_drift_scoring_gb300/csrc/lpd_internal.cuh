@@ -150,6 +150,8 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
 constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3;
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
+cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader *hdr, const int2 *rowid,
+                              double *dval, uint32_t *keys, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
                            const int2 *rowid, const double *dval, const uint32_t *keys,
                            BlockPartial *bp, lpd_metrics *metrics, cudaStream_t stream);

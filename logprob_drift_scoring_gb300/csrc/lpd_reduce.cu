@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, con
 #pragma unroll
         for (int q = 0; q < 16; ++q) mk[q] = (r0 + q < n_rows) ? mask[r0 + q] : 0;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) idv[q] = mk[q] ? ids[r0 + q] : 0;
+        for (int q = 0; q < 16; ++q) idv[q] = (mk[q] && ids) ? ids[r0 + q] : 0;
         uint32_t bits = 0;
         int cnt = 0;
 #pragma unroll
@@ -97,6 +97,20 @@ __global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, con
         hdr->n_active = base;
         metrics->status = 0u;
     }
+}
+
+// Metrics over caller-given per-row dlogp (the union of several ranks' rows):
+// active row i takes d = dlogp[row] widened to fp64 and the key |d| in fp32;
+// a non-finite value on an active row sets LPD_STATUS_NONFINITE.
+__global__ void __launch_bounds__(kFinThreads) dlogp_rows_kernel(const float *__restrict__ dlogp,
+                                                                 const WsHeader *hdr, const int2 *rowid,
+                                                                 double *dval, uint32_t *keys, uint32_t *status) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    if (i >= hdr->n_active) return;
+    const float d = dlogp[rowid[i].x];
+    dval[i] = static_cast<double>(d);
+    keys[i] = __float_as_uint(fabsf(d));
+    if (!isfinite(d)) atomicOr(status, static_cast<uint32_t>(LPD_STATUS_NONFINITE));
 }
 
 // ---------------------------------------------------------------- stage 2b
@@ -385,6 +399,15 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lr, float *out_d, lpd_metrics *metrics, WsHeader *hdr,
                                  int2 *rowid, cudaStream_t stream) {
     select_active_kernel<<<1, 1024, 0, stream>>>(n_rows, mask, ids, out_lt, out_lr, out_d, metrics, hdr, rowid);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader *hdr, const int2 *rowid,
+                              double *dval, uint32_t *keys, uint32_t *status, cudaStream_t stream) {
+    const int64_t blocks = (n_rows + kFinThreads - 1) / kFinThreads;
+    if (blocks == 0) return cudaSuccess;
+    dlogp_rows_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(dlogp, hdr, rowid, dval, keys,
+                                                                                 status);
     return cudaGetLastError();
 }
 

@@ -11,8 +11,11 @@ per-rank metric records (torch.distributed, any backend) and combines them:
   records: the active-token count, the token-weighted means (ratio0_mean,
   clipfrac0, approx_kl0, mean_abs_dlogp) and the worst token (largest
   max_abs_dlogp, lowest global row on ties).  Percentiles of the union are not
-  a function of per-rank percentiles and are left to a pass over the gathered
-  dlogp values.
+  a function of per-rank percentiles;
+* gather_rank_rows / global_drift_metrics: every rank's per-token dlogp and
+  mask (5 bytes a row) gathered in rank order, and the full metrics record of
+  the union computed from them on the GPU (lpd_drift_metrics_from_dlogp),
+  percentiles included.
 
 The merge visits ranks in rank order, so its result does not depend on the
 collective's algorithm or arrival order ("[WS2] Framework for ablation
@@ -62,3 +65,34 @@ def merge_rank_metrics(per_rank: list[dict], row_offsets: list[int] | None = Non
         for k in MEAN_KEYS:
             out[k] /= total
     return out
+
+
+def gather_rank_rows(local_dlogp, local_mask, group=None):
+    """Every rank's per-row dlogp (float32) and mask (uint8), concatenated in
+    rank order.  Ranks may hold different numbers of rows.  The tensors travel
+    on their own device (NCCL for CUDA tensors, gloo for CPU ones)."""
+    import torch
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    sizes = [None] * world
+    dist.all_gather_object(sizes, int(local_dlogp.shape[0]), group=group)
+    width = max(max(sizes), 1)
+    d = torch.zeros(width, dtype=torch.float32, device=local_dlogp.device)
+    m = torch.zeros(width, dtype=torch.uint8, device=local_mask.device)
+    d[:local_dlogp.shape[0]] = local_dlogp
+    m[:local_mask.shape[0]] = local_mask
+    ds = [torch.empty_like(d) for _ in range(world)]
+    ms = [torch.empty_like(m) for _ in range(world)]
+    dist.all_gather(ds, d, group=group)
+    dist.all_gather(ms, m, group=group)
+    return (torch.cat([x[:n] for x, n in zip(ds, sizes)]), torch.cat([x[:n] for x, n in zip(ms, sizes)]))
+
+
+def global_drift_metrics(local_dlogp, local_mask, clip=(0.8, 1.2), group=None) -> dict:
+    """The metrics record of all ranks' rows together, identical on every rank
+    (CUDA tensors: the union is scored by the library on this rank's GPU)."""
+    from logprob_drift_scoring_gb300 import binding as B
+
+    d, m = gather_rank_rows(local_dlogp, local_mask, group)
+    return B.drift_metrics_from_dlogp(d, m, clip)

@@ -327,3 +327,20 @@ def test_topology_workspace_size():
     assert B.lpd_topology_workspace_size(5, 100, 1000, 4, B.LPD_BF16, B.LPD_BF16) == 0
     assert B.lpd_topology_workspace_size(0, 100, 1000, 0, B.LPD_BF16, B.LPD_BF16) == 0
     assert B.lpd_topology_workspace_size(0, 100, 1000, 4, 9, B.LPD_BF16) == 0
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(n=-1), B.LPD_ERR_BAD_SIZE),
+    (dict(d=None), B.LPD_ERR_NULL_POINTER),
+    (dict(m=None), B.LPD_ERR_NULL_POINTER),
+    (dict(met=None), B.LPD_ERR_NULL_POINTER),
+    (dict(lo=1.3), B.LPD_ERR_BAD_CLIP),
+    (dict(ws=None), B.LPD_ERR_WORKSPACE),
+    (dict(ws_bytes=16), B.LPD_ERR_WORKSPACE),
+])
+def test_metrics_from_dlogp_validation(kwargs, code):
+    a = dict(n=8, d=FAKE, m=FAKE, lo=0.8, hi=1.2, met=FAKE, ws=WS_OK, ws_bytes=1 << 20)
+    a.update(kwargs)
+    rc = B.lib().lpd_drift_metrics_from_dlogp(a["n"], a["d"], a["m"], a["lo"], a["hi"], a["met"], a["ws"],
+                                              a["ws_bytes"], None)
+    assert rc == code

@@ -40,7 +40,9 @@ def _worker(rank, world, port, out_dir):
 
     import bench
     import oracle
-    from logprob_drift_scoring_gb300.ranks import gather_rank_metrics, merge_rank_metrics
+    import torch
+
+    from logprob_drift_scoring_gb300.ranks import gather_rank_metrics, gather_rank_rows, merge_rank_metrics
 
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
     t, r, ids, mask = _data()
@@ -50,8 +52,16 @@ def _worker(rank, world, port, out_dir):
     per_rank = gather_rank_metrics(local.metrics, rank_meta={"row_offset": lo})
     merged = merge_rank_metrics(per_rank, [p["row_offset"] for p in per_rank])
     tmax = bench.barrier_max(float(rank + 1), world)
+    # rows of every rank in rank order: first the real split's dlogp, then
+    # deliberately uneven sizes (rank k holds 3 + 4k rows)
+    d_all, m_all = gather_rank_rows(torch.from_numpy(local.dlogp.astype(np.float32)),
+                                    torch.from_numpy(mask[rows].copy()))
+    n_k = 3 + 4 * rank
+    u_d, u_m = gather_rank_rows(torch.arange(n_k, dtype=torch.float32) + 100 * rank,
+                                (torch.arange(n_k) % 2).to(torch.uint8))
     with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
-        json.dump({"per_rank": per_rank, "merged": merged, "tmax": tmax}, f)
+        json.dump({"per_rank": per_rank, "merged": merged, "tmax": tmax, "d_all": d_all.tolist(),
+                   "m_all": m_all.tolist(), "u_d": u_d.tolist(), "u_m": u_m.tolist()}, f)
     dist.destroy_process_group()
 
 
@@ -77,3 +87,15 @@ def test_two_rank_metrics_merge_and_timing(tmp_path):
     counts = [p["n_active"] for p in res[0]["per_rank"]]
     halves = np.array_split(np.arange(len(mask)), world)
     assert counts == [int(mask[h].sum()) for h in halves]
+    # gathered rows: the union in rank order, identical on every rank; its
+    # metrics (percentiles included) are those of the whole batch
+    whole_d = oracle.score(t, r, ids, mask).dlogp.astype(np.float32)
+    for k in range(world):
+        assert np.array_equal(np.array(res[k]["d_all"], np.float32), whole_d)
+        assert np.array_equal(np.array(res[k]["m_all"], np.uint8), mask)
+        assert res[k]["u_d"] == [0.0, 1.0, 2.0] + [100.0 + i for i in range(7)]
+        assert res[k]["u_m"] == [0, 1, 0] + [i % 2 for i in range(7)]
+    union = oracle.metrics(np.array(res[0]["d_all"], np.float64), mask, 0.8, 1.2)
+    ref = oracle.metrics(whole_d.astype(np.float64), mask, 0.8, 1.2)
+    for key in ("p95_abs_dlogp", "p99_abs_dlogp", "max_abs_dlogp", "approx_kl0", "n_active", "argmax_row"):
+        assert union[key] == ref[key], key
