@@ -32,8 +32,7 @@ constexpr int kMergeThreads = 128;
 constexpr int kMaxParts = LPD_ATTN_MAX_PARTS;
 constexpr int kSmallParts = 8;  // part counts up to this run fully unrolled
 
-// A thread's unit is kV adjacent 16-byte chunks of one row (kV = 2 when a row
-// has an even number of chunks and the block's staging fits, else 1).
+// A thread's unit is kV adjacent 16-byte chunks of one row (merge_kv picks kV).
 struct MergeArgs {
     const char *parts;       // [K][n][d] as 16-byte chunks
     const float *lse;        // [K][n]
@@ -85,9 +84,11 @@ __device__ __forceinline__ void unpack(const uint4 w, float *v) {
 }
 
 // Staged shared memory of one block: chunk_s[(k * kV + v) * 128 + t] holds
-// chunk v of thread t's unit in part k (consecutive threads, consecutive 16
-// bytes: no bank conflicts); lse_s[rr * kMaxK + k] the lse of the block's
-// row rr in part k; ord_s both orders (the looped kMaxK = 64 form only).
+// chunk v of thread t's unit in slot k (consecutive threads, consecutive 16
+// bytes: no bank conflicts).  Slot k is part k, except in the plain merge of
+// up to kSmallParts parts, where it is the k-th part visited.  lse_s[rr *
+// kMaxK + k] is the lse of the block's row rr in part k; ord_s holds both
+// orders (the looped kMaxK = 64 form only).
 template <int kV, int kMaxK>
 struct Staged {
     const uint4 *chunk_s;
