@@ -95,6 +95,49 @@ __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
     a.mr = mr;
 }
 
+// Every lane's state reduced over the warp, the result held by all lanes: the
+// two maxima first (exact), then each lane's sums rescaled once to them (dd
+// with the same exact-difference correction as merge_acc) and added in a
+// fixed xor butterfly.  IEEE addition commutes, so partner lanes form the same
+// sums and every lane ends with the same bits.
+template <bool kEntropy>
+__device__ __forceinline__ Acc warp_reduce_acc(Acc a) {
+    float mt = a.mt, mr = a.mr;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+        mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
+    }
+    const float at = __fmul_rn(__fsub_rn(a.mt, mt), kLog2e), ar = __fmul_rn(__fsub_rn(a.mr, mr), kLog2e);
+    const float ft = ex2(at), fr = ex2(ar);
+    float dd = __fadd_rn(__fmul_rn(a.dd, ft), __fmul_rn(a.sr, scale_diff(ft, fr, at, ar)));
+    float st = __fmul_rn(a.st, ft), sr = __fmul_rn(a.sr, fr);
+    float ht = 0.f, hr = 0.f;
+    if (kEntropy) {
+        ht = ent_rescale(a.ht, a.st, ft, at);
+        hr = ent_rescale(a.hr, a.sr, fr, ar);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        st = __fadd_rn(st, __shfl_xor_sync(0xffffffffu, st, off));
+        sr = __fadd_rn(sr, __shfl_xor_sync(0xffffffffu, sr, off));
+        dd = __fadd_rn(dd, __shfl_xor_sync(0xffffffffu, dd, off));
+        if (kEntropy) {
+            ht = __fadd_rn(ht, __shfl_xor_sync(0xffffffffu, ht, off));
+            hr = __fadd_rn(hr, __shfl_xor_sync(0xffffffffu, hr, off));
+        }
+    }
+    Acc r;
+    r.mt = mt;
+    r.mr = mr;
+    r.st = st;
+    r.sr = sr;
+    r.dd = dd;
+    r.ht = ht;
+    r.hr = hr;
+    return r;
+}
+
 // ---- packed fp32 pairs ---------------------------------------------------------
 // Two fp32 values in one 64-bit register pair, operated on with the f32x2
 // instructions.  Each half is rounded exactly like the scalar .rn operation, so

@@ -10,13 +10,14 @@
 // Layout of the work.  One persistent CTA per SM takes active rows i =
 // blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams each row
 // through a ring of shared-memory stages with 1-D bulk copies (TMA,
-// cp.async.bulk, completion on an mbarrier); every stage holds the same 4096
+// cp.async.bulk, completion on an mbarrier); every stage holds the same 8192
 // columns of both sides.  16 consumer warps read the stage, and thread t owns
-// columns [4t, 4t+4) and [2048+4t, 2048+4t+4) of every tile.  Each thread keeps
-// an online (max, sum exp) pair per side in fp32 plus the sum of the two
-// sides' term differences; at the end of a segment each warp merges its 32
-// states in a fixed butterfly and writes one state to the workspace.  The finalise kernel merges the 16 warp pairs, the
-// segments and does the fp64 row arithmetic.
+// columns [2048 g + 4t, 2048 g + 4t + 4), g = 0..3, of every tile.  Each thread
+// keeps an online (max, sum exp) pair per side in fp32 plus the sum of the two
+// sides' term differences; at the end of a segment each warp reduces its 32
+// states (both maxima first, then the rescaled sums in a fixed xor butterfly)
+// and writes one state to the workspace.  The finalise kernel merges the 16
+// warp states and the segments and does the fp64 row arithmetic.
 //
 // Batch invariance ("Attention Debug Matrix", section "Metrics": the
 // batch-composition control must be bitwise zero): the value that reaches a
@@ -483,20 +484,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
                 accumulate16<kEntropy>(vt, vr, acc2);
             }
-            Acc acc = acc2_fold(acc2);
-            // fixed butterfly over the warp
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                Acc o;
-                o.mt = __shfl_xor_sync(0xffffffffu, acc.mt, off);
-                o.st = __shfl_xor_sync(0xffffffffu, acc.st, off);
-                o.dd = __shfl_xor_sync(0xffffffffu, acc.dd, off);
-                o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
-                o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
-                o.ht = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.ht, off) : 0.f;
-                o.hr = kEntropy ? __shfl_xor_sync(0xffffffffu, acc.hr, off) : 0.f;
-                merge_acc<kEntropy>(acc, o);
-            }
+            const Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2));
             if (lane == 0) {
                 float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;
                 dst[0] = make_float4(acc.mt, acc.st, acc.dd, acc.mr);
