@@ -159,20 +159,20 @@ __device__ __forceinline__ void xform_table(const Xform &c, float4 *ops) {
 // Near-identical logits on the two sides must get near-identical transformed
 // values, so tanh has to stay at the level of fp32 rounding (the hardware
 // tanh.approx, about 2^-11 relative, does not).  Own tanh, from its series
-// and its exponential form:
-//   z = y^2 < 0.49:  tanh(y) = y (1 + z P(z)), P of degree 6 fitted to
-//                    (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: within 0.69 ulp
-//                    of tanh in float32 Horner evaluation);
-//   otherwise:       tanh(y) = sign(y) (1 - 2 / (1 + 2^(2|y| log2 e))), with
-//                    ex2.approx and rcp.approx (a few ulp where |y| >= 0.7,
-//                    exactly +-1 once the power overflows; NaN stays NaN).
+// and its exponential form, with y = x / p and z = y^2:
+//   z < 0.36:   p tanh(y) = x (1 + z P(z)), P of degree 5 fitted to
+//               (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: tanh within 0.70 ulp
+//               in float32 Horner evaluation); p y is written as x itself;
+//   otherwise:  p tanh(y) = p sign(y) (1 - 2 / (1 + 2^(2|y| log2 e))), with
+//               ex2.approx and rcp.approx (a few ulp where |y| >= 0.6,
+//               exactly +-p once the power overflows; NaN stays NaN).
 // Every path takes the same per-element decision on the same rounded z, and
 // the packed path rounds each half like the scalar one, so a column's value
 // does not depend on which load path or lane handled it.
-constexpr float kTanhZMax = 0.49f;
+constexpr float kTanhZMax = 0.36f;
 __host__ __device__ constexpr float tanh_c(int k) {
-    return k == 0 ? -3.333333135e-01f : k == 1 ? 1.333329082e-01f : k == 2 ? -5.396154150e-02f
-         : k == 3 ? 2.181738243e-02f : k == 4 ? -8.638928644e-03f : k == 5 ? 3.035830799e-03f : -6.726949941e-04f;
+    return k == 0 ? -3.333333135e-01f : k == 1 ? 1.333319992e-01f : k == 2 ? -5.394675583e-02f
+         : k == 3 ? 2.170414850e-02f : k == 4 ? -8.193124086e-03f : 2.163204830e-03f;
 }
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -181,11 +181,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
-__device__ __forceinline__ float tanh_poly(float y, float z) {
-    float p = tanh_c(6);
+// z P(z)
+__device__ __forceinline__ float tanh_q(float z) {
+    float p = tanh_c(5);
 #pragma unroll
-    for (int k = 5; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
-    return __fmaf_rn(y, __fmul_rn(z, p), y);
+    for (int k = 4; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
+    return __fmul_rn(z, p);
 }
 
 __device__ __forceinline__ float tanh_exp(float y) {
@@ -194,19 +195,15 @@ __device__ __forceinline__ float tanh_exp(float y) {
     return copysignf(t, y);
 }
 
-__device__ __forceinline__ float tanh_own(float y) {
-    const float z = __fmul_rn(y, y);
-    return z < kTanhZMax ? tanh_poly(y, z) : tanh_exp(y);
-}
-
 __device__ __forceinline__ float softcap1(float x, float p, float rcp) {
-    return __fmul_rn(p, tanh_own(__fmul_rn(x, rcp)));
+    const float y = __fmul_rn(x, rcp), z = __fmul_rn(y, y);
+    return z < kTanhZMax ? __fmaf_rn(x, tanh_q(z), x) : __fmul_rn(p, tanh_exp(y));
 }
 
 // Sixteen values in place.  When no value of the warp needs the exponential
-// form (the usual case: |x| < 0.7 p everywhere) only the packed polynomial runs.
+// form (the usual case: |x| < 0.6 p everywhere) only the packed polynomial runs.
 __device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
-    const f2_t r2 = f2(rcp, rcp), p2 = f2(p, p);
+    const f2_t r2 = f2(rcp, rcp);
     f2_t y[8], z[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -214,24 +211,24 @@ __device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
         z[q] = mul2(y[q], y[q]);
     }
     const float zmax = max16(z);
-    f2_t t[8];
+    f2_t o[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        f2_t pp = f2(tanh_c(6), tanh_c(6));
+        f2_t pp = f2(tanh_c(5), tanh_c(5));
 #pragma unroll
-        for (int k = 5; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
-        t[q] = fma2(y[q], mul2(z[q], pp), y[q]);
+        for (int k = 4; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
+        o[q] = fma2(v[q], mul2(z[q], pp), v[q]);
     }
     if (__any_sync(0xffffffffu, !(zmax < kTanhZMax))) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float lo = f2_lo(z[q]) < kTanhZMax ? f2_lo(t[q]) : tanh_exp(f2_lo(y[q]));
-            const float hi = f2_hi(z[q]) < kTanhZMax ? f2_hi(t[q]) : tanh_exp(f2_hi(y[q]));
-            t[q] = f2(lo, hi);
+            const float lo = f2_lo(z[q]) < kTanhZMax ? f2_lo(o[q]) : __fmul_rn(p, tanh_exp(f2_lo(y[q])));
+            const float hi = f2_hi(z[q]) < kTanhZMax ? f2_hi(o[q]) : __fmul_rn(p, tanh_exp(f2_hi(y[q])));
+            o[q] = f2(lo, hi);
         }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = mul2(p2, t[q]);
+    for (int q = 0; q < 8; ++q) v[q] = o[q];
 }
 
 __device__ __forceinline__ float xform1(float x, const XformView &c) {

@@ -1,8 +1,8 @@
 """Derives the polynomial of the row kernel's soft-cap tanh (lpd_rows.cu).
 
-tanh(y) = y * (1 + z * P(z)), z = y^2, for z < 0.49 (|y| < 0.7).  P has
-degree 6 and is a weighted least-squares fit of (tanh(y)/y - 1) / z on 4000
-Chebyshev nodes of z in [0, 0.49].  The weight z * y / tanh(y) makes the
+tanh(y) = y * (1 + z * P(z)), z = y^2, for z < 0.36 (|y| < 0.6).  P has
+degree 5 and is a weighted least-squares fit of (tanh(y)/y - 1) / z on 4000
+Chebyshev nodes of z in [0, 0.36].  The weight z * y / tanh(y) makes the
 residual the relative error of tanh, and 30 reweighting passes push the fit
 towards equal-ripple.  The coefficients are rounded to float32, and the script
 reports the worst error of a float32 Horner evaluation (one rounding per fused
@@ -14,7 +14,7 @@ import numpy as np
 from mpmath import mp, mpf, tanh as mtanh
 
 mp.dps = 40
-Y_MAX, DEGREE, NODES = 0.7, 6, 4000
+Y_MAX, DEGREE, NODES = 0.6, 5, 4000
 
 
 def target(z):
@@ -59,5 +59,5 @@ def worst_ulp(cf, samples=20001):
 
 if __name__ == "__main__":
     cf = fit()
-    print("coefficients c0..c6:", ", ".join(f"{float(v):.9e}f" for v in cf))
+    print("coefficients c0..c%d:" % DEGREE, ", ".join(f"{float(v):.9e}f" for v in cf))
     print("worst float32 error: %.3f ulp" % worst_ulp(cf))

@@ -94,10 +94,10 @@ def test_softcap_tanh_accuracy_per_value():
     with f(a) = 30 tanh(a / 30), whose sensitivity to f is at most 1.  The
     kernel's own tanh must keep f within a few ulp: the bar is 8 ulp of
     max(1, |f|) plus the float32 rounding of logp itself.  The values cover
-    both forms of the tanh (|a| < 21 and beyond), the switch point, tiny and
+    both forms of the tanh (|a| < 18 and beyond), the switch point, tiny and
     saturating arguments and +-inf."""
-    a = np.concatenate([np.linspace(-200, 200, 4001), 21 + np.linspace(-1e-3, 1e-3, 201),
-                        -21 + np.linspace(-1e-3, 1e-3, 201), [1e-30, -1e-30, 1e-7, 3e3, -3e3, np.inf, -np.inf]])
+    a = np.concatenate([np.linspace(-200, 200, 4001), 18 + np.linspace(-1e-3, 1e-3, 201),
+                        -18 + np.linspace(-1e-3, 1e-3, 201), [1e-30, -1e-30, 1e-7, 3e3, -3e3, np.inf, -np.inf]])
     a = a.astype(np.float32)
     n = a.size
     x = np.zeros((n, 2), np.float32)
