@@ -44,6 +44,14 @@
  * log-sum-exp or selected logit on an active row.  When status != 0 the
  * metric values are unspecified; per-token outputs of the offending rows are
  * NaN or non-finite.
+ *
+ * Bounded waits: no kernel waits without a limit.  The streaming row pass
+ * gives up a pipeline wait after 2 s (4 s in the fused LM-head kernel), sets
+ * LPD_STATUS_TIMEOUT, lets its in-flight copies land and returns; the context
+ * stays usable.  The environment variable LPD_WAIT_LIMIT_NS (read at each
+ * call, decimal nanoseconds) shortens the row pass's pipeline limit, so that
+ * this path can be exercised on purpose; the final wait for copies in flight
+ * always keeps the full limit.
  */
 #ifndef LPD_H
 #define LPD_H

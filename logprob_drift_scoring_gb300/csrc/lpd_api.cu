@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "lpd_internal.cuh"
@@ -95,6 +96,16 @@ int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *l
     return cuda_status(launch_select_active(n_rows, mask, ids, lt, lr, d, met, w.hdr, w.rowid, s));
 }
 
+// LPD_WAIT_LIMIT_NS shortens the row pass's bounded pipeline waits (tests use
+// it to take the timeout path); unset, empty or invalid: 0, the default limit.
+unsigned long long wait_limit_override() {
+    const char *v = std::getenv("LPD_WAIT_LIMIT_NS");
+    if (!v || !*v) return 0;
+    char *end = nullptr;
+    const unsigned long long x = std::strtoull(v, &end, 10);
+    return (end && *end == '\0') ? x : 0;
+}
+
 // Stage 2: the streaming row pass, then the per-row finalise.
 // Optional extras of the row pass: a transform chain per side, or entropy outputs.
 struct RowExtras {
@@ -138,6 +149,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     a.part = w.part;
     a.pick = w.pick;
     a.status = &met->status;
+    a.wait_limit_ns = wait_limit_override();
     int rc = cuda_status(launch_rows(a, dt, dr, tma, mode, s));
     if (rc) return rc;
     FinArgs f{};

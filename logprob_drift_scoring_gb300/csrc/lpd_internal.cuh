@@ -97,6 +97,7 @@ struct RowArgs {
     float4 *part;
     float2 *pick;
     uint32_t *status;
+    unsigned long long wait_limit_ns;  // pipeline waits give up after this long (0: the default)
 };
 
 struct FinArgs {
