@@ -76,11 +76,14 @@ __device__ __forceinline__ float scale_diff(float f, float g, float alpha, float
 // addition commute), so a butterfly leaves every lane with the same value.
 // Without kEntropy the entropy sums are left alone (they are not carried);
 // the other fields are the same either way.
+// lt, lr: each side's factor from a logit difference to a base-2 exponent
+// (log2 e, or s log2 e when the maxima are kept in unscaled units of a side
+// whose logits are scaled by s).
 template <bool kEntropy = true>
-__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
+__device__ __forceinline__ void merge_acc(Acc &a, const Acc &b, float lt = kLog2e, float lr = kLog2e) {
     const float mt = fmaxf(a.mt, b.mt), mr = fmaxf(a.mr, b.mr);
-    const float aa = __fmul_rn(__fsub_rn(a.mt, mt), kLog2e), ab = __fmul_rn(__fsub_rn(b.mt, mt), kLog2e);
-    const float ba = __fmul_rn(__fsub_rn(a.mr, mr), kLog2e), bb = __fmul_rn(__fsub_rn(b.mr, mr), kLog2e);
+    const float aa = __fmul_rn(__fsub_rn(a.mt, mt), lt), ab = __fmul_rn(__fsub_rn(b.mt, mt), lt);
+    const float ba = __fmul_rn(__fsub_rn(a.mr, mr), lr), bb = __fmul_rn(__fsub_rn(b.mr, mr), lr);
     const float fa = ex2(aa), fb = ex2(ab), ga = ex2(ba), gb = ex2(bb);
     const float xa = __fadd_rn(__fmul_rn(a.dd, fa), __fmul_rn(a.sr, scale_diff(fa, ga, aa, ba)));
     const float xb = __fadd_rn(__fmul_rn(b.dd, fb), __fmul_rn(b.sr, scale_diff(fb, gb, ab, bb)));
@@ -101,14 +104,14 @@ __device__ __forceinline__ void merge_acc(Acc &a, const Acc &b) {
 // fixed xor butterfly.  IEEE addition commutes, so partner lanes form the same
 // sums and every lane ends with the same bits.
 template <bool kEntropy>
-__device__ __forceinline__ Acc warp_reduce_acc(Acc a) {
+__device__ __forceinline__ Acc warp_reduce_acc(Acc a, float lt = kLog2e, float lr = kLog2e) {
     float mt = a.mt, mr = a.mr;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
         mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
     }
-    const float at = __fmul_rn(__fsub_rn(a.mt, mt), kLog2e), ar = __fmul_rn(__fsub_rn(a.mr, mr), kLog2e);
+    const float at = __fmul_rn(__fsub_rn(a.mt, mt), lt), ar = __fmul_rn(__fsub_rn(a.mr, mr), lr);
     const float ft = ex2(at), fr = ex2(ar);
     float dd = __fadd_rn(__fmul_rn(a.dd, ft), __fmul_rn(a.sr, scale_diff(ft, fr, at, ar)));
     float st = __fmul_rn(a.st, ft), sr = __fmul_rn(a.sr, fr);
@@ -233,12 +236,13 @@ __device__ __forceinline__ f2_t tree8(const f2_t *e) {
 // fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
 // -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
 template <bool kEntropy = false>
-__device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a) {
+__device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a, float lt = kLog2e,
+                                             float lr = kLog2e) {
     const float cmt = max16(vt), cmr = max16(vr);
     if (cmt > a.mt || cmr > a.mr) {
         const float nmt = fmaxf(a.mt, cmt), nmr = fmaxf(a.mr, cmr);
-        const float at = __fmul_rn(__fsub_rn(a.mt, nmt), kLog2e);
-        const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), kLog2e);
+        const float at = __fmul_rn(__fsub_rn(a.mt, nmt), lt);
+        const float ar = __fmul_rn(__fsub_rn(a.mr, nmr), lr);
         const float ft = ex2(at), fr = ex2(ar);
         const float corr = scale_diff(ft, fr, at, ar);
         if (kEntropy) {
@@ -251,11 +255,11 @@ __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc
         a.mt = nmt;
         a.mr = nmr;
     }
-    const f2_t mt2 = f2(a.mt, a.mt), mr2 = f2(a.mr, a.mr), l2 = f2(kLog2e, kLog2e);
+    const f2_t mt2 = f2(a.mt, a.mt), mr2 = f2(a.mr, a.mr), lt2 = f2(lt, lt), lr2 = f2(lr, lr);
     f2_t et[8], er[8], dq[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        const f2_t xt = mul2(sub2(vt[p], mt2), l2), xr = mul2(sub2(vr[p], mr2), l2);
+        const f2_t xt = mul2(sub2(vt[p], mt2), lt2), xr = mul2(sub2(vr[p], mr2), lr2);
         et[p] = ex2_2(xt);
         er[p] = ex2_2(xr);
         dq[p] = sub2(et[p], er[p]);

@@ -121,6 +121,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     if (n_rows == 0) return LPD_OK;
     RowArgs a{};
     int mode = kRowPlain;
+    float scale_t = 1.f, scale_r = 1.f, lg_t = kLog2e, lg_r = kLog2e;
     if (ex.xform) {
         a.xt = ex.xform[0];
         a.xr = ex.xform[1];
@@ -134,8 +135,13 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
                 prod[side] *= ex.xform[side].param[k];
             }
         if (scales_only) {
-            a.st = prod[0];
-            a.sr = prod[1];
+            // the product of scales rides in each side's exponent factor
+            a.lt = static_cast<float>(static_cast<double>(prod[0]) * 1.4426950408889634);
+            a.lr = static_cast<float>(static_cast<double>(prod[1]) * 1.4426950408889634);
+            scale_t = prod[0];
+            scale_r = prod[1];
+            lg_t = a.lt;
+            lg_r = a.lr;
             mode = kRowScale;
         }
     } else if (ex.ent_t || ex.ent_r) {
@@ -171,6 +177,10 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     f.out_ent_t = ex.ent_t;
     f.out_ent_r = ex.ent_r;
     f.topo = ex.topo;
+    f.scale_t = scale_t;
+    f.scale_r = scale_r;
+    f.lg_t = lg_t;
+    f.lg_r = lg_r;
     if (ex.order) {
         f.n_order = n_seg;
         for (int j = 0; j < n_seg; ++j) f.order[j] = static_cast<int8_t>(ex.order[j]);

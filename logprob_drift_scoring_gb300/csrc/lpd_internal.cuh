@@ -88,7 +88,7 @@ struct Xform {
 
 struct RowArgs {
     Xform xt, xr;    // train and rollout chains (transform mode only)
-    float st, sr;    // product of each side's scales (scale-only chains)
+    float lt, lr;    // scale-only chains: each side's s log2 e (maxima kept unscaled)
     Segment seg[kMaxSegments];
     int n_seg;
     int64_t vocab;
@@ -105,6 +105,8 @@ struct FinArgs {
     int n_perm;                    // 0: no merge-order diagnostic
     int8_t perm[kMaxSegments];
     int topo;                      // LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE or LPD_TOPO_ALLREDUCE_PARTIALS
+    float scale_t, scale_r;        // scale-only chains: each side's product of scales (else 1)
+    float lg_t, lg_r;              // the row pass's factor to base-2 exponents (s log2 e, else log2 e)
     int n_order;                   // 0: segments reduced in index order
     int8_t order[kMaxSegments];
     int64_t vocab;

@@ -19,11 +19,13 @@
 namespace lpd {
 namespace {
 
-__device__ __forceinline__ double lse_train(const Acc &a) {
-    return static_cast<double>(a.mt) + log(static_cast<double>(a.st));
+// lse of a side whose maxima are kept in unscaled units (scale 1 otherwise):
+// the product of two floats is exact in fp64.
+__device__ __forceinline__ double lse_train(const Acc &a, float scale) {
+    return static_cast<double>(scale) * static_cast<double>(a.mt) + log(static_cast<double>(a.st));
 }
-__device__ __forceinline__ double lse_rollout(const Acc &a) {
-    return static_cast<double>(a.mr) + log(static_cast<double>(a.sr));
+__device__ __forceinline__ double lse_rollout(const Acc &a, float scale) {
+    return static_cast<double>(scale) * static_cast<double>(a.mr) + log(static_cast<double>(a.sr));
 }
 
 // ---------------------------------------------------------------- stage 1
@@ -191,11 +193,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
                 o.sr = p1.x;
                 o.ht = p1.y;
                 o.hr = p1.z;
-                merge_acc(sk, o);
+                merge_acc(sk, o, a.lg_t, a.lg_r);
             }
             seg[k] = sk;
         }
-        const double xt = xs.x, xr = xs.y;
+        // the selected logits, scaled by a scale-only chain (exact in fp64)
+        const double xt = static_cast<double>(a.scale_t) * xs.x, xr = static_cast<double>(a.scale_r) * xs.y;
         Acc row = acc_init();
         double lse_t, lse_r;
         if (a.topo == LPD_TOPO_ALLREDUCE_PARTIALS) {
@@ -209,20 +212,22 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
             float st = 0.f, sr = 0.f;
             for (int j = 0; j < a.n_seg; ++j) {
                 const Acc &sk = seg[a.n_order ? a.order[j] : j];
-                st = __fadd_rn(st, __fmul_rn(sk.st, ex2(__fmul_rn(__fsub_rn(sk.mt, mt), kLog2e))));
-                sr = __fadd_rn(sr, __fmul_rn(sk.sr, ex2(__fmul_rn(__fsub_rn(sk.mr, mr), kLog2e))));
+                st = __fadd_rn(st, __fmul_rn(sk.st, ex2(__fmul_rn(__fsub_rn(sk.mt, mt), a.lg_t))));
+                sr = __fadd_rn(sr, __fmul_rn(sk.sr, ex2(__fmul_rn(__fsub_rn(sk.mr, mr), a.lg_r))));
             }
-            lse_t = static_cast<double>(mt) + log(static_cast<double>(st));
-            lse_r = static_cast<double>(mr) + log(static_cast<double>(sr));
+            lse_t = static_cast<double>(a.scale_t) * static_cast<double>(mt) + log(static_cast<double>(st));
+            lse_r = static_cast<double>(a.scale_r) * static_cast<double>(mr) + log(static_cast<double>(sr));
             d = (xt - lse_t) - (xr - lse_r);
         } else {
             // online pairwise merge in global vocab-shard order (or the given one)
-            for (int j = 0; j < a.n_seg; ++j) merge_acc(row, seg[a.n_order ? a.order[j] : j]);
-            lse_t = lse_train(row);
-            lse_r = lse_rollout(row);
+            for (int j = 0; j < a.n_seg; ++j) merge_acc(row, seg[a.n_order ? a.order[j] : j], a.lg_t, a.lg_r);
+            lse_t = lse_train(row, a.scale_t);
+            lse_r = lse_rollout(row, a.scale_r);
             const double st = row.st, sr = row.sr, dd = row.dd;
             const double l_ratio = fabs(dd) < 0.5 * st ? log1p(-dd / st) : log(sr / st);
-            d = ((xt - xr) - (static_cast<double>(row.mt) - static_cast<double>(row.mr))) + l_ratio;
+            d = ((xt - xr) - (static_cast<double>(a.scale_t) * static_cast<double>(row.mt) -
+                              static_cast<double>(a.scale_r) * static_cast<double>(row.mr))) +
+                l_ratio;
         }
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (a.out_lt) a.out_lt[r] = static_cast<float>(xt - lse_t);
@@ -232,9 +237,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
         if (a.out_ent_r) a.out_ent_r[r] = static_cast<float>(log((double)row.sr) - 0.6931471805599453 * (double)row.hr / row.sr);
         if (a.n_perm) {
             Acc pr = acc_init();
-            for (int j = 0; j < a.n_perm; ++j) merge_acc(pr, seg[a.perm[j]]);
-            if (a.out_perm_lt) a.out_perm_lt[r] = static_cast<float>(xt - lse_train(pr));
-            if (a.out_perm_lr) a.out_perm_lr[r] = static_cast<float>(xr - lse_rollout(pr));
+            for (int j = 0; j < a.n_perm; ++j) merge_acc(pr, seg[a.perm[j]], a.lg_t, a.lg_r);
+            if (a.out_perm_lt) a.out_perm_lt[r] = static_cast<float>(xt - lse_train(pr, a.scale_t));
+            if (a.out_perm_lr) a.out_perm_lr[r] = static_cast<float>(xr - lse_rollout(pr, a.scale_r));
         }
     }
     if (a.out_d) a.out_d[r] = static_cast<float>(d);

@@ -298,8 +298,8 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
 }
 
 // kMode: 0 plain, 1 with a general transform chain, 2 with the entropy sums,
-// 3 with a scale-only chain (one packed multiply by the side's product of
-// scales, so no tanh code sits in this instantiation).
+// 3 with a scale-only chain (each side's product of scales folded into its
+// exponent factor, so no tanh code and no extra arithmetic per element).
 template <class DT, class DR, bool kTma, int kMode>
 __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     constexpr bool kXform = kMode == 1;
@@ -381,6 +381,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
     // ---------------------------------------------------------- consumers
     const int t = threadIdx.x;
+    // Scale-only chains keep the logits unscaled: the scale s rides in the
+    // factor to base-2 exponents, (x - m) s log2 e, and the finalise forms
+    // s m and s x[id] in fp64.
+    const float lg_t = kScale ? a.lt : kLog2e, lg_r = kScale ? a.lr : kLog2e;
     const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0}, cxr{xf_ops + (kXform ? LPD_MAX_TRANSFORM_OPS : 0),
                                                               kXform ? a.xr.n_ops : 0};
     uint32_t it = 0;
@@ -429,14 +433,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                             xform16(vt, cxt);
                             xform16(vr, cxr);
                         }
-                        if (kScale) {
-                            const f2_t s_t = f2(a.st, a.st), s_r = f2(a.sr, a.sr);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                vt[q] = mul2(vt[q], s_t);
-                                vr[q] = mul2(vr[q], s_r);
-                            }
-                        }
                     } else {
                         // ragged last tile: the same vector loads, then the
                         // columns the bulk copy did not cover (a few bytes at the
@@ -465,19 +461,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                                         x[h] = xform1(x[h], cxt);
                                         y[h] = xform1(y[h], cxr);
                                     }
-                                    if (kScale && col < nv) {
-                                        x[h] = __fmul_rn(x[h], a.st);
-                                        y[h] = __fmul_rn(y[h], a.sr);
-                                    }
                                 }
                                 vt[p] = f2(x[0], x[1]);
                                 vr[p] = f2(y[0], y[1]);
                             } else if (kXform) {
                                 vt[p] = f2(xform1(f2_lo(vt[p]), cxt), xform1(f2_hi(vt[p]), cxt));
                                 vr[p] = f2(xform1(f2_lo(vr[p]), cxr), xform1(f2_hi(vr[p]), cxr));
-                            } else if (kScale) {
-                                vt[p] = mul2(vt[p], f2(a.st, a.st));
-                                vr[p] = mul2(vr[p], f2(a.sr, a.sr));
                             }
                         }
                     }
@@ -497,10 +486,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                                 x[h] = xform1(x[h], cxt);
                                 y[h] = xform1(y[h], cxr);
                             }
-                            if (kScale && col < nv) {
-                                x[h] = __fmul_rn(x[h], a.st);
-                                y[h] = __fmul_rn(y[h], a.sr);
-                            }
                         }
                         vt[p] = f2(x[0], x[1]);
                         vr[p] = f2(y[0], y[1]);
@@ -508,9 +493,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 }
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
                     a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
-                accumulate16<kEntropy>(vt, vr, acc2);
+                accumulate16<kEntropy>(vt, vr, acc2, lg_t, lg_r);
             }
-            const Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2));
+            const Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2), lg_t, lg_r);
             if (lane == 0) {
                 float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;
                 dst[0] = make_float4(acc.mt, acc.st, acc.dd, acc.mr);
