@@ -428,14 +428,13 @@ cudaError_t launch_merge_shape(const MergeArgs &a, int kv, size_t smem, cudaStre
 }
 
 // Chunks per thread: one up to kSmallParts parts (more resident blocks beat
-// sharing the per-part scalar work between two chunks); beyond, two when a
-// row has an even number of chunks and the staging of up to 32 parts fits.
+// sharing the per-part scalar work between two chunks, in the plain merge and
+// in the order-drift form alike: measured); beyond, two when a row has an even
+// number of chunks and the staging of up to 32 parts fits.
 int merge_kv(int n_parts, int cpr) {
     if (n_parts <= kSmallParts) return 1;
     return (cpr % 2 == 0 && n_parts <= 32) ? 2 : 1;
 }
-
-}  // namespace
 
 size_t attn_merge_smem(int n_parts, int cpr) {
     const int kv = merge_kv(n_parts, cpr);
@@ -444,6 +443,8 @@ size_t attn_merge_smem(int n_parts, int cpr) {
     return static_cast<size_t>(n_parts) * kv * kMergeThreads * 16 + 2 * static_cast<size_t>(nr_max) * max_k * 4 +
            static_cast<size_t>(nr_max) * 4 + 2 * kMaxParts;
 }
+
+}  // namespace
 
 cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream) {
     const int es = c.bf16 ? 2 : 4;

@@ -179,7 +179,6 @@ struct AttnMergeCall {
     float *row_dout, *row_dlse;
     lpd_merge_drift *drift;
 };
-size_t attn_merge_smem(int n_parts, int cpr);
 cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream);
 
 // The all-gather of the allgather_logits arm: shard pieces of every row into
