@@ -48,10 +48,10 @@
  * Bounded waits: no kernel waits without a limit.  The streaming row pass
  * gives up a pipeline wait after 2 s (4 s in the fused LM-head kernel), sets
  * LPD_STATUS_TIMEOUT, lets its in-flight copies land and returns; the context
- * stays usable.  The environment variable LPD_WAIT_LIMIT_NS (read at each
- * call, decimal nanoseconds) shortens the row pass's pipeline limit, so that
- * this path can be exercised on purpose; the final wait for copies in flight
- * always keeps the full limit.
+ * stays usable.  For tests of that path, the environment variable
+ * LPD_STALL_ROW_PASS=1 (read at each call) makes one CTA of the row pass
+ * withhold its first copy: the call then takes about 4 s and returns with
+ * LPD_STATUS_TIMEOUT.
  */
 #ifndef LPD_H
 #define LPD_H

@@ -96,14 +96,11 @@ int run_select(int64_t n_rows, const int32_t *ids, const uint8_t *mask, float *l
     return cuda_status(launch_select_active(n_rows, mask, ids, lt, lr, d, met, w.hdr, w.rowid, s));
 }
 
-// LPD_WAIT_LIMIT_NS shortens the row pass's bounded pipeline waits (tests use
-// it to take the timeout path); unset, empty or invalid: 0, the default limit.
-unsigned long long wait_limit_override() {
-    const char *v = std::getenv("LPD_WAIT_LIMIT_NS");
-    if (!v || !*v) return 0;
-    char *end = nullptr;
-    const unsigned long long x = std::strtoull(v, &end, 10);
-    return (end && *end == '\0') ? x : 0;
+// LPD_STALL_ROW_PASS=1 (tests of the timeout path only): the row pass's CTA 0
+// withholds its first copy, so that its bounded wait runs out.
+bool stall_requested() {
+    const char *v = std::getenv("LPD_STALL_ROW_PASS");
+    return v && v[0] == '1' && v[1] == '\0';
 }
 
 // Stage 2: the streaming row pass, then the per-row finalise.
@@ -155,7 +152,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     a.part = w.part;
     a.pick = w.pick;
     a.status = &met->status;
-    a.wait_limit_ns = wait_limit_override();
+    a.stall = stall_requested() ? 1 : 0;
     int rc = cuda_status(launch_rows(a, dt, dr, tma, mode, s));
     if (rc) return rc;
     FinArgs f{};

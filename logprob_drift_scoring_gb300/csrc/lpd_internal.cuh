@@ -97,7 +97,7 @@ struct RowArgs {
     float4 *part;
     float2 *pick;
     uint32_t *status;
-    unsigned long long wait_limit_ns;  // pipeline waits give up after this long (0: the default)
+    int stall;       // tests of the timeout path: CTA 0 withholds its first copy
 };
 
 struct FinArgs {

@@ -77,19 +77,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of the same phase (try_wait may suspend the thread for a
-// while before it reports false).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                          uint64_t policy) {
     asm volatile(
@@ -100,29 +87,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 // Bounded wait for phase `parity` of an mbarrier.  Gives up (and tells every
-// other thread of the CTA to give up) after limit_ns (kWaitLimitNs unless the
-// caller shortened it), recording LPD_STATUS_TIMEOUT; a pipeline stage
-// normally completes in microseconds.
+// other thread of the CTA to give up) after kWaitLimitNs, recording
+// LPD_STATUS_TIMEOUT; a pipeline stage normally completes in microseconds.
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                           uint32_t *status, bool honour_abort = true,
-                                           unsigned long long limit_ns = kWaitLimitNs) {
-    if (limit_ns < kWaitLimitNs) {
-        // shortened limit: non-blocking probes and a clock check on every spin
-        const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t n = 0; n < kWaitLimitIters; ++n) {
-            if (mbar_test_wait(bar, parity)) return true;
-            if (honour_abort && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) break;
-        }
-    } else {
+                                           uint32_t *status, bool honour_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1; n < kWaitLimitIters; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t n = 1; n < kWaitLimitIters; ++n) {
-            if (mbar_try_wait(bar, parity)) return true;
-            if ((n & 255u) == 0) {
-                if (honour_abort && *abort_flag) return false;
-                if (globaltimer_ns() - t0 > limit_ns) break;
-            }
+        if ((n & 255u) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
         }
     }
     *abort_flag = 1;
@@ -316,8 +291,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_active = a.hdr->n_active;
-    const unsigned long long wait_limit =
-        a.wait_limit_ns && a.wait_limit_ns < kWaitLimitNs ? a.wait_limit_ns : kWaitLimitNs;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -351,8 +324,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                 const char *rb = sg.r + r * sg.r_stride;
                 for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
                     const uint32_t stage = it % n_stages, round = it / n_stages;
-                    if (round > 0 &&
-                        !wait_phase(&empty[stage], (round - 1) & 1, &abort_flag, a.status, true, wait_limit)) {
+                    if (round > 0 && !wait_phase(&empty[stage], (round - 1) & 1, &abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
@@ -361,8 +333,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     const uint32_t br = static_cast<uint32_t>(nv * DR::kBytes) & ~15u;
                     char *st = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
                     mbar_arrive_expect_tx(&full[stage], bt + br);
-                    if (bt) bulk_g2s(st, tb + c0 * DT::kBytes, bt, &full[stage], policy);
-                    if (br) bulk_g2s(st + kStageT, rb + c0 * DR::kBytes, br, &full[stage], policy);
+                    // a.stall (tests of the timeout path only): CTA 0 never
+                    // issues its first copy, so its consumers run into the
+                    // bounded wait; no copy is in flight for that stage
+                    const bool withhold = a.stall && it == 0 && blockIdx.x == 0;
+                    if (bt && !withhold) bulk_g2s(st, tb + c0 * DT::kBytes, bt, &full[stage], policy);
+                    if (br && !withhold) bulk_g2s(st + kStageT, rb + c0 * DR::kBytes, br, &full[stage], policy);
                     ++it;
                 }
             }
@@ -371,7 +347,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
         // thread issued must have landed: the last n_stages ones are the only
         // ones that can still be in flight.  Normally they completed long ago
         // (the consumers waited for them); after an abandoned pipeline this is
-        // the bounded wait for the stragglers, always with the full limit.
+        // the bounded wait for the stragglers.
         (void)ok;
         const uint32_t first = it > static_cast<uint32_t>(n_stages) ? it - n_stages : 0;
         for (uint32_t j = first; j < it; ++j)
@@ -420,7 +396,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                     const uint32_t stage = it % n_stages, round = it / n_stages;
                     // the whole warp leaves together if any lane gave up, so no
                     // lane is left behind at a warp-synchronous instruction
-                    const bool ok = wait_phase(&full[stage], round & 1, &abort_flag, a.status, true, wait_limit);
+                    const bool ok = wait_phase(&full[stage], round & 1, &abort_flag, a.status);
                     if (__any_sync(0xffffffffu, !ok)) return;
                     const char *stg = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
                     if (nv == kTile) {

@@ -381,14 +381,15 @@ def test_full_size_sharded():
     torch.cuda.empty_cache()
 
 
-def test_shortened_wait_limit_times_out_cleanly(monkeypatch):
-    """LPD_WAIT_LIMIT_NS=1 makes the row pass give up its first wait that is not
-    already satisfied: the call returns with LPD_STATUS_TIMEOUT set instead of
-    hanging, and the next call on the same context scores normally."""
+def test_stalled_pipeline_times_out_cleanly(monkeypatch):
+    """LPD_STALL_ROW_PASS=1 makes one CTA of the row pass withhold its first
+    copy (a barrier nothing completes): the call returns after the bounded
+    waits with LPD_STATUS_TIMEOUT set instead of hanging, and the next call on
+    the same context scores normally."""
     w = W.synthetic(600, 3 * 8192 + 96, seed=91, device=DEV, active_prob=1.0)
     assert (w.train.stride(0) * 2) % 16 == 0   # rows take the bulk-copy ring, whose waits are bounded
-    monkeypatch.setenv("LPD_WAIT_LIMIT_NS", "1")
+    monkeypatch.setenv("LPD_STALL_ROW_PASS", "1")
     res = run(w.train, w.rollout, w.token_ids, w.action_mask)
     assert res.metrics["status"] & B.LPD_STATUS_TIMEOUT
-    monkeypatch.delenv("LPD_WAIT_LIMIT_NS")
+    monkeypatch.delenv("LPD_STALL_ROW_PASS")
     check_against_oracle(w)
