@@ -72,18 +72,37 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(config: str):
-    """dram bytes per launch of the row pass from the committed ncu summary, if
-    it was captured on the current kernel source; else None."""
+def profiled_row_kernel(config: str) -> dict | None:
+    """The row pass's committed ncu summary for this config, if it was captured
+    on the current kernel source: DRAM bytes per launch scaled to the full
+    workload, and the DRAM throughput (% of peak) of the captured case."""
     p = ROOT / "profiles" / f"row_kernel_{config}.md"
     if not p.exists():
         return None
     text = p.read_text()
     m_src = re.search(r"kernel_source_sha1:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    m_pct = re.search(r"gpu__dram_throughput\.avg\.pct_of_peak_sustained_elapsed \| ([0-9.]+) %", text)
     if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
         return None
-    return float(m_tr.group(1))
+    return {"traffic": float(m_tr.group(1)), "dram_pct": float(m_pct.group(1)) if m_pct else None}
+
+
+def profiled_traffic(config: str):
+    prof = profiled_row_kernel(config)
+    return prof["traffic"] if prof else None
+
+
+def host_cpu() -> dict:
+    """Core count and CPU model of the host the oracle runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"Model name:\s*(.+)", out)
+        model = m.group(1).strip() if m else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "model": model}
 
 
 # ---------------------------------------------------------------- clocks
@@ -332,7 +351,7 @@ def time_cpu_oracle(config: str, target_s: float = 12.0, max_rows: int = 4096, s
     t0 = time.perf_counter()
     oracle.score_rows(tn, rn, ids, np.arange(n), lib=lib)
     elapsed = time.perf_counter() - t0
-    return {"value": n / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": f"{n} active rows of the {config} recipe, both sides, float64 serial C, {elapsed:.1f} s"}
 
 
@@ -424,7 +443,7 @@ def time_cpu_oracle_attn(target_s: float = 12.0, seed: int = 1234):
     t0 = time.perf_counter()
     oracle.attn_merge(parts, lse, lib=lib)
     elapsed = time.perf_counter() - t0
-    return {"value": w.n_rows / elapsed, "unit": ATTN_UNIT, "cores": 1, "kind": "oracle",
+    return {"value": w.n_rows / elapsed, "unit": ATTN_UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": f"{w.n_rows} rows (T={tokens} x 32 heads, K=8 causal, head_dim 128) of the attn recipe, "
                       f"float64 serial C, {elapsed:.1f} s"}
 
@@ -632,9 +651,11 @@ def run_ours(args):
 
     peaks = measured_peaks()
     achieved = (n_active * bpt + extra_bytes) / (stage2 / 1e3) / 1e9
-    traffic = profiled_traffic(args.config)
+    prof = profiled_row_kernel(args.config) if not whole else None
+    traffic = prof["traffic"] if prof else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "ncu_dram_pct_small_case": prof["dram_pct"] if prof else None,
                 "peak_source": f"{peaks['source']} copy bandwidth (burst)",
                 "span": "whole call" if whole else "stage 2: row kernel + per-row finalise",
                 "algorithmic_bytes_per_launch": n_active * bpt + extra_bytes}
@@ -772,7 +793,8 @@ def run_reference(args):
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": CONFIGS[args.config]["workload"], "sample_rows_per_step": rows_per_step},
            "impl": "reference",
-           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                            "host": host_cpu()},
            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
     return out
@@ -802,6 +824,7 @@ def run_reference_attn(args, world):
            "config": {"workload": CONFIGS["attn"]["workload"], "sample_rows_per_step": rows},
            "impl": "reference",
            "cpu_baseline": {"value": round(value, 2), "unit": ATTN_UNIT, "cores": 1, "kind": "oracle",
+                            "host": host_cpu(),
                             "sample": sample},
            "e2e": {"value": round(value, 2), "unit": ATTN_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
