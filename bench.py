@@ -67,7 +67,8 @@ def measured_peaks() -> dict:
 def kernel_source_hash() -> str:
     h = hashlib.sha1()
     for rel in KERNEL_SOURCES + ["logprob_drift_scoring_gb300/csrc/lpd_internal.cuh",
-                                 "logprob_drift_scoring_gb300/csrc/lpd_acc.cuh"]:
+                                 "logprob_drift_scoring_gb300/csrc/lpd_acc.cuh",
+                                 "logprob_drift_scoring_gb300/csrc/lpd_xform.cuh"]:
         h.update((ROOT / rel).read_bytes())
     return h.hexdigest()[:12]
 
@@ -364,7 +365,8 @@ def measured_tflops() -> dict:
 
 
 def run_fused(args, w, world, rank):
-    """The fused LM-head path: one lpd_score_fused call per step."""
+    """The fused LM-head path: one lpd_score_fused call per step (with
+    --transform, lpd_score_fused_transformed with that chain on both sides)."""
     import torch
     from logprob_drift_scoring_gb300 import binding as B
 
@@ -373,10 +375,15 @@ def run_fused(args, w, world, rank):
     outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
     met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=dev)
     ws = torch.empty(B.lpd_fused_workspace_size(n, w.hidden, w.vocab), dtype=torch.uint8, device=dev)
+    chain = parse_chain(args.transform) if args.transform else None
 
     def step():
-        B.lpd_score_fused(w.hidden_train, w.hidden_rollout, w.weight, w.token_ids, w.action_mask, *w.clip, *outs,
-                          met, ws)
+        if chain is None:
+            B.lpd_score_fused(w.hidden_train, w.hidden_rollout, w.weight, w.token_ids, w.action_mask, *w.clip,
+                              *outs, met, ws)
+        else:
+            B.lpd_score_fused_transformed(w.hidden_train, w.hidden_rollout, w.weight, chain, chain, w.token_ids,
+                                          w.action_mask, *w.clip, *outs, met, ws)
 
     for _ in range(args.warmup):
         step()
@@ -402,11 +409,14 @@ def run_fused(args, w, world, rank):
         "metric": METRIC, "value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": CONFIGS["fused"]["workload"], "rows": n, "active_tokens": n_active,
+        "config": {"workload": CONFIGS["fused"]["workload"]
+                   + (f" + transform {args.transform}" if args.transform else ""), "rows": n,
+                   "active_tokens": n_active,
                    "hidden": w.hidden, "vocab": w.vocab, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peak["tflops"], 4), "traffic": None,
-                     "peak_source": f"{peak['source']} bf16 GEMM", "span": "whole lpd_score_fused call",
+                     "peak_source": f"{peak['source']} bf16 GEMM", "span": "whole lpd_score_fused call" if chain is None
+                     else "whole lpd_score_fused_transformed call",
                      "algorithmic_flops_per_launch": flops},
         "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * args.steps, "clocks": clocks.summary(),
         "impl": "lpd",

@@ -379,6 +379,23 @@ int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const 
                     lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                     void *stream);
 
+/* lpd_score_fused with a logit transform chain per side (each may be NULL for
+ * the identity; "[WS2] Framework for ablation experiment", LogProb knobs table,
+ * row 7).  Each fp32 logit out of the tensor cores goes through its side's
+ * chain, with the same arithmetic as lpd_score_transformed, before the online
+ * log-sum-exp sees it and before the selected logit is taken; the columns past
+ * `vocab` in the last tile stay out of the sum.  Arguments, workspace, outputs
+ * and errors are those of lpd_score_fused; a chain that is not valid returns
+ * LPD_ERR_BAD_TRANSFORM before any launch. */
+int lpd_score_fused_transformed(const void *hidden_train, const void *hidden_rollout,
+                                const void *W, const lpd_transform *train_chain,
+                                const lpd_transform *rollout_chain, int64_t n_rows,
+                                int64_t hidden, int64_t vocab, const int32_t *token_ids,
+                                const uint8_t *action_mask, double clip_lo, double clip_hi,
+                                float *out_logp_train, float *out_logp_rollout,
+                                float *out_dlogp, lpd_metrics *out_metrics, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
 /* ---- attention (out, lse) merge --------------------------------------------- */
 
 /* Split-KV / context-parallel attention partials are merged with the same

@@ -97,8 +97,8 @@ MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
-            "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_transformed", "lpd_score_entropy",
-            "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
+            "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_fused_transformed", "lpd_score_transformed",
+            "lpd_score_entropy", "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
             "lpd_topology_workspace_size", "lpd_score_sharded_topology", "lpd_drift_metrics_from_dlogp")
 LPD_NOALLOC_MAX_ROWS = 32768
 LPD_ATTN_MAX_PARTS = 64
@@ -140,6 +140,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_fused_workspace_size.argtypes = [I64, I64, I64]
         L.lpd_score_fused.restype = ctypes.c_int
         L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
+        L.lpd_score_fused_transformed.restype = ctypes.c_int
+        L.lpd_score_fused_transformed.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_transformed.restype = ctypes.c_int
         L.lpd_score_transformed.argtypes = [P, P, P, P, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_entropy.restype = ctypes.c_int
@@ -363,6 +365,19 @@ def lpd_score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, cli
     _check(rc, "lpd_score_fused")
 
 
+def lpd_score_fused_transformed(hidden_train, hidden_rollout, W, train_ops, rollout_ops, token_ids, action_mask,
+                                clip_lo, clip_hi, out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace,
+                                stream=None) -> None:
+    n_rows, hidden = hidden_train.shape
+    ct, cr = transform_struct(train_ops), transform_struct(rollout_ops)
+    rc = lib().lpd_score_fused_transformed(
+        _ptr(hidden_train), _ptr(hidden_rollout), _ptr(W), ctypes.byref(ct) if ct else None,
+        ctypes.byref(cr) if cr else None, n_rows, hidden, W.shape[0], _ptr(token_ids), _ptr(action_mask),
+        float(clip_lo), float(clip_hi), _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp),
+        _ptr(out_metrics), _ptr(workspace), workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(rc, "lpd_score_fused_transformed")
+
+
 def lpd_score_noalloc(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
                       out_dlogp, out_metrics, stream=None) -> None:
     """lpd_score with the library's built-in scratch instead of a workspace
@@ -448,8 +463,10 @@ def read_metrics(buf) -> dict:
     return LpdMetrics.from_buffer_copy(host).as_dict()
 
 
-def score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip=(0.8, 1.2), stream=None):
-    """Allocate outputs and workspace with torch, run lpd_score_fused."""
+def score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip=(0.8, 1.2), stream=None,
+                train_ops=None, rollout_ops=None):
+    """Allocate outputs and workspace with torch, run lpd_score_fused (or
+    lpd_score_fused_transformed when a chain is given)."""
     import torch
 
     dev = hidden_train.device
@@ -457,8 +474,12 @@ def score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip=(0
     outs = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
     met = torch.empty(METRICS_BYTES, dtype=torch.uint8, device=dev)
     ws = torch.empty(lpd_fused_workspace_size(n, hidden_train.shape[1], W.shape[0]), dtype=torch.uint8, device=dev)
-    lpd_score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip[0], clip[1], *outs, met, ws,
-                    stream=stream)
+    if train_ops is None and rollout_ops is None:
+        lpd_score_fused(hidden_train, hidden_rollout, W, token_ids, action_mask, clip[0], clip[1], *outs, met, ws,
+                        stream=stream)
+    else:
+        lpd_score_fused_transformed(hidden_train, hidden_rollout, W, train_ops, rollout_ops, token_ids, action_mask,
+                                    clip[0], clip[1], *outs, met, ws, stream=stream)
     return ScoreResult(outs[0], outs[1], outs[2], read_metrics(met))
 
 

@@ -723,6 +723,17 @@ int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const 
                     double clip_lo, double clip_hi, float *out_logp_train, float *out_logp_rollout,
                     float *out_dlogp, lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                     void *stream) {
+    return lpd_score_fused_transformed(hidden_train, hidden_rollout, W, nullptr, nullptr, n_rows, hidden, vocab,
+                                       token_ids, action_mask, clip_lo, clip_hi, out_logp_train, out_logp_rollout,
+                                       out_dlogp, out_metrics, workspace, workspace_bytes, stream);
+}
+
+int lpd_score_fused_transformed(const void *hidden_train, const void *hidden_rollout, const void *W,
+                                const lpd_transform *train_chain, const lpd_transform *rollout_chain,
+                                int64_t n_rows, int64_t hidden, int64_t vocab, const int32_t *token_ids,
+                                const uint8_t *action_mask, double clip_lo, double clip_hi, float *out_logp_train,
+                                float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
+                                void *workspace, size_t workspace_bytes, void *stream) {
     int rc = check_rows_vocab(n_rows, vocab);
     if (rc) return rc;
     if (hidden <= 0) return LPD_ERR_BAD_SIZE;
@@ -733,8 +744,12 @@ int lpd_score_fused(const void *hidden_train, const void *hidden_rollout, const 
     if ((rc = check_clip(clip_lo, clip_hi))) return rc;
     if ((rc = check_workspace(workspace, workspace_bytes, lpd_fused_workspace_size(n_rows, hidden, vocab))))
         return rc;
+    Xform xt, xr;
+    if ((rc = to_xform(train_chain, &xt)) || (rc = to_xform(rollout_chain, &xr))) return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     FusedCall c{};
+    c.xt = xt;
+    c.xr = xr;
     c.layout = fused_layout(n_rows, hidden, vocab);
     c.workspace = workspace;
     c.hidden_train = hidden_train;

@@ -19,7 +19,9 @@
 //      fixed K order, into two 256-column accumulators in tensor memory; warps
 //      2-5 read the accumulators back (tcgen05.ld) and fold each row's 256
 //      logits of both sides into one online log-sum-exp state (lpd_acc.cuh),
-//      written as that (row, vocab tile)'s partial.  Tiles are visited in
+//      written as that (row, vocab tile)'s partial (in the transform
+//      variant each side's logit chain is applied first, lpd_xform.cuh).
+//      Tiles are visited in
 //      groups of 8 row tiles so that the CTAs running together share their W
 //      tiles and hidden tiles in L2.
 //   3. head_finalize_kernel: one warp per active row merges its vocab-tile
@@ -39,6 +41,7 @@
 
 #include "lpd_acc.cuh"
 #include "lpd_internal.cuh"
+#include "lpd_xform.cuh"
 
 namespace lpd {
 namespace {
@@ -178,6 +181,7 @@ struct HeadArgs {
     float *part_b;         // [A_pad, n_tiles_n] sr
     float2 *pick;          // [A_pad] selected logits
     uint32_t *status;
+    Xform xt, xr;          // transform chains (the kXform kernel only)
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, int n_m, int n_n, int &m, int &n) {
@@ -189,12 +193,17 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_m, int n_n, int &m,
     n = static_cast<int>(local / gm);
 }
 
+// kXform: each side's transform chain is applied to the accumulator values
+// right after they leave tensor memory, before the vocab-tail mask, so the
+// selected logit and the sums see transformed values and padding stays -inf.
+template <bool kXform>
 __global__ void __launch_bounds__(kHeadThreads, 1)
     head_kernel(const __grid_constant__ HeadMaps maps, const __grid_constant__ HeadArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     __shared__ uint64_t full[kStages], empty[kStages], tmem_full, tmem_empty, mma_done;
     __shared__ uint32_t tmem_base_slot;
     __shared__ int abort_flag;
+    __shared__ float4 xf_ops[2 * LPD_MAX_TRANSFORM_OPS];
     // the swizzled tiles need 1024-byte alignment
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -214,6 +223,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         mbar_init(&tmem_full, 1);
         mbar_init(&tmem_empty, 4);
         mbar_init(&mma_done, 1);
+        if (kXform) {
+            xform_table(a.xt, xf_ops);
+            xform_table(a.xr, xf_ops + LPD_MAX_TRANSFORM_OPS);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -297,6 +310,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;  // tensor-memory lanes [32 quad, 32 quad + 32)
         const int row_in_tile = quad * 32 + lane;
+        const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0},
+            cxr{xf_ops + LPD_MAX_TRANSFORM_OPS, kXform ? a.xr.n_ops : 0};
         uint32_t local = 0;
         for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
             const bool ok = wait_phase(&tmem_full, local & 1, &abort_flag, a.status);
@@ -315,6 +330,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 f2_t vt[8], vr[8];
                 tmem_ld16(lane_addr + c, vt);
                 tmem_ld16(lane_addr + kBN + c, vr);
+                if (kXform) {
+                    xform16(vt, cxt);
+                    xform16(vr, cxr);
+                }
                 const int64_t col0 = c_base + c;
                 if (col0 + 16 > a.vocab) {  // vocab tail: columns past V are not logits
 #pragma unroll
@@ -534,16 +553,26 @@ cudaError_t launch_fused(const FusedCall &c, cudaStream_t stream) {
     a.part_b = part_b;
     a.pick = pick;
     a.status = c.status;
+    a.xt = c.xt;
+    a.xr = c.xr;
+    const bool xf = c.xt.n_ops > 0 || c.xr.n_ops > 0;
     const size_t smem = static_cast<size_t>(kStages) * kStage + 1024;
     static int configured_device = -1;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        e = cudaFuncSetAttribute(head_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(head_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    head_kernel<<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
+    if (xf)
+        head_kernel<true><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
+    else
+        head_kernel<false><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const unsigned fin_blocks = static_cast<unsigned>((c.n_rows + 7) / 8);

@@ -140,6 +140,7 @@ struct FusedCall {
     int64_t n_rows, hidden, vocab;
     float *out_lt, *out_lr, *out_d;
     uint32_t *status;
+    Xform xt, xr;  // logit transform chains (n_ops 0 on both sides: none)
 };
 
 FusedLayout fused_layout(int64_t n_rows, int64_t hidden, int64_t vocab);

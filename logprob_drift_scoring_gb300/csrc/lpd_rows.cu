@@ -30,6 +30,7 @@
 
 #include "lpd_acc.cuh"
 #include "lpd_internal.cuh"
+#include "lpd_xform.cuh"
 
 namespace lpd {
 namespace {
@@ -143,123 +144,6 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
 // is copied into registers once per thread (constant indices only, so it never
 // lives in local memory); ops past n are skipped.  Only real columns are
 // transformed; masked tail columns stay -inf.
-// A side's chain as the consumers read it: one {kind, p, 1/p} entry per op in
-// a shared-memory table (dynamic indexing stays cheap there), walked by a real
-// loop so each op body is emitted once per call site.
-struct XformView {
-    const float4 *ops;  // x: kind (as int bits), y: p, z: 1/p
-    int n;
-};
-
-__device__ __forceinline__ void xform_table(const Xform &c, float4 *ops) {
-    for (int k = 0; k < c.n_ops; ++k)
-        ops[k] = make_float4(__int_as_float(c.kind[k]), c.param[k], __frcp_rn(c.param[k]), 0.f);
-}
-
-// ---- soft-cap p * tanh(x / p) ---------------------------------------------
-// Near-identical logits on the two sides must get near-identical transformed
-// values, so tanh has to stay at the level of fp32 rounding (the hardware
-// tanh.approx, about 2^-11 relative, does not).  Own tanh, from its series
-// and its exponential form, with y = x / p and z = y^2:
-//   z < 0.36:   p tanh(y) = x (1 + z P(z)), P of degree 5 fitted to
-//               (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: tanh within 0.70 ulp
-//               in float32 Horner evaluation); p y is written as x itself;
-//   otherwise:  p tanh(y) = p sign(y) (1 - 2 / (1 + 2^(2|y| log2 e))), with
-//               ex2.approx and rcp.approx (a few ulp where |y| >= 0.6,
-//               exactly +-p once the power overflows; NaN stays NaN).
-// Every path takes the same per-element decision on the same rounded z, and
-// the packed path rounds each half like the scalar one, so a column's value
-// does not depend on which load path or lane handled it.
-constexpr float kTanhZMax = 0.36f;
-__host__ __device__ constexpr float tanh_c(int k) {
-    return k == 0 ? -3.333333135e-01f : k == 1 ? 1.333319992e-01f : k == 2 ? -5.394675583e-02f
-         : k == 3 ? 2.170414850e-02f : k == 4 ? -8.193124086e-03f : 2.163204830e-03f;
-}
-
-__device__ __forceinline__ float rcp_approx(float x) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
-// z P(z)
-__device__ __forceinline__ float tanh_q(float z) {
-    float p = tanh_c(5);
-#pragma unroll
-    for (int k = 4; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
-    return __fmul_rn(z, p);
-}
-
-__device__ __forceinline__ float tanh_exp(float y) {
-    const float e = ex2(__fmul_rn(fabsf(y), 2.8853900817779268f));  // 2^(2|y| log2 e)
-    const float t = __fmaf_rn(-2.f, rcp_approx(__fadd_rn(1.f, e)), 1.f);
-    return copysignf(t, y);
-}
-
-__device__ __forceinline__ float softcap1(float x, float p, float rcp) {
-    const float y = __fmul_rn(x, rcp), z = __fmul_rn(y, y);
-    return z < kTanhZMax ? __fmaf_rn(x, tanh_q(z), x) : __fmul_rn(p, tanh_exp(y));
-}
-
-// Sixteen values in place.  When no value of the warp needs the exponential
-// form (the usual case: |x| < 0.6 p everywhere) only the packed polynomial runs.
-__device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
-    const f2_t r2 = f2(rcp, rcp);
-    f2_t y[8], z[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        y[q] = mul2(v[q], r2);
-        z[q] = mul2(y[q], y[q]);
-    }
-    const float zmax = max16(z);
-    f2_t o[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        f2_t pp = f2(tanh_c(5), tanh_c(5));
-#pragma unroll
-        for (int k = 4; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
-        o[q] = fma2(v[q], mul2(z[q], pp), v[q]);
-    }
-    if (__any_sync(0xffffffffu, !(zmax < kTanhZMax))) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float lo = f2_lo(z[q]) < kTanhZMax ? f2_lo(o[q]) : __fmul_rn(p, tanh_exp(f2_lo(y[q])));
-            const float hi = f2_hi(z[q]) < kTanhZMax ? f2_hi(o[q]) : __fmul_rn(p, tanh_exp(f2_hi(y[q])));
-            o[q] = f2(lo, hi);
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = o[q];
-}
-
-__device__ __forceinline__ float xform1(float x, const XformView &c) {
-#pragma unroll 1
-    for (int k = 0; k < c.n; ++k) {
-        const float4 op = c.ops[k];
-        if (__float_as_int(op.x) == LPD_OP_SCALE)
-            x = __fmul_rn(x, op.y);
-        else
-            x = softcap1(x, op.y, op.z);
-    }
-    return x;
-}
-
-// The chain over sixteen values: ops outermost, so each op's kind is decided
-// once per chunk (it is the same for every thread); both ops run packed.
-__device__ __forceinline__ void xform16(f2_t *v, const XformView &c) {
-#pragma unroll 1
-    for (int k = 0; k < c.n; ++k) {
-        const float4 op = c.ops[k];
-        if (__float_as_int(op.x) == LPD_OP_SCALE) {
-            const f2_t p2 = f2(op.y, op.y);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = mul2(v[q], p2);
-        } else {
-            softcap16(v, op.y, op.z);
-        }
-    }
-}
-
 // Column of slot q (0..15) of consumer thread t within a tile.
 __device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroupCols + 4 * t + (q & 3); }
 

@@ -179,19 +179,35 @@ def test_fused_workspace_size():
     assert B.lpd_fused_workspace_size(128, 4096, 1000) >= 2 * 128 * 4096 * 2
 
 
-@pytest.mark.parametrize("ops", [
+BAD_CHAINS = [
     [(3, 1.0)],                      # unknown kind
     [(B.LPD_OP_SCALE, 0.0)],         # non-positive
     [(B.LPD_OP_SCALE, -2.0)],
     [(B.LPD_OP_SOFTCAP, float("inf"))],
     [(B.LPD_OP_SOFTCAP, float("nan"))],
-])
+]
+
+
+@pytest.mark.parametrize("ops", BAD_CHAINS)
 def test_transform_chain_rejected(ops):
     t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 16)
     c = B.transform_struct(ops)
     rc = B.lib().lpd_score_transformed(ctypes.byref(t), ctypes.byref(t), None, ctypes.byref(c), 8, 16, FAKE, FAKE,
                                        0.8, 1.2, None, None, None, FAKE, WS_OK, 1 << 20, None)
     assert rc == B.LPD_ERR_BAD_TRANSFORM
+
+
+@pytest.mark.parametrize("ops", BAD_CHAINS)
+def test_fused_transform_chain_rejected(ops):
+    c = B.transform_struct(ops)
+    lib = B.lib()
+    rc = lib.lpd_score_fused_transformed(FAKE, FAKE, FAKE, ctypes.byref(c), None, 8, 128, 100, FAKE, FAKE, 0.8, 1.2,
+                                         None, None, None, FAKE, WS_OK, 1 << 30, None)
+    assert rc == B.LPD_ERR_BAD_TRANSFORM
+    # the fused-path argument checks still come first for the transformed entry
+    rc = lib.lpd_score_fused_transformed(FAKE, FAKE, FAKE, ctypes.byref(c), None, 8, 100, 100, FAKE, FAKE, 0.8, 1.2,
+                                         None, None, None, FAKE, WS_OK, 1 << 30, None)
+    assert rc == B.LPD_ERR_ALIGNMENT
 
 
 def test_transform_chain_too_long():

@@ -133,13 +133,17 @@ def test_fused_head_in_a_graph():
     h = W.head(300, 512, 8192, seed=77, device=DEV)
     h2 = W.head(300, 512, 8192, seed=78, device=DEV)
     n = h.n_rows
-    outs = [torch.empty(n, device=DEV) for _ in range(3)]
+    outs = [torch.empty(n, device=DEV) for _ in range(6)]
     met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    met2 = torch.empty_like(met)
     ws = torch.empty(B.lpd_fused_workspace_size(n, 512, 8192), dtype=torch.uint8, device=DEV)
+    ops = [(B.LPD_OP_SCALE, 10.0), (B.LPD_OP_SOFTCAP, 5.0)]
 
     def step():
-        B.lpd_score_fused(h.hidden_train, h.hidden_rollout, h.weight, h.token_ids, h.action_mask, 0.8, 1.2, *outs,
-                          met, ws)
+        B.lpd_score_fused(h.hidden_train, h.hidden_rollout, h.weight, h.token_ids, h.action_mask, 0.8, 1.2,
+                          *outs[:3], met, ws)
+        B.lpd_score_fused_transformed(h.hidden_train, h.hidden_rollout, h.weight, ops, ops[::-1], h.token_ids,
+                                      h.action_mask, 0.8, 1.2, *outs[3:], met2, ws)
 
     _check_replays([h.hidden_train, h.hidden_rollout, h.weight, h.token_ids],
-                   [h2.hidden_train, h2.hidden_rollout, h2.weight, h2.token_ids], outs + [met], step)
+                   [h2.hidden_train, h2.hidden_rollout, h2.weight, h2.token_ids], outs + [met, met2], step)
