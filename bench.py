@@ -13,8 +13,10 @@ Printed (one JSON line, rank 0):
   value      active tokens scored per second, device-timed (CUDA events)
   roofline   stage 2's algorithmic bytes / its average duration vs the
              measured HBM copy bandwidth
-  e2e        the same metric through the C ABI with the inputs copied from
-             pinned host memory every step and the metrics record read back
+  e2e        the same metric through the C ABI (lpd_score_host) with the
+             inputs in pinned host memory: every step copies the active rows
+             of both sides plus ids and mask to the device, scores them and
+             reads the metrics record back
   cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
 
 --impl reference times the oracle alone (the reference arm of this build).
@@ -714,8 +716,9 @@ def _dtypes(w):
 
 
 def run_e2e(w, args, world: int = 1):
-    """Through lpd_score with host inputs: per step, copy logits, ids and mask
-    from pinned host memory, score, and read the metrics record back."""
+    """Through lpd_score_host with host inputs: per step, the active rows of
+    both sides' logits plus ids and mask go from pinned host memory to the
+    device, the rows are scored, and the metrics record is read back."""
     import torch
     from logprob_drift_scoring_gb300 import binding as B
 
@@ -735,13 +738,12 @@ def run_e2e(w, args, world: int = 1):
     met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=dev)
     met_host = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, pin_memory=pinned)
     ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, w.n_rows), dtype=torch.uint8, device=dev)
-    bi = sum(h.numel() * h.element_size() for h in host)
     n_active = int(w.action_mask.sum().item())
+    copied = []
 
     def one():
-        for d, h in zip(dbuf, host):
-            d.copy_(h, non_blocking=True)
-        B.lpd_score(dbuf[0], dbuf[1], dbuf[2], dbuf[3], w.clip[0], w.clip[1], *outs, met, ws)
+        copied.append(B.lpd_score_host(host[0], host[1], host[2], host[3], w.clip[0], w.clip[1], *dbuf, *outs, met,
+                                       ws))
         met_host.copy_(met, non_blocking=True)
 
     for _ in range(2):  # warm-up: the first pass over fresh pinned buffers is slow
@@ -757,9 +759,10 @@ def run_e2e(w, args, world: int = 1):
     ms = barrier_max(s.elapsed_time(e) / steps, world)
     del dbuf, host
     torch.cuda.empty_cache()
-    return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi,
+    assert len(set(copied)) == 1  # the same rows every step
+    return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": copied[0],
             "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ms, 3), "pinned": pinned,
-            "steps": steps}
+            "steps": steps, "copies": "active rows of both sides (one 2-D copy per run of active rows), ids, mask"}
 
 
 # ---------------------------------------------------------------- reference arm

@@ -203,6 +203,36 @@ int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows
               float *out_logp_rollout, float *out_dlogp, lpd_metrics *out_metrics,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* lpd_score on logits held in HOST memory (page-locked for full link speed).
+ * The scorer never reads an inactive row ("Measurement Contract": prompt and
+ * padding positions are excluded), so only active rows cross the host-device
+ * link: the host reads action_mask_host during the call and, for every run of
+ * consecutive active rows, issues one 2-D copy per side into the same rows of
+ * the caller's device staging buffers; ids and mask are copied whole.  Then
+ * lpd_score runs on the staged rows.  Everything is ordered on `stream`.
+ * Inactive rows of the staging buffers keep whatever they held.
+ *
+ * train_host, rollout_host   lpd_logits over host memory [n_rows, vocab].
+ * train_dev, rollout_dev     lpd_logits over device memory [n_rows, vocab]
+ *                            (row_stride >= vocab), each with the dtype of
+ *                            its host side, else LPD_ERR_BAD_DTYPE.
+ * token_ids_host, action_mask_host   host int32[n_rows], uint8[n_rows].
+ * token_ids_dev, action_mask_dev     device int32[n_rows], uint8[n_rows].
+ * out_h2d_bytes   host int64, or NULL: the bytes this call copies to the
+ *                 device (active rows of both sides, ids and mask).
+ * Other arguments, outputs and errors as lpd_score.  As with any
+ * asynchronous copy, the host buffers must not change until the copies have
+ * completed on `stream`.  The copies issued depend on the mask's contents at
+ * call time, so the call is not meant for CUDA-graph capture. */
+int lpd_score_host(const lpd_logits *train_host, const lpd_logits *rollout_host,
+                   const lpd_logits *train_dev, const lpd_logits *rollout_dev,
+                   int64_t n_rows, int64_t vocab, const int32_t *token_ids_host,
+                   const uint8_t *action_mask_host, int32_t *token_ids_dev,
+                   uint8_t *action_mask_dev, double clip_lo, double clip_hi,
+                   float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
+                   lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
+                   int64_t *out_h2d_bytes, void *stream);
+
 /* Stage 1 of lpd_score ("Measurement Contract": prompt, padding and masked
  * positions are excluded): the order-preserving list of active rows with
  * their token ids, and their count, into the workspace; zeroes the per-token

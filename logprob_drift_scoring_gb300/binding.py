@@ -95,7 +95,8 @@ class LpdMergeDrift(ctypes.Structure):
 MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
 
 # every symbol include/lpd.h declares
-EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_select_active",
+EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_score_host",
+            "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_fused_transformed", "lpd_score_transformed",
             "lpd_score_entropy", "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
@@ -142,6 +143,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_fused_transformed.restype = ctypes.c_int
         L.lpd_score_fused_transformed.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
+        L.lpd_score_host.restype = ctypes.c_int
+        L.lpd_score_host.argtypes = [P, P, P, P, I64, I64, P, P, P, P, D, D, P, P, P, P, P, SZ, P, P]
         L.lpd_score_transformed.restype = ctypes.c_int
         L.lpd_score_transformed.argtypes = [P, P, P, P, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_entropy.restype = ctypes.c_int
@@ -237,6 +240,24 @@ def lpd_score(train, rollout, token_ids, action_mask, clip_lo, clip_hi, out_logp
                          _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics), _ptr(workspace),
                          workspace.numel() if workspace is not None else 0, _stream(stream))
     _check(rc, "lpd_score")
+
+
+def lpd_score_host(train_host, rollout_host, token_ids_host, action_mask_host, clip_lo, clip_hi, train_dev,
+                   rollout_dev, token_ids_dev, action_mask_dev, out_logp_train, out_logp_rollout, out_dlogp,
+                   out_metrics, workspace, stream=None) -> int:
+    """lpd_score_host: host tensors in, device staging and outputs; returns
+    the bytes copied to the device."""
+    th, rh = logits_struct(train_host), logits_struct(rollout_host)
+    td, rd = logits_struct(train_dev), logits_struct(rollout_dev)
+    copied = ctypes.c_int64(0)
+    rc = lib().lpd_score_host(ctypes.byref(th), ctypes.byref(rh), ctypes.byref(td), ctypes.byref(rd),
+                              train_host.shape[0], train_host.shape[1], _ptr(token_ids_host), _ptr(action_mask_host),
+                              _ptr(token_ids_dev), _ptr(action_mask_dev), float(clip_lo), float(clip_hi),
+                              _ptr(out_logp_train), _ptr(out_logp_rollout), _ptr(out_dlogp), _ptr(out_metrics),
+                              _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                              ctypes.byref(copied), _stream(stream))
+    _check(rc, "lpd_score_host")
+    return int(copied.value)
 
 
 def lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, action_mask, clip_lo, clip_hi,

@@ -509,6 +509,60 @@ int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, s);
 }
 
+int lpd_score_host(const lpd_logits *train_host, const lpd_logits *rollout_host, const lpd_logits *train_dev,
+                   const lpd_logits *rollout_dev, int64_t n_rows, int64_t vocab, const int32_t *token_ids_host,
+                   const uint8_t *action_mask_host, int32_t *token_ids_dev, uint8_t *action_mask_dev, double clip_lo,
+                   double clip_hi, float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
+                   lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes, int64_t *out_h2d_bytes,
+                   void *stream) {
+    if (out_h2d_bytes) *out_h2d_bytes = 0;
+    int rc = validate_pair(train_host, rollout_host, n_rows, vocab);
+    if (rc || (rc = validate_pair(train_dev, rollout_dev, n_rows, vocab))) return rc;
+    if (train_host->dtype != train_dev->dtype || rollout_host->dtype != rollout_dev->dtype) return LPD_ERR_BAD_DTYPE;
+    if (!out_metrics ||
+        ((!token_ids_host || !action_mask_host || !token_ids_dev || !action_mask_dev) && n_rows > 0))
+        return LPD_ERR_NULL_POINTER;
+    if ((rc = check_clip(clip_lo, clip_hi))) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t bytes = 0;
+    if (n_rows > 0) {
+        const size_t n = static_cast<size_t>(n_rows);
+        if ((rc = cuda_status(cudaMemcpyAsync(token_ids_dev, token_ids_host, n * sizeof(int32_t),
+                                              cudaMemcpyHostToDevice, s))) ||
+            (rc = cuda_status(cudaMemcpyAsync(action_mask_dev, action_mask_host, n, cudaMemcpyHostToDevice, s))))
+            return rc;
+        bytes += static_cast<int64_t>(n * (sizeof(int32_t) + 1));
+        const lpd_logits *side_h[2] = {train_host, rollout_host}, *side_d[2] = {train_dev, rollout_dev};
+        for (int64_t r0 = 0; r0 < n_rows;) {
+            if (!action_mask_host[r0]) {
+                ++r0;
+                continue;
+            }
+            int64_t r1 = r0 + 1;
+            while (r1 < n_rows && action_mask_host[r1]) ++r1;
+            for (int k = 0; k < 2; ++k) {
+                const size_t eb = static_cast<size_t>(elt_bytes(side_h[k]->dtype));
+                const size_t ph = static_cast<size_t>(side_h[k]->row_stride) * eb;
+                const size_t pd = static_cast<size_t>(side_d[k]->row_stride) * eb;
+                const size_t width = static_cast<size_t>(vocab) * eb;
+                // the device descriptor names the staging buffer this call fills
+                char *dst = static_cast<char *>(const_cast<void *>(side_d[k]->ptr)) + r0 * pd;
+                const char *src = static_cast<const char *>(side_h[k]->ptr) + r0 * ph;
+                if ((rc = cuda_status(cudaMemcpy2DAsync(dst, pd, src, ph, width, static_cast<size_t>(r1 - r0),
+                                                        cudaMemcpyHostToDevice, s))))
+                    return rc;
+                bytes += static_cast<int64_t>(width) * (r1 - r0);
+            }
+            r0 = r1;
+        }
+    }
+    if (out_h2d_bytes) *out_h2d_bytes = bytes;
+    return lpd_score(train_dev, rollout_dev, n_rows, vocab, token_ids_dev, action_mask_dev, clip_lo, clip_hi,
+                     out_logp_train, out_logp_rollout, out_dlogp, out_metrics, workspace, workspace_bytes, stream);
+}
+
 int lpd_score_transformed(const lpd_logits *train, const lpd_logits *rollout, const lpd_transform *train_chain,
                           const lpd_transform *rollout_chain, int64_t n_rows, int64_t vocab, const int32_t *token_ids,
                           const uint8_t *action_mask, double clip_lo, double clip_hi, float *out_logp_train,

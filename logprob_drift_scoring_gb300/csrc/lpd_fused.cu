@@ -17,13 +17,15 @@
 //      (128-byte swizzle); warp 1 issues tcgen05.mma (kind::f16, bf16 x bf16
 //      -> fp32, M=128 N=256 K=16) for both sides against the same W tile, in a
 //      fixed K order, into two 256-column accumulators in tensor memory; warps
-//      2-5 read the accumulators back (tcgen05.ld) and fold each row's 256
-//      logits of both sides into one online log-sum-exp state (lpd_acc.cuh),
-//      written as that (row, vocab tile)'s partial (in the transform
-//      variant each side's logit chain is applied first, lpd_xform.cuh).
-//      Tiles are visited in
-//      groups of 8 row tiles so that the CTAs running together share their W
-//      tiles and hidden tiles in L2.
+//      2-17 read the accumulators back (tcgen05.ld), four warps per row, each
+//      folding 64 columns of both sides into an online log-sum-exp state
+//      (lpd_acc.cuh); the four states are merged in column order and written
+//      as that (row, vocab tile)'s partial (in the transform variant each
+//      side's logit chain is applied first, lpd_xform.cuh).  The accumulators
+//      fill tensor memory, so the next tile's MMAs wait for this drain; four
+//      warps per row cut that wait to a quarter.  Tiles are visited in groups of 8 row
+//      tiles so that the CTAs running together share their W tiles and hidden
+//      tiles in L2.
 //   3. head_finalize_kernel: one warp per active row merges its vocab-tile
 //      partials in vocab order (fixed tree) and applies the same fp64 row
 //      arithmetic as the unfused path.
@@ -54,7 +56,10 @@ constexpr int kStages = 3;
 constexpr int kATile = kBM * kBK * 2;          // 16 KB
 constexpr int kBTile = kBN * kBK * 2;          // 32 KB
 constexpr int kStage = 2 * kATile + kBTile;    // 64 KB
-constexpr int kHeadThreads = 6 * 32;           // producer, MMA, 4 epilogue warps
+constexpr int kEpiSplit = 4;                   // epilogue warps per tensor-memory lane quadrant
+constexpr int kEpiWarps = 4 * kEpiSplit;
+constexpr int kEpiCols = kBN / kEpiSplit;      // accumulator columns per epilogue warp
+constexpr int kHeadThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
 constexpr int kGroupM = 8;                     // row tiles per raster group
 constexpr uint32_t kTmemCols = 512;            // two 128 x 256 fp32 accumulators
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
@@ -201,6 +206,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     head_kernel(const __grid_constant__ HeadMaps maps, const __grid_constant__ HeadArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     __shared__ uint64_t full[kStages], empty[kStages], tmem_full, tmem_empty, mma_done;
+    // a row's column-half states, handed by the other warps of its lane
+    // quadrant to the quadrant's lead warp (one phase per tile)
+    __shared__ uint64_t xchg_full[4];
+    __shared__ float xchg[kEpiSplit > 1 ? kEpiSplit - 1 : 1][5][kBM];
     __shared__ uint32_t tmem_base_slot;
     __shared__ int abort_flag;
     __shared__ float4 xf_ops[2 * LPD_MAX_TRANSFORM_OPS];
@@ -221,8 +230,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(&tmem_full, 1);
-        mbar_init(&tmem_empty, 4);
+        mbar_init(&tmem_empty, kEpiWarps);
         mbar_init(&mma_done, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&xchg_full[q], (kEpiSplit - 1) * 32);
         if (kXform) {
             xform_table(a.xt, xf_ops);
             xform_table(a.xr, xf_ops + LPD_MAX_TRANSFORM_OPS);
@@ -308,7 +318,15 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;  // tensor-memory lanes [32 quad, 32 quad + 32)
+        // Warp w reads tensor-memory lanes [32 (w % 4), +32): one row per lane.
+        // The kEpiSplit warps of a quadrant take consecutive kEpiCols-column
+        // ranges of the tile; the others hand their row states to the lead
+        // (split 0) through shared memory, and the lead merges them in column
+        // order, frees the accumulators and writes the tile's partial.  The
+        // lead frees them only after reading the hand-over, so a helper cannot
+        // overwrite it (its next tile needs the next MMA, which needs the free).
+        const int quad = warp & 3;
+        const int split = (warp - 2) >> 2;
         const int row_in_tile = quad * 32 + lane;
         const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0},
             cxr{xf_ops + LPD_MAX_TRANSFORM_OPS, kXform ? a.xr.n_ops : 0};
@@ -326,7 +344,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             Acc2 acc = acc2_init();
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < kBN; c += 16) {
+            for (int c = split * kEpiCols; c < (split + 1) * kEpiCols; c += 16) {
                 f2_t vt[8], vr[8];
                 tmem_ld16(lane_addr + c, vt);
                 tmem_ld16(lane_addr + kBN + c, vr);
@@ -357,12 +375,41 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 }
                 accumulate16(vt, vr, acc);
             }
-            // accumulators drained: the MMA warp may overwrite them
+            Acc r = acc2_fold(acc);
             tc_fence_before();
             __syncwarp();
+            if (split > 0) {
+                // helper: its accumulator reads are done; hand the state over
+                float *x = &xchg[split - 1][0][0];
+                x[0 * kBM + row_in_tile] = r.mt;
+                x[1 * kBM + row_in_tile] = r.st;
+                x[2 * kBM + row_in_tile] = r.dd;
+                x[3 * kBM + row_in_tile] = r.mr;
+                x[4 * kBM + row_in_tile] = r.sr;
+                if (lane == 0) mbar_arrive(&tmem_empty);
+                mbar_arrive(&xchg_full[quad]);
+                continue;
+            }
+            if (kEpiSplit > 1) {
+                const bool got = wait_phase(&xchg_full[quad], local & 1, &abort_flag, a.status);
+                if (__any_sync(0xffffffffu, !got)) break;
+#pragma unroll
+                for (int h = 0; h < kEpiSplit - 1; ++h) {
+                    const float *x = &xchg[h][0][0];
+                    Acc o;
+                    o.mt = x[0 * kBM + row_in_tile];
+                    o.st = x[1 * kBM + row_in_tile];
+                    o.dd = x[2 * kBM + row_in_tile];
+                    o.mr = x[3 * kBM + row_in_tile];
+                    o.sr = x[4 * kBM + row_in_tile];
+                    o.ht = o.hr = 0.f;
+                    merge_acc<false>(r, o);
+                }
+                __syncwarp();
+            }
+            // accumulators drained and hand-over read: the MMA warp may reuse both
             if (lane == 0) mbar_arrive(&tmem_empty);
             if (valid) {
-                const Acc r = acc2_fold(acc);
                 const int64_t o = i * n_n + n;
                 a.part_a[o] = make_float4(r.mt, r.st, r.dd, r.mr);
                 a.part_b[o] = r.sr;

@@ -360,3 +360,29 @@ def test_metrics_from_dlogp_validation(kwargs, code):
     rc = B.lib().lpd_drift_metrics_from_dlogp(a["n"], a["d"], a["m"], a["lo"], a["hi"], a["met"], a["ws"],
                                               a["ws_bytes"], None)
     assert rc == code
+
+
+def _call_host(th=None, rh=None, td=None, rd=None, n_rows=8, vocab=16, ids_dev=FAKE, lo=0.8, ws_bytes=1 << 20):
+    t = B.LpdLogits(FAKE, B.LPD_BF16, 0, 16)
+    th, rh, td, rd = (x if x is not None else t for x in (th, rh, td, rd))
+    copied = ctypes.c_int64(-1)
+    rc = B.lib().lpd_score_host(ctypes.byref(th), ctypes.byref(rh), ctypes.byref(td), ctypes.byref(rd), n_rows,
+                                vocab, FAKE, FAKE, ids_dev, FAKE, lo, 1.2, None, None, None, FAKE, WS_OK, ws_bytes,
+                                ctypes.byref(copied), None)
+    return rc, copied.value
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(td=B.LpdLogits(FAKE, B.LPD_F32, 0, 16)), B.LPD_ERR_BAD_DTYPE),        # device dtype != host dtype
+    (dict(rh=B.LpdLogits(FAKE, B.LPD_F32, 0, 16)), B.LPD_ERR_BAD_DTYPE),
+    (dict(rd=B.LpdLogits(FAKE, B.LPD_BF16, 0, 15)), B.LPD_ERR_BAD_STRIDE),      # staging row shorter than vocab
+    (dict(th=B.LpdLogits(None, B.LPD_BF16, 0, 16)), B.LPD_ERR_NULL_POINTER),
+    (dict(ids_dev=None), B.LPD_ERR_NULL_POINTER),
+    (dict(lo=2.0), B.LPD_ERR_BAD_CLIP),
+    (dict(ws_bytes=16), B.LPD_ERR_WORKSPACE),
+    (dict(n_rows=-1), B.LPD_ERR_BAD_SIZE),
+])
+def test_score_host_rejects_invalid_arguments(kwargs, code):
+    rc, copied = _call_host(**kwargs)
+    assert rc == code
+    assert copied == 0  # nothing was copied
