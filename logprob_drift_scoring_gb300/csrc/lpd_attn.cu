@@ -48,7 +48,9 @@ struct MergeArgs {
     int n_parts;
     int nr_max;              // bound on the rows one block touches
     int base2;
+    int row_in_warp;         // upr divides 32: a row's units are lanes of one warp
     uint8_t order_a[kMaxParts], order_b[kMaxParts];
+    uint8_t slot_b[kSmallParts];  // staging slot (order-A visit position) of order B's k-th part
     int64_t off_a[kSmallParts];  // order_a[k] * part_bytes for the first parts
 };
 
@@ -177,9 +179,11 @@ __device__ __forceinline__ void fold(const MergeArgs &a, const Staged<kV, kMaxK>
     fold_finish(f, want_lse, a.base2, o, lse);
 }
 
-// The plain merge of up to kSmallParts parts: the row's lse values sit in
-// registers in visiting order and chunk k of the visit is staged in slot k.
-template <bool kBf16>
+// Merges of up to kSmallParts parts with one chunk per thread: the row's lse
+// values sit in registers in visiting order and chunk k of order A's visit is
+// staged in slot k.  Order A folds slot k at step k; order B (the drift
+// form's second fold) folds slot slot_b[k], a kernel parameter.
+template <bool kBf16, bool kB>
 __device__ __forceinline__ void fold_seq(const MergeArgs &a, const float (&l)[kSmallParts], const uint4 *chunk_s,
                                          int t, float cvt, bool want_lse, float *o, float &lse) {
     constexpr int E = kBf16 ? 8 : 4;
@@ -189,7 +193,7 @@ __device__ __forceinline__ void fold_seq(const MergeArgs &a, const float (&l)[kS
     for (int k = 0; k < kSmallParts; ++k) {
         if (l[k] == -CUDART_INF_F) continue;  // also every k >= K
         float v[E];
-        unpack<kBf16>(chunk_s[k * kMergeThreads + t], v);
+        unpack<kBf16>(chunk_s[(kB ? a.slot_b[k] : k) * kMergeThreads + t], v);
         fold_step(f, l[k], v, cvt);
     }
     fold_finish(f, want_lse, a.base2, o, lse);
@@ -233,8 +237,8 @@ __device__ __forceinline__ void stage_lse(const MergeArgs &a, const Tile &g, flo
 template <bool kBf16, bool kDrift, int kV, int kMaxK>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeArgs a) {
     constexpr int E = kBf16 ? 8 : 4;
-    // plain merge of few parts: visiting order fixed per launch, one chunk per thread
-    constexpr bool kSeq = !kDrift && kMaxK <= kSmallParts && kV == 1;
+    // few parts, one chunk per thread: visiting orders fixed per launch, lse in registers
+    constexpr bool kSeq = kMaxK <= kSmallParts && kV == 1;
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = a.n_parts;
     const int lse_stride = a.nr_max * kMaxK;
@@ -268,11 +272,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         const int rl = static_cast<int>(row - g.r0);
         // a part with lse = -inf saw no keys for this row: its chunks are never copied
         const char *src = a.parts + static_cast<int64_t>(u) * (16 * kV);
-        float lseq[kSmallParts];  // kSeq: the row's lse in visiting order
+        float lseq[kSmallParts], lseq_b[kSmallParts];  // kSeq: the row's lse in each visiting order
         if constexpr (kSeq) {
 #pragma unroll
             for (int k = 0; k < kSmallParts; ++k) {
                 lseq[k] = (live && k < K) ? lcur[rl * kMaxK + a.order_a[k]] : -CUDART_INF_F;
+                if (kDrift) lseq_b[k] = (live && k < K) ? lcur[rl * kMaxK + a.order_b[k]] : -CUDART_INF_F;
                 if (lseq[k] != -CUDART_INF_F) cp_async16(chunk_s + k * kMergeThreads + t, src + a.off_a[k]);
             }
         } else if (live) {
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
             gn = tile_at(a, next);
             stage_lse<kMaxK>(a, gn, lse_s + (buf ^ 1) * lse_stride, t, K);
         }
-        if (kDrift)
+        if (kDrift && !a.row_in_warp)
             for (int i = t; i < g.nr; i += kMergeThreads) rowmax_s[i] = 0u;
         cp_async_wait_all();
         __syncthreads();  // the next tile's lse and the zeroed row maxima are visible
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         float oa[kV * E], la = 0.f;
         if (live) {
             if constexpr (kSeq)
-                fold_seq<kBf16>(a, lseq, chunk_s, t, cvt, head, oa, la);
+                fold_seq<kBf16, false>(a, lseq, chunk_s, t, cvt, head, oa, la);
             else
                 fold<kBf16, kV, kMaxK, false>(a, st, K, t, rl, cvt, head, oa, la);
             float4 *dst = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(u) * (kV * E));
@@ -313,20 +318,34 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
             if (head) a.out_lse[row] = la;
         }
         if constexpr (kDrift) {
+            float dmax = 0.f;
             if (live) {
                 float ob[kV * E], lb;
-                fold<kBf16, kV, kMaxK, true>(a, st, K, t, rl, cvt, head, ob, lb);
-                float dmax = 0.f;
+                if constexpr (kSeq)
+                    fold_seq<kBf16, true>(a, lseq_b, chunk_s, t, cvt, head, ob, lb);
+                else
+                    fold<kBf16, kV, kMaxK, true>(a, st, K, t, rl, cvt, head, ob, lb);
 #pragma unroll
                 for (int e = 0; e < kV * E; ++e) {
                     const float d = oa[e] == ob[e] ? 0.f : fabsf(__fsub_rn(oa[e], ob[e]));
                     dmax = (d > dmax || d != d) ? d : dmax;  // NaN wins
                 }
-                atomicMax(rowmax_s + rl, __float_as_uint(dmax));
                 if (head) a.row_dlse[row] = la == lb ? 0.f : fabsf(__fsub_rn(la, lb));
             }
-            __syncthreads();
-            for (int i = t; i < g.nr; i += kMergeThreads) atomicMax(a.row_dout + g.r0 + i, rowmax_s[i]);
+            if (a.row_in_warp) {
+                // the row's units are the aligned group of upr lanes: reduce
+                // there (float bits of non-negative values and NaN order like
+                // the numbers, NaN above all) and let the row's first lane write
+                for (uint32_t off = 1; off < a.upr; off <<= 1) {
+                    const float o = __shfl_xor_sync(0xffffffffu, dmax, off);
+                    dmax = (o > dmax || o != o) ? o : dmax;
+                }
+                if (head) a.row_dout[row] = __float_as_uint(dmax);
+            } else {
+                if (live) atomicMax(rowmax_s + rl, __float_as_uint(dmax));
+                __syncthreads();
+                for (int i = t; i < g.nr; i += kMergeThreads) atomicMax(a.row_dout + g.r0 + i, rowmax_s[i]);
+            }
         }
         if (!more) break;
         __syncthreads();  // every thread is done with this tile's lse buffer before it is refilled
@@ -420,9 +439,7 @@ cudaError_t launch_merge(const MergeArgs &a, size_t smem, cudaStream_t stream) {
 
 template <bool kBf16, bool kDrift>
 cudaError_t launch_merge_shape(const MergeArgs &a, int kv, size_t smem, cudaStream_t stream) {
-    if (a.n_parts <= kSmallParts)
-        return kv == 2 ? launch_merge<kBf16, kDrift, 2, kSmallParts>(a, smem, stream)
-                       : launch_merge<kBf16, kDrift, 1, kSmallParts>(a, smem, stream);
+    if (a.n_parts <= kSmallParts) return launch_merge<kBf16, kDrift, 1, kSmallParts>(a, smem, stream);  // kv is 1
     return kv == 2 ? launch_merge<kBf16, kDrift, 2, kMaxParts>(a, smem, stream)
                    : launch_merge<kBf16, kDrift, 1, kMaxParts>(a, smem, stream);
 }
@@ -450,14 +467,18 @@ cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream) {
     const int es = c.bf16 ? 2 : 4;
     const int cpr = static_cast<int>(static_cast<int64_t>(c.head_dim) * es / 16);
     const bool drift = c.diag;
+    const int kv = merge_kv(c.n_parts, cpr);
+    const int upr = cpr / kv;
+    // a row's units fill an aligned group of lanes: its drift maximum is a
+    // warp reduction written once, otherwise atomics into zeroed memory
+    const bool row_in_warp = upr <= 32 && 32 % upr == 0;
     if (drift) {
         cudaError_t e = cudaMemsetAsync(c.drift, 0, sizeof(lpd_merge_drift), stream);
-        if (e == cudaSuccess && c.n_rows > 0) e = cudaMemsetAsync(c.row_dout, 0, c.n_rows * sizeof(float), stream);
+        if (e == cudaSuccess && c.n_rows > 0 && !row_in_warp)
+            e = cudaMemsetAsync(c.row_dout, 0, c.n_rows * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
     if (c.n_rows > 0) {
-        const int kv = merge_kv(c.n_parts, cpr);
-        const int upr = cpr / kv;
         MergeArgs a{};
         a.parts = static_cast<const char *>(c.parts);
         a.lse = c.lse;
@@ -473,11 +494,15 @@ cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream) {
         a.n_parts = c.n_parts;
         a.nr_max = kMergeThreads / upr + 2;
         a.base2 = c.base2;
+        a.row_in_warp = row_in_warp ? 1 : 0;
+        int pos_a[kMaxParts] = {};
         for (int k = 0; k < c.n_parts; ++k) {
             a.order_a[k] = static_cast<uint8_t>(c.order_a[k]);
             a.order_b[k] = static_cast<uint8_t>(drift ? c.order_b[k] : c.order_a[k]);
+            pos_a[c.order_a[k]] = k;
             if (k < kSmallParts) a.off_a[k] = static_cast<int64_t>(c.order_a[k]) * a.part_bytes;
         }
+        for (int k = 0; k < c.n_parts && k < kSmallParts; ++k) a.slot_b[k] = static_cast<uint8_t>(pos_a[a.order_b[k]]);
         const size_t smem = attn_merge_smem(c.n_parts, cpr);
         cudaError_t e;
         if (c.bf16)

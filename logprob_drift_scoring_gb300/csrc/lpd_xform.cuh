@@ -28,9 +28,10 @@ __device__ __forceinline__ void xform_table(const Xform &c, float4 *ops) {
 // values, so tanh has to stay at the level of fp32 rounding (the hardware
 // tanh.approx, about 2^-11 relative, does not).  Own tanh, from its series
 // and its exponential form, with y = x / p and z = y^2:
-//   z < 0.36:   p tanh(y) = x (1 + z P(z)), P of degree 5 fitted to
-//               (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: tanh within 0.70 ulp
-//               in float32 Horner evaluation); p y is written as x itself;
+//   z < 0.36:   p tanh(y) = x (1 + z P(z)), P of degree 4 fitted to
+//               (tanh(y)/y - 1)/z (csrc/tanh_coeffs.py: tanh within 0.63 ulp
+//               in float32 Horner evaluation; degree 5 gained nothing, the
+//               final rounding dominates); p y is written as x itself;
 //   otherwise:  p tanh(y) = p sign(y) (1 - 2 / (1 + 2^(2|y| log2 e))), with
 //               ex2.approx and rcp.approx (a few ulp where |y| >= 0.6,
 //               exactly +-p once the power overflows; NaN stays NaN).
@@ -38,9 +39,10 @@ __device__ __forceinline__ void xform_table(const Xform &c, float4 *ops) {
 // the packed path rounds each half like the scalar one, so a column's value
 // does not depend on which load path or lane handled it.
 constexpr float kTanhZMax = 0.36f;
+constexpr int kTanhDegree = 4;
 __host__ __device__ constexpr float tanh_c(int k) {
-    return k == 0 ? -3.333333135e-01f : k == 1 ? 1.333319992e-01f : k == 2 ? -5.394675583e-02f
-         : k == 3 ? 2.170414850e-02f : k == 4 ? -8.193124086e-03f : 2.163204830e-03f;
+    return k == 0 ? -3.333327174e-01f : k == 1 ? 1.333131194e-01f : k == 2 ? -5.373601243e-02f
+         : k == 3 ? 2.064501122e-02f : -5.728444550e-03f;
 }
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -51,9 +53,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 // z P(z)
 __device__ __forceinline__ float tanh_q(float z) {
-    float p = tanh_c(5);
+    float p = tanh_c(kTanhDegree);
 #pragma unroll
-    for (int k = 4; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
+    for (int k = kTanhDegree - 1; k >= 0; --k) p = __fmaf_rn(p, z, tanh_c(k));
     return __fmul_rn(z, p);
 }
 
@@ -82,9 +84,9 @@ __device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
     f2_t o[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        f2_t pp = f2(tanh_c(5), tanh_c(5));
+        f2_t pp = f2(tanh_c(kTanhDegree), tanh_c(kTanhDegree));
 #pragma unroll
-        for (int k = 4; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
+        for (int k = kTanhDegree - 1; k >= 0; --k) pp = fma2(pp, z[q], f2(tanh_c(k), tanh_c(k)));
         o[q] = fma2(v[q], mul2(z[q], pp), v[q]);
     }
     if (__any_sync(0xffffffffu, !(zmax < kTanhZMax))) {
