@@ -74,6 +74,13 @@ CASES = {
     "f32_unaligned_generic": (100, 4097, torch.float32, torch.float32, {}),
     "f32_vocab5_padded_tma_tail": (90, 5, torch.float32, torch.float32, dict(row_pad=3)),
     "bf16_vocab7_padded_tma_tail": (40, 7, torch.bfloat16, torch.bfloat16, dict(row_pad=1)),
+    # past 2^22 columns: column indices and byte offsets well beyond 32-bit
+    # products of the per-tile arithmetic; ids near both ends come from the
+    # uniform draw plus the spikes
+    "huge_vocab_mixed": (6, (1 << 22) + 123, torch.bfloat16, torch.float32, dict(spike_frac=0.5)),
+    # 300 000 rows: many grid-stride passes per CTA and a percentile select
+    # over ~270 000 keys
+    "many_rows_vocab16": (300_000, 16, torch.bfloat16, torch.bfloat16, {}),
 }
 
 
@@ -290,6 +297,10 @@ def _small_sharded(bounds, rows=120, seed=20):
     [(0, 4096), (4096, 8192), (8192, 12288), (12288, 16384)],
     [(0, 1000), (1000, 9000), (9000, 9001), (9001, 12000)],
     [(0, 5000)],
+    # the maximum of 16 shards, uneven, one of a single column
+    [(a, b) for a, b in zip([0, 700, 701, 2000, 2100, 4097, 5000, 6000, 6001, 7000, 8192, 9000, 10001, 11000, 12000,
+                             13000], [700, 701, 2000, 2100, 4097, 5000, 6000, 6001, 7000, 8192, 9000, 10001, 11000,
+                                      12000, 13000, 14001])],
 ])
 def test_sharded_vs_oracle(bounds):
     base, w = _small_sharded(bounds)
