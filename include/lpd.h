@@ -32,10 +32,12 @@
  * floating-point atomics are used anywhere.
  *
  * Memory: the caller owns every buffer.  Logits, ids, mask, per-token outputs,
- * the metrics record and the workspace are DEVICE pointers; nothing is
- * allocated or retained by the library between calls.  All calls are
- * asynchronous on the given stream (a cudaStream_t passed as void*, NULL for
- * the legacy default stream) and may be captured in a CUDA graph.
+ * the metrics record and the workspace are DEVICE pointers (lpd_score_host
+ * alone takes its logits, ids and mask in host memory); nothing is allocated
+ * or retained by the library between calls.  All calls are asynchronous on
+ * the given stream (a cudaStream_t passed as void*, NULL for the legacy
+ * default stream) and, all but lpd_score_host, may be captured in a CUDA
+ * graph.
  *
  * Errors: invalid arguments are detected on the host before anything is
  * launched and returned as a negative LPD_ERR_* code.  Problems that only the
@@ -502,7 +504,7 @@ int lpd_attn_merge_order_drift(const void *out_parts, int32_t parts_dtype, const
 /* ---- scoring without a caller-provided workspace -------------------------- */
 
 /* Largest n_rows lpd_score_noalloc accepts: its built-in scratch is sized for
- * this many rows (about 17.7 MB of device memory per GPU that loads the
+ * this many rows (about 21.9 MB of device memory per GPU that loads the
  * library, held until the process exits). */
 #define LPD_NOALLOC_MAX_ROWS 32768
 

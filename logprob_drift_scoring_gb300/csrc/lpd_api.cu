@@ -157,6 +157,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     if (rc) return rc;
     FinArgs f{};
     f.n_seg = n_seg;
+    f.n_warps = row_warps(mode);
     f.n_perm = n_perm;
     for (int j = 0; j < n_perm; ++j) f.perm[j] = static_cast<int8_t>(perm[j]);
     f.vocab = vocab;

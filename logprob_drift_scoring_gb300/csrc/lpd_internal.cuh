@@ -11,21 +11,23 @@
 namespace lpd {
 
 // ---------------------------------------------------------------- geometry
-// The streaming row kernel runs one CTA per SM: 16 consumer warps plus one
-// producer warp.  A tile is 8192 logical columns of one vocab segment, read as
-// four groups of 2048; consumer thread t owns columns [2048 g + 4t, 2048 g + 4t
-// + 4) of group g = 0..3 of every tile (16 columns per thread per tile).
-// These constants fix each row's arithmetic order, so they are part of the
-// batch-invariance contract: changing them changes results (bitwise), but never
-// makes them depend on the batch.
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;  // 512
-constexpr int kRowThreads = kConsumers + 32;     // + producer warp
+// The streaming row kernel runs one CTA per SM: W consumer warps plus one
+// producer warp.  A tile is 16 * 32 W logical columns of one vocab segment,
+// read as four groups of G = 4 * 32 W; consumer thread t owns columns
+// [G g + 4t, G g + 4t + 4) of group g = 0..3 of every tile (16 columns per
+// thread per tile).  W is 20 (tiles of 10240 columns) in every mode but the
+// general transform chain, whose tanh code needs more registers than 21 warps
+// leave (the register file allows 80 a thread at up to 6 warps per scheduler)
+// and which keeps W = 16 (8192 columns).  These constants fix each row's
+// arithmetic order, so they are part of the batch-invariance contract:
+// changing them changes results (bitwise), but never makes them depend on the
+// batch.
+constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3;
+__host__ __device__ constexpr int row_warps(int mode) { return mode == kRowTransform ? 16 : 20; }
+constexpr int kConsumerWarps = 20;               // the largest W: the workspace's warp-state stride
 constexpr int kColsPerThread = 16;
-constexpr int kGroupCols = 4 * kConsumers;       // 2048
-constexpr int kTile = kColsPerThread * kConsumers;  // 8192 columns
 constexpr int kMaxSegments = 16;                 // shards per side
-constexpr int kRingBytes = 192 * 1024;           // shared-memory staging ring
+constexpr int kRingBytes = 200 * 1024;           // shared-memory staging ring
 constexpr int kFinThreads = 256;                 // rows per finalise block
 constexpr int kSelThreads = 1024;
 
@@ -102,6 +104,7 @@ struct RowArgs {
 
 struct FinArgs {
     int n_seg;
+    int n_warps;                   // warp states per (row, segment): row_warps of the pass's mode
     int n_perm;                    // 0: no merge-order diagnostic
     int8_t perm[kMaxSegments];
     int topo;                      // LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE or LPD_TOPO_ALLREDUCE_PARTIALS
@@ -151,7 +154,6 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lt, float *out_lr, float *out_d,
                                  lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
                                  cudaStream_t stream);
-constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3;
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
 cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader *hdr, const int2 *rowid,

@@ -151,7 +151,7 @@ __device__ __forceinline__ void block_tree(Part *sh) {
     }
 }
 
-// One thread per active row: merge the 16 warp states of each segment, then
+// One thread per active row: merge the warp states of each segment, then
 // the segments in vocab order (and optionally in a given permutation), then
 // the per-row arithmetic in fp64:
 //   lse = m + log(s),  logp = x[id] - lse,
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_cons
             Acc sk = acc_init();
             const float4 *pw = a.part + (i * a.n_seg + k) * kConsumerWarps * 2;
 #pragma unroll 4
-            for (int w = 0; w < kConsumerWarps; ++w) {
+            for (int w = 0; w < a.n_warps; ++w) {
                 const float4 p0 = pw[2 * w], p1 = pw[2 * w + 1];
                 Acc o;
                 o.mt = p0.x;

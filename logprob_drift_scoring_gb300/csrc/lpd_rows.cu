@@ -10,14 +10,16 @@
 // Layout of the work.  One persistent CTA per SM takes active rows i =
 // blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams each row
 // through a ring of shared-memory stages with 1-D bulk copies (TMA,
-// cp.async.bulk, completion on an mbarrier); every stage holds the same 8192
-// columns of both sides.  16 consumer warps read the stage, and thread t owns
-// columns [2048 g + 4t, 2048 g + 4t + 4), g = 0..3, of every tile.  Each thread
-// keeps an online (max, sum exp) pair per side in fp32 plus the sum of the two
-// sides' term differences; at the end of a segment each warp reduces its 32
-// states (both maxima first, then the rescaled sums in a fixed xor butterfly)
-// and writes one state to the workspace.  The finalise kernel merges the 16
-// warp states and the segments and does the fp64 row arithmetic.
+// cp.async.bulk, completion on an mbarrier); every stage holds the same tile of
+// 16 * 32 W columns of both sides (W = row_warps(mode) consumer warps: 20, so
+// 10240 columns, or 16 for the general transform chain).  The W warps read the
+// stage, and thread t owns columns [G g + 4t, G g + 4t + 4), g = 0..3, G =
+// 128 W, of every tile.  Each thread keeps an online (max, sum exp) pair per
+// side in fp32 plus the sum of the two sides' term differences; at the end of
+// a segment each warp reduces its 32 states (both maxima first, then the
+// rescaled sums in a fixed xor butterfly) and writes one state to the
+// workspace.  The finalise kernel merges the W warp states and the segments
+// and does the fp64 row arithmetic.
 //
 // Batch invariance ("Attention Debug Matrix", section "Metrics": the
 // batch-composition control must be bitwise zero): the value that reaches a
@@ -144,8 +146,9 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
 // is copied into registers once per thread (constant indices only, so it never
 // lives in local memory); ops past n are skipped.  Only real columns are
 // transformed; masked tail columns stay -inf.
-// Column of slot q (0..15) of consumer thread t within a tile.
-__device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroupCols + 4 * t + (q & 3); }
+// Column of slot q (0..15) of consumer thread t within a tile of groups of kGroup columns.
+template <int kGroup>
+__device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroup + 4 * t + (q & 3); }
 
 // ---- the arithmetic: accumulate16 and the packed state live in lpd_acc.cuh ----
 
@@ -160,10 +163,14 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
 // 3 with a scale-only chain (each side's product of scales folded into its
 // exponent factor, so no tanh code and no extra arithmetic per element).
 template <class DT, class DR, bool kTma, int kMode>
-__global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
-    constexpr bool kXform = kMode == 1;
-    constexpr bool kEntropy = kMode == 2;
-    constexpr bool kScale = kMode == 3;
+__global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
+    row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
+    constexpr bool kXform = kMode == kRowTransform;
+    constexpr bool kEntropy = kMode == kRowEntropy;
+    constexpr bool kScale = kMode == kRowScale;
+    constexpr int kWarps = row_warps(kMode);
+    constexpr int kGroupCols = 4 * 32 * kWarps;
+    constexpr int kTile = kColsPerThread * 32 * kWarps;
     extern __shared__ __align__(1024) char smem[];
     __shared__ int abort_flag;
     __shared__ float4 xf_ops[kXform ? 2 * LPD_MAX_TRANSFORM_OPS : 1];
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
         if (kTma) {
             for (int s = 0; s < n_stages; ++s) {
                 mbar_init(&full[s], 1);
-                mbar_init(&empty[s], kConsumerWarps);
+                mbar_init(&empty[s], kWarps);
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp == kWarps) {
         // ------------------------------------------------------ producer
         if (!kTma || lane != 0) return;
         uint64_t policy;
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                         }
 #pragma unroll
                         for (int p = 0; p < 8; ++p) {
-                            const int col0 = slot_col(t, 2 * p);  // the pair is col0, col0 + 1
+                            const int col0 = slot_col<kGroupCols>(t, 2 * p);  // the pair is col0, col0 + 1
                             if (col0 >= nv) {
                                 vt[p] = vr[p] = f2(-INFINITY, -INFINITY);  // wholly past the segment
                             } else if (col0 + 1 >= min(nbt, nbr)) {
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
                         float x[2], y[2];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const int col = slot_col(t, 2 * p + h);
+                            const int col = slot_col<kGroupCols>(t, 2 * p + h);
                             x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                             y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
                             if (kXform && col < nv) {
@@ -367,7 +374,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) row_kernel(const __grid_consta
 
 template <class DT, class DR, bool kTma, int kMode>
 cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
-    const int stage_bytes = kTile * (DT::kBytes + DR::kBytes);
+    constexpr int kThreads = row_warps(kMode) * 32 + 32;  // + producer warp
+    const int stage_bytes = kColsPerThread * 32 * row_warps(kMode) * (DT::kBytes + DR::kBytes);
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
     auto kern = row_kernel<DT, DR, kTma, kMode>;
@@ -380,7 +388,7 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<device_sm_count(), kRowThreads, smem, stream>>>(a, n_stages);
+    kern<<<device_sm_count(), kThreads, smem, stream>>>(a, n_stages);
     return cudaGetLastError();
 }
 
