@@ -13,13 +13,16 @@
 namespace lpd {
 
 int device_sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -417,11 +417,9 @@ __global__ void drift_finalize_kernel(lpd_merge_drift *d, int64_t n) {
 template <bool kBf16, bool kDrift, int kV, int kMaxK>
 cudaError_t launch_merge(const MergeArgs &a, size_t smem, cudaStream_t stream) {
     auto *fn = merge_kernel<kBf16, kDrift, kV, kMaxK>;
+    static std::atomic<uint64_t> raised{0};
     cudaError_t e;
-    if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
-            cudaSuccess)
-        return e;
+    if (smem > 48 * 1024 && (e = set_smem_max_once(fn, raised)) != cudaSuccess) return e;
     const int64_t tiles = (static_cast<int64_t>(a.units) + kMergeThreads - 1) / kMergeThreads;
     int64_t grid = tiles;
     if (!kDrift) {

@@ -604,18 +604,10 @@ cudaError_t launch_fused(const FusedCall &c, cudaStream_t stream) {
     a.xr = c.xr;
     const bool xf = c.xt.n_ops > 0 || c.xr.n_ops > 0;
     const size_t smem = static_cast<size_t>(kStages) * kStage + 1024;
-    static int configured_device = -1;
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(head_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(head_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
+    static std::atomic<uint64_t> configured_plain{0}, configured_xform{0};
+    if ((e = xf ? set_smem_once(head_kernel<true>, smem, configured_xform)
+                : set_smem_once(head_kernel<false>, smem, configured_plain)) != cudaSuccess)
+        return e;
     if (xf)
         head_kernel<true><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
     else

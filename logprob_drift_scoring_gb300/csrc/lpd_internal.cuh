@@ -2,6 +2,8 @@
 // Nothing here is part of the public interface (include/lpd.h).
 #pragma once
 
+#include <atomic>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -32,6 +34,34 @@ constexpr int kFinThreads = 256;                 // rows per finalise block
 constexpr int kSelThreads = 1024;
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Sets a kernel's dynamic shared-memory limit once per device.  `done` holds
+// one bit per device id below 64 (the attribute is per device); concurrent
+// first calls may both set it, which is harmless.
+template <class Kernel>
+cudaError_t set_smem_once(Kernel *kern, size_t smem, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// The same with the device's opt-in maximum, for kernels whose shared memory
+// per launch depends on the call: the limit never has to move between calls
+// (a lower value set by one host thread could fail another's launch).
+template <class Kernel>
+cudaError_t set_smem_max_once(Kernel *kern, std::atomic<uint64_t> &done) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && (done.load(std::memory_order_acquire) & (uint64_t{1} << dev))) return cudaSuccess;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    return set_smem_once(kern, static_cast<size_t>(optin), done);
+}
 
 // ---------------------------------------------------------------- workspace
 // Device workspace carved into fixed regions; every region 256-byte aligned.

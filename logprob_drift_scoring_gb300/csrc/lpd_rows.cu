@@ -379,15 +379,9 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
     auto kern = row_kernel<DT, DR, kTma, kMode>;
-    static int configured_device = -1;  // attribute is per device; cheap to repeat
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = set_smem_once(kern, smem, configured);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
     kern<<<device_sm_count(), kThreads, smem, stream>>>(a, n_stages);
     return cudaGetLastError();
 }
