@@ -199,3 +199,20 @@ def test_fused_empty_chains_are_the_plain_kernel():
     torch.cuda.synchronize()
     for a, b in ((plain.logp_train, ident.logp_train), (plain.dlogp, ident.dlogp)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_full_size_fused_transform_sampled_rows():
+    w = W.fused(device=DEV)
+    ops = [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]
+    res = B.score_fused(w.hidden_train, w.hidden_rollout, w.weight, w.token_ids, w.action_mask, w.clip,
+                        train_ops=ops, rollout_ops=ops)
+    torch.cuda.synchronize()
+    assert res.metrics["status"] == 0 and res.metrics["n_active"] == w.n_rows
+    rows = np.array([0, 127, 128, 16383])
+    sel = torch.as_tensor(rows, device=DEV)
+    sub = W.HeadWorkload("sub", w.hidden_train[sel], w.hidden_rollout[sel], w.weight, w.token_ids[sel],
+                         w.action_mask[sel])
+    ref = oracle_rows_transformed(sub, np.arange(rows.size), ops, ops)
+    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout), (res.dlogp, ref.dlogp)):
+        assert np.max(np.abs(got[sel].cpu().numpy().astype(np.float64) - want)) <= LOGP_ATOL

@@ -130,3 +130,27 @@ def test_softcap_load_paths_agree_bitwise():
     for a, b in ((aligned.logp_train, generic.logp_train), (aligned.logp_rollout, generic.logp_rollout),
                  (aligned.dlogp, generic.dlogp)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("ops", [[(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SCALE, 1 / 0.7)]])
+def test_full_size_transform_sampled_rows(ops):
+    """The Qwen workload with the chains the benchmark times (soft-cap then
+    temperature on the general path, temperature alone on the scale-only
+    path); sampled active rows against the oracle, and the metrics equal to
+    the oracle's metric function on the pass's own per-token values."""
+    w = W.qwen(device=DEV)
+    res = B.score(w.train, w.rollout, w.token_ids, w.action_mask, w.clip, train_ops=ops, rollout_ops=ops)
+    torch.cuda.synchronize()
+    assert res.metrics["status"] == 0
+    mask = w.action_mask.cpu().numpy()
+    rows = np.sort(np.random.default_rng(23).choice(np.flatnonzero(mask), size=48, replace=False))
+    sel = torch.as_tensor(rows, device=DEV)
+    ref = oracle.score_transformed(to_oracle(w.train[sel]), to_oracle(w.rollout[sel]), w.token_ids.cpu().numpy()[rows],
+                                   np.ones(rows.size, np.uint8), ops, ops, *w.clip)
+    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout), (res.dlogp, ref.dlogp)):
+        assert np.max(np.abs(got[sel].cpu().numpy().astype(np.float64) - want)) <= LOGP_ATOL
+    d = res.dlogp.cpu().numpy().astype(np.float64)
+    prop = oracle.metrics(d, mask, *w.clip)
+    prop["status"] = 0
+    assert_metrics_match(res.metrics, prop, d, mask, w.clip, ambiguity=1e-6)
