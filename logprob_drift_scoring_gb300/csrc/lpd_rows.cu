@@ -150,6 +150,14 @@ __device__ __forceinline__ void lds4<F32>(const char *stage, int col, f2_t *v) {
 template <int kGroup>
 __device__ __forceinline__ int slot_col(int t, int q) { return (q >> 2) * kGroup + 4 * t + (q & 3); }
 
+// Tile kinds for the tile body: known full, known ragged (the segment's last,
+// shorter tile), or decided at run time from the tile's width.
+enum TileKind { kTileFull, kTileRagged, kTileAny };
+template <int K>
+struct TileTag {
+    static constexpr int kind = K;
+};
+
 // ---- the arithmetic: accumulate16 and the packed state live in lpd_acc.cuh ----
 
 __device__ __forceinline__ float select16(const f2_t *v, int q) {
@@ -280,17 +288,18 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
             const char *tb = sg.t + r * sg.t_stride;
             const char *rb = sg.r + r * sg.r_stride;
             Acc2 acc2 = acc2_init();
-            for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
-                const int nv = static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
+            auto tile = [&](const int64_t c0, auto tag) -> bool {
+                constexpr int kKind = decltype(tag)::kind;
+                const int nv = kKind == kTileFull ? kTile : static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
                 f2_t vt[8], vr[8];  // slots (2p, 2p+1) in pair p
                 if (kTma) {
                     const uint32_t stage = it % n_stages, round = it / n_stages;
                     // the whole warp leaves together if any lane gave up, so no
                     // lane is left behind at a warp-synchronous instruction
                     const bool ok = wait_phase(&full[stage], round & 1, &abort_flag, a.status);
-                    if (__any_sync(0xffffffffu, !ok)) return;
+                    if (__any_sync(0xffffffffu, !ok)) return false;
                     const char *stg = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
-                    if (nv == kTile) {
+                    if (kKind == kTileFull || (kKind == kTileAny && nv == kTile)) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
@@ -361,6 +370,18 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
                     a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
                 accumulate16<kEntropy>(vt, vr, acc2, lg_t, lg_r);
+                return true;
+            };
+            if constexpr (kXform) {
+                // the transform chain's larger body: full tiles in a tight loop,
+                // the segment's ragged last tile after it (measured faster)
+                int64_t c0 = 0;
+                for (; c0 + kTile <= sg.len; c0 += kTile)
+                    if (!tile(c0, TileTag<kTileFull>{})) return;
+                if (c0 < sg.len && !tile(c0, TileTag<kTileRagged>{})) return;
+            } else {
+                for (int64_t c0 = 0; c0 < sg.len; c0 += kTile)
+                    if (!tile(c0, TileTag<kTileAny>{})) return;
             }
             const Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2), lg_t, lg_r);
             if (lane == 0) {
