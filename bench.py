@@ -723,14 +723,21 @@ def run_e2e(w, args, world: int = 1):
     from logprob_drift_scoring_gb300 import binding as B
 
     dev = w.token_ids.device
-    host = []
+    host, bufs = [], []
     pinned = True
+    host_memory = "lpd_host_alloc (huge-page advised, registered)"
     for t in (w.train, w.rollout, w.token_ids, w.action_mask):
         try:
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            hb = B.HostBuffer(t.shape, t.dtype)
+            bufs.append(hb)
+            h = hb.tensor
         except RuntimeError:
-            h = torch.empty(t.shape, dtype=t.dtype)
-            pinned = False
+            host_memory = "cudaHostAlloc"
+            try:
+                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            except RuntimeError:
+                h = torch.empty(t.shape, dtype=t.dtype)
+                pinned = False
         h.copy_(t)
         host.append(h)
     dbuf = [torch.empty_like(t) for t in (w.train, w.rollout, w.token_ids, w.action_mask)]
@@ -758,11 +765,14 @@ def run_e2e(w, args, world: int = 1):
     torch.cuda.synchronize()
     ms = barrier_max(s.elapsed_time(e) / steps, world)
     del dbuf, host
+    for hb in bufs:
+        hb.free()
     torch.cuda.empty_cache()
     assert len(set(copied)) == 1  # the same rows every step
     return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": copied[0],
             "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ms, 3), "pinned": pinned,
-            "steps": steps, "copies": "active rows of both sides (one 2-D copy per run of active rows), ids, mask"}
+            "steps": steps, "copies": "active rows of both sides (one 2-D copy per run of active rows), ids, mask",
+            "host_memory": host_memory}
 
 
 # ---------------------------------------------------------------- reference arm
