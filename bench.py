@@ -757,20 +757,25 @@ def run_e2e(w, args, world: int = 1):
         one()
     torch.cuda.synchronize()
     steps = args.e2e_steps
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
+    # one event between steps as well, so single slow steps (a stalled host
+    # copy) show up next to the mean
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for k in range(steps):
         one()
-    e.record()
+        ev[k + 1].record()
     torch.cuda.synchronize()
-    ms = barrier_max(s.elapsed_time(e) / steps, world)
+    per_step = sorted(ev[k].elapsed_time(ev[k + 1]) for k in range(steps))
+    ms = barrier_max(ev[0].elapsed_time(ev[steps]) / steps, world)
     del dbuf, host
     for hb in bufs:
         hb.free()
     torch.cuda.empty_cache()
     assert len(set(copied)) == 1  # the same rows every step
     return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": copied[0],
-            "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ms, 3), "pinned": pinned,
+            "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ms, 3),
+            "ms_per_step_median": round(per_step[len(per_step) // 2], 3), "ms_per_step_max": round(per_step[-1], 3),
+            "pinned": pinned,
             "steps": steps, "copies": "active rows of both sides (one 2-D copy per run of active rows), ids, mask",
             "host_memory": host_memory}
 
