@@ -398,3 +398,54 @@ def test_host_alloc_without_a_gpu_fails_cleanly():
     assert B.lib().lpd_host_free(None, 0) == B.LPD_ERR_NULL_POINTER
     with pytest.raises(RuntimeError):
         B.HostBuffer((4, 4), torch.float32)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "lpd.h"
+
+int main(void) {
+    lpd_backend_info_t info;
+    lpd_logits t;
+    lpd_metrics *met = (lpd_metrics *)0x1000;
+    int rc;
+    if (lpd_backend_info(&info) != LPD_OK || strcmp(info.backend_id, "lpd.sm103a.v1") != 0) return 1;
+    if (lpd_backend_info(NULL) != LPD_ERR_NULL_POINTER) return 2;
+    if (lpd_workspace_size(LPD_KIND_SCORE, 1000, 0, 0) == 0) return 3;
+    memset(&t, 0, sizeof t);
+    t.dtype = LPD_BF16;
+    t.row_stride = 10;
+    /* vocab 11 > row_stride 10: refused on the host, nothing launched */
+    rc = lpd_score(&t, &t, 4, 11, NULL, NULL, 0.8, 1.2, NULL, NULL, NULL, met, NULL, 0, NULL);
+    if (rc != LPD_ERR_NULL_POINTER && rc != LPD_ERR_BAD_STRIDE) return 4;
+    printf("%s|%s|%d\n", info.op_name, lpd_strerror(LPD_ERR_BAD_STRIDE), (int)sizeof(lpd_metrics));
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/lpd.h compiles as strict C99 and a C program links against
+    liblpd.so and calls it (host-side entry points only: no GPU needed)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from logprob_drift_scoring_gb300 import _build
+
+    lib = _build.LIB
+    src = tmp_path / "use_lpd.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_lpd"
+    inc = Path(__file__).resolve().parents[1] / "include"
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", f"-I{inc}", str(src), str(lib),
+           f"-Wl,-rpath,{lib.parent}", "-o", str(exe)]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    name, msg, size = out.stdout.strip().split("|")
+    assert name == "selected_logprob_drift" and msg == B.lib().lpd_strerror(B.LPD_ERR_BAD_STRIDE).decode()
+    assert int(size) == ctypes.sizeof(B.LpdMetrics)
