@@ -83,6 +83,7 @@ extern "C" {
 #define LPD_ERR_ALIGNMENT (-9)    /* a pointer or stride breaks a stated alignment rule */
 #define LPD_ERR_UNSUPPORTED (-10) /* a size outside what this build supports */
 #define LPD_ERR_BAD_TRANSFORM (-11) /* transform chain: bad op count, kind or parameter */
+#define LPD_ERR_BAD_MEMORY (-12)    /* a host-side argument points to device memory */
 
 /* ---- device-reported status bits (lpd_metrics.status) ------------------ */
 #define LPD_STATUS_TOKEN_OOB 1u /* an active row's token id is outside [0, vocab) */
@@ -223,6 +224,8 @@ int lpd_score(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows
  * token_ids_dev, action_mask_dev     device int32[n_rows], uint8[n_rows].
  * out_h2d_bytes   host int64, or NULL: the bytes this call copies to the
  *                 device (active rows of both sides, ids and mask).
+ * The host reads action_mask_host itself: a pointer the CUDA runtime reports
+ * as device memory returns LPD_ERR_BAD_MEMORY before anything is copied.
  * Other arguments, outputs and errors as lpd_score.  As with any
  * asynchronous copy, the host buffers must not change until the copies have
  * completed on `stream`.  The copies issued depend on the mask's contents at

@@ -26,6 +26,7 @@ LPD_ERR_CUDA = -8
 LPD_ERR_ALIGNMENT = -9
 LPD_ERR_UNSUPPORTED = -10
 LPD_ERR_BAD_TRANSFORM = -11
+LPD_ERR_BAD_MEMORY = -12
 LPD_OP_SCALE, LPD_OP_SOFTCAP = 1, 2
 LPD_STATUS_TOKEN_OOB = 1
 LPD_STATUS_NONFINITE = 2

@@ -420,6 +420,7 @@ const char *lpd_strerror(int code) {
         case LPD_ERR_ALIGNMENT: return "a pointer or stride breaks an alignment rule";
         case LPD_ERR_UNSUPPORTED: return "size outside what this build supports";
         case LPD_ERR_BAD_TRANSFORM: return "transform chain: bad op count, kind or parameter";
+        case LPD_ERR_BAD_MEMORY: return "a host-side argument points to device memory";
         case static_cast<int>(LPD_STATUS_TOKEN_OOB): return "status: active token id outside [0, vocab)";
         case static_cast<int>(LPD_STATUS_NONFINITE): return "status: non-finite log-sum-exp or selected logit";
         case static_cast<int>(LPD_STATUS_TIMEOUT): return "status: an internal pipeline wait gave up";
@@ -529,6 +530,13 @@ int lpd_score_host(const lpd_logits *train_host, const lpd_logits *rollout_host,
     if ((rc = check_clip(clip_lo, clip_hi))) return rc;
     if ((rc = check_workspace(workspace, workspace_bytes, lpd_workspace_size(LPD_KIND_SCORE, n_rows, 0, 0))))
         return rc;
+    if (n_rows > 0) {
+        // the mask is read right here on the host: device memory would fault
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, action_mask_host) == cudaSuccess && pa.type == cudaMemoryTypeDevice)
+            return LPD_ERR_BAD_MEMORY;
+        cudaGetLastError();  // a failed query leaves no sticky error behind
+    }
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int64_t bytes = 0;
     if (n_rows > 0) {

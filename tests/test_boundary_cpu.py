@@ -44,7 +44,10 @@ def test_backend_info():
 
 
 def test_strerror_covers_every_code():
-    for code in range(0, -11, -1):
+    header = (Path(__file__).resolve().parents[1] / "include" / "lpd.h").read_text()
+    codes = [int(c) for c in re.findall(r"#define LPD_ERR_\w+ \((-\d+)\)", header)]
+    assert len(codes) >= 12 and len(set(codes)) == len(codes)
+    for code in [0] + codes:
         assert B.lpd_strerror(code) != "unknown code", code
     for bit in (B.LPD_STATUS_TOKEN_OOB, B.LPD_STATUS_NONFINITE, B.LPD_STATUS_TIMEOUT):
         assert B.lpd_strerror(bit).startswith("status")

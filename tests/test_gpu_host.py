@@ -135,3 +135,20 @@ def test_huge_page_host_buffers():
     empty = B.HostBuffer((0,), torch.float32)
     assert empty.tensor.numel() == 0
     empty.free()
+
+
+def test_device_mask_is_refused():
+    # the host reads the mask during the call: device memory there is an
+    # argument error, reported before anything is copied
+    w = W.synthetic(50, 3000, seed=13, device=DEV)
+    th, rh = _host_copy(w.train), _host_copy(w.rollout)
+    td, rd = _staging(w.train), _staging(w.rollout)
+    ids_h = w.token_ids.cpu()
+    outs = [torch.empty(50, device=DEV) for _ in range(3)]
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, 50), dtype=torch.uint8, device=DEV)
+    with pytest.raises(RuntimeError, match="device memory"):
+        B.lpd_score_host(th, rh, ids_h, w.action_mask, *w.clip, td, rd, torch.empty_like(w.token_ids),
+                         torch.empty_like(w.action_mask), *outs, met, ws)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isnan(td.float()))  # nothing was copied
