@@ -725,9 +725,11 @@ def run_e2e(w, args, world: int = 1):
     dev = w.token_ids.device
     host, bufs = [], []
     pinned = True
-    host_memory = "lpd_host_alloc (huge-page advised, registered)"
+    host_memory = "lpd_host_alloc (huge-page advised, registered)" if args.host_memory == "lpd" else "cudaHostAlloc"
     for t in (w.train, w.rollout, w.token_ids, w.action_mask):
         try:
+            if args.host_memory != "lpd":
+                raise RuntimeError("torch pinned memory requested")
             hb = B.HostBuffer(t.shape, t.dtype)
             bufs.append(hb)
             h = hb.tensor
@@ -868,6 +870,8 @@ def main(argv=None):
     ap.add_argument("--config", choices=sorted(CONFIGS), default="qwen")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--host-memory", choices=["lpd", "torch"], default="lpd",
+                    help="e2e host inputs in lpd_host_alloc memory or torch pinned (cudaHostAlloc) memory")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=48)
