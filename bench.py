@@ -19,7 +19,8 @@ Printed (one JSON line, rank 0):
              reads the metrics record back
   cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
 
---impl reference times the oracle alone (the reference arm of this build).
+--impl reference times the oracle alone: the reference arm (the method is
+published as text without code, so the float64 oracle stands in for it).
 Multi-GPU (torchrun, N>1): every rank scores its own batch (replicas, weak
 scaling, no collective on the data path); the step time is the max over ranks.
 """

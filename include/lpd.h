@@ -81,7 +81,7 @@ extern "C" {
 #define LPD_ERR_WORKSPACE (-7)    /* workspace NULL or smaller than lpd_workspace_size() */
 #define LPD_ERR_CUDA (-8)         /* a CUDA runtime call failed (launch, attribute) */
 #define LPD_ERR_ALIGNMENT (-9)    /* a pointer or stride breaks a stated alignment rule */
-#define LPD_ERR_UNSUPPORTED (-10) /* a size outside what this build supports */
+#define LPD_ERR_UNSUPPORTED (-10) /* a size outside what this library supports */
 #define LPD_ERR_BAD_TRANSFORM (-11) /* transform chain: bad op count, kind or parameter */
 #define LPD_ERR_BAD_MEMORY (-12)    /* a host-side argument points to device memory */
 

@@ -418,7 +418,7 @@ const char *lpd_strerror(int code) {
         case LPD_ERR_WORKSPACE: return "workspace missing or smaller than lpd_workspace_size()";
         case LPD_ERR_CUDA: return "a CUDA runtime call failed";
         case LPD_ERR_ALIGNMENT: return "a pointer or stride breaks an alignment rule";
-        case LPD_ERR_UNSUPPORTED: return "size outside what this build supports";
+        case LPD_ERR_UNSUPPORTED: return "size outside what this library supports";
         case LPD_ERR_BAD_TRANSFORM: return "transform chain: bad op count, kind or parameter";
         case LPD_ERR_BAD_MEMORY: return "a host-side argument points to device memory";
         case static_cast<int>(LPD_STATUS_TOKEN_OOB): return "status: active token id outside [0, vocab)";
