@@ -724,23 +724,14 @@ def run_e2e(w, args, world: int = 1):
     from logprob_drift_scoring_gb300 import binding as B
 
     dev = w.token_ids.device
-    host, bufs = [], []
+    host = []
     pinned = True
-    host_memory = "lpd_host_alloc (huge-page advised, registered)" if args.host_memory == "lpd" else "cudaHostAlloc"
     for t in (w.train, w.rollout, w.token_ids, w.action_mask):
         try:
-            if args.host_memory != "lpd":
-                raise RuntimeError("torch pinned memory requested")
-            hb = B.HostBuffer(t.shape, t.dtype)
-            bufs.append(hb)
-            h = hb.tensor
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         except RuntimeError:
-            host_memory = "cudaHostAlloc"
-            try:
-                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            except RuntimeError:
-                h = torch.empty(t.shape, dtype=t.dtype)
-                pinned = False
+            h = torch.empty(t.shape, dtype=t.dtype)
+            pinned = False
         h.copy_(t)
         host.append(h)
     dbuf = [torch.empty_like(t) for t in (w.train, w.rollout, w.token_ids, w.action_mask)]
@@ -771,8 +762,6 @@ def run_e2e(w, args, world: int = 1):
     per_step = sorted(ev[k].elapsed_time(ev[k + 1]) for k in range(steps))
     ms = barrier_max(ev[0].elapsed_time(ev[steps]) / steps, world)
     del dbuf, host
-    for hb in bufs:
-        hb.free()
     torch.cuda.empty_cache()
     assert len(set(copied)) == 1  # the same rows every step
     return {"value": round(world * n_active / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": copied[0],
@@ -780,7 +769,7 @@ def run_e2e(w, args, world: int = 1):
             "ms_per_step_median": round(per_step[len(per_step) // 2], 3), "ms_per_step_max": round(per_step[-1], 3),
             "pinned": pinned,
             "steps": steps, "copies": "active rows of both sides (one 2-D copy per run of active rows), ids, mask",
-            "host_memory": host_memory}
+            "host_memory": "torch pinned (cudaHostAlloc)" if pinned else "pageable"}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -871,8 +860,6 @@ def main(argv=None):
     ap.add_argument("--config", choices=sorted(CONFIGS), default="qwen")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--host-memory", choices=["lpd", "torch"], default="lpd",
-                    help="e2e host inputs in lpd_host_alloc memory or torch pinned (cudaHostAlloc) memory")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=48)

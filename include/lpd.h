@@ -33,9 +33,8 @@
  *
  * Memory: the caller owns every buffer.  Logits, ids, mask, per-token outputs,
  * the metrics record and the workspace are DEVICE pointers (lpd_score_host
- * alone takes its logits, ids and mask in host memory); no call allocates or
- * retains anything between calls, except lpd_host_alloc, whose whole job is to
- * allocate page-locked host memory for the caller.  All calls are asynchronous on
+ * alone takes its logits, ids and mask in host memory); nothing is allocated
+ * or retained by the library between calls.  All calls are asynchronous on
  * the given stream (a cudaStream_t passed as void*, NULL for the legacy
  * default stream) and, all but lpd_score_host, may be captured in a CUDA
  * graph.
@@ -238,17 +237,6 @@ int lpd_score_host(const lpd_logits *train_host, const lpd_logits *rollout_host,
                    float *out_logp_train, float *out_logp_rollout, float *out_dlogp,
                    lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                    int64_t *out_h2d_bytes, void *stream);
-
-/* Page-locked host memory for lpd_score_host's inputs: an anonymous mapping
- * advised for transparent huge pages (Linux), then registered with the CUDA
- * runtime so copies from it are direct DMA at the link rate.  Returns NULL
- * when the mapping or the registration fails (for instance without a GPU);
- * the caller then has no buffer and nothing to free.  lpd_host_free takes the
- * pointer and the byte count of the allocation and returns LPD_OK,
- * LPD_ERR_NULL_POINTER, or LPD_ERR_CUDA when the unregistration fails (the
- * mapping is released in every case). */
-void *lpd_host_alloc(size_t bytes);
-int lpd_host_free(void *ptr, size_t bytes);
 
 /* Stage 1 of lpd_score ("Measurement Contract": prompt, padding and masked
  * positions are excluded): the order-preserving list of active rows with

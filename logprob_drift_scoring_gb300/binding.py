@@ -97,7 +97,6 @@ MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
 
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_score_host",
-            "lpd_host_alloc", "lpd_host_free",
             "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_fused_transformed", "lpd_score_transformed",
@@ -145,10 +144,6 @@ def lib() -> ctypes.CDLL:
         L.lpd_score_fused.argtypes = [P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
         L.lpd_score_fused_transformed.restype = ctypes.c_int
         L.lpd_score_fused_transformed.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, D, D, P, P, P, P, P, SZ, P]
-        L.lpd_host_alloc.restype = ctypes.c_void_p
-        L.lpd_host_alloc.argtypes = [SZ]
-        L.lpd_host_free.restype = ctypes.c_int
-        L.lpd_host_free.argtypes = [P, SZ]
         L.lpd_score_host.restype = ctypes.c_int
         L.lpd_score_host.argtypes = [P, P, P, P, I64, I64, P, P, P, P, D, D, P, P, P, P, P, SZ, P, P]
         L.lpd_score_transformed.restype = ctypes.c_int
@@ -264,42 +259,6 @@ def lpd_score_host(train_host, rollout_host, token_ids_host, action_mask_host, c
                               ctypes.byref(copied), _stream(stream))
     _check(rc, "lpd_score_host")
     return int(copied.value)
-
-
-class HostBuffer:
-    """Page-locked host memory from lpd_host_alloc, seen as a torch CPU tensor
-    (`.tensor`) of the given shape and dtype: the staging memory for
-    lpd_score_host's inputs.  free() (or garbage collection of this object)
-    releases it; the tensor must not be used afterwards."""
-
-    def __init__(self, shape, dtype):
-        import torch
-
-        shape = tuple(int(d) for d in shape)
-        n = 1
-        for d in shape:
-            n *= d
-        nbytes = max(1, n * torch.empty(0, dtype=dtype).element_size())
-        ptr = lib().lpd_host_alloc(nbytes)
-        if not ptr:
-            raise RuntimeError("lpd_host_alloc failed (no GPU, or page-locking refused)")
-        self._ptr, self._bytes = ptr, nbytes
-        self._raw = (ctypes.c_char * nbytes).from_address(ptr)
-        self.tensor = torch.frombuffer(self._raw, dtype=torch.uint8)[:n * torch.empty(0, dtype=dtype).element_size()] \
-            .view(dtype).view(shape)
-
-    def free(self) -> None:
-        if self._ptr:
-            self.tensor = None
-            self._raw = None
-            _check(lib().lpd_host_free(self._ptr, self._bytes), "lpd_host_free")
-            self._ptr = None
-
-    def __del__(self):
-        try:
-            self.free()
-        except Exception:
-            pass
 
 
 def lpd_score_transformed(train, rollout, train_ops, rollout_ops, token_ids, action_mask, clip_lo, clip_hi,

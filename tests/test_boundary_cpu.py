@@ -391,18 +391,6 @@ def test_score_host_rejects_invalid_arguments(kwargs, code):
     assert copied == 0  # nothing was copied
 
 
-def test_host_alloc_without_a_gpu_fails_cleanly():
-    import torch
-
-    if torch.cuda.is_available():
-        pytest.skip("a GPU is present")
-    assert B.lib().lpd_host_alloc(1 << 20) is None
-    assert B.lib().lpd_host_alloc(0) is None
-    assert B.lib().lpd_host_free(None, 0) == B.LPD_ERR_NULL_POINTER
-    with pytest.raises(RuntimeError):
-        B.HostBuffer((4, 4), torch.float32)
-
-
 C_PROGRAM = r"""
 #include <stdio.h>
 #include <string.h>

@@ -107,36 +107,6 @@ def test_zero_rows():
     assert copied == 0 and met["n_active"] == 0 and met["flags"] == B.LPD_FLAG_NO_ACTIVE
 
 
-def test_huge_page_host_buffers():
-    # inputs staged in lpd_host_alloc memory give the same bits as torch's
-    # pinned memory, and the buffers are page-locked
-    w = W.synthetic(300, 7001, seed=12, device=DEV, active_prob=0.6, dtype_rollout=torch.float32)
-    ref = _check(w)
-    bufs = [B.HostBuffer(t.shape, t.dtype) for t in (w.train, w.rollout, w.token_ids, w.action_mask)]
-    try:
-        for hb, t in zip(bufs, (w.train, w.rollout, w.token_ids, w.action_mask)):
-            assert hb.tensor.is_pinned()
-            hb.tensor.copy_(t)
-        n = w.n_rows
-        td, rd = _staging(w.train), _staging(w.rollout)
-        ids_d = torch.empty(n, dtype=torch.int32, device=DEV)
-        mask_d = torch.empty(n, dtype=torch.uint8, device=DEV)
-        outs = [torch.empty(n, device=DEV) for _ in range(3)]
-        met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
-        ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, n), dtype=torch.uint8, device=DEV)
-        B.lpd_score_host(*(hb.tensor for hb in bufs), *w.clip, td, rd, ids_d, mask_d, *outs, met, ws)
-        torch.cuda.synchronize()
-        for a, b in zip(outs, ref[0]):
-            assert torch.equal(a, b)
-        assert B.read_metrics(met) == ref[1]
-    finally:
-        for hb in bufs:
-            hb.free()
-    empty = B.HostBuffer((0,), torch.float32)
-    assert empty.tensor.numel() == 0
-    empty.free()
-
-
 def test_device_mask_is_refused():
     # the host reads the mask during the call: device memory there is an
     # argument error, reported before anything is copied
