@@ -101,6 +101,94 @@ __global__ void __launch_bounds__(1024) select_active_kernel(int64_t n_rows, con
     }
 }
 
+// The same compaction spread over blocks of kSelBlockRows rows, for batches
+// of 2 to kSelMaxBlocks such blocks: one kernel counts each block's active
+// rows into the workspace header's spare slots, a second lets every block
+// take its base from the counts of the blocks before it and write its pairs.
+// The output is the single-CTA kernel's, pair for pair.
+constexpr int kSelBlockThreads = 256;
+constexpr int kSelBlockRows = kSelBlockThreads * 16;  // 4096
+constexpr int kSelMaxBlocks = 31;                     // spare int64 slots in WsHeader
+
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_sum, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < kSelBlockThreads / 32 ? warp_sum[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += y;
+        }
+        if (lane < kSelBlockThreads / 32) warp_sum[lane] = wi - w;
+        if (lane == 31) warp_sum[31] = wi;
+    }
+    __syncthreads();
+    total = warp_sum[31];
+    return warp_sum[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(kSelBlockThreads) count_active_kernel(int64_t n_rows,
+                                                                       const uint8_t *__restrict__ mask,
+                                                                       WsHeader *hdr) {
+    __shared__ int warp_sum[32];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kSelBlockRows + threadIdx.x * 16;
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) cnt += (r0 + q < n_rows && mask[r0 + q]) ? 1 : 0;
+    int total;
+    block_excl_scan(cnt, warp_sum, total);
+    if (threadIdx.x == 0) hdr->reserved[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kSelBlockThreads) compact_active_kernel(
+    int64_t n_rows, const uint8_t *__restrict__ mask, const int32_t *__restrict__ ids, float *__restrict__ out_lt,
+    float *__restrict__ out_lr, float *__restrict__ out_d, lpd_metrics *metrics, WsHeader *hdr,
+    int2 *__restrict__ rowid) {
+    __shared__ int warp_sum[32];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kSelBlockRows + threadIdx.x * 16;
+    uint8_t mk[16];
+    int32_t idv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) mk[q] = (r0 + q < n_rows) ? mask[r0 + q] : 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) idv[q] = (mk[q] && ids) ? ids[r0 + q] : 0;
+    int64_t base = 0;
+    for (unsigned b = 0; b < blockIdx.x; ++b) base += hdr->reserved[b];  // the blocks before this one
+    uint32_t bits = 0;
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const int64_t r = r0 + q;
+        if (mk[q]) {
+            bits |= 1u << q;
+            ++cnt;
+        } else if (r < n_rows) {
+            if (out_lt) out_lt[r] = 0.f;
+            if (out_lr) out_lr[r] = 0.f;
+            if (out_d) out_d[r] = 0.f;
+        }
+    }
+    int total;
+    int64_t pos = base + block_excl_scan(cnt, warp_sum, total);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        if (bits >> q & 1u) rowid[pos++] = make_int2(static_cast<int>(r0 + q), idv[q]);
+    }
+    if (threadIdx.x == 0) {
+        if (blockIdx.x == gridDim.x - 1) hdr->n_active = base + total;
+        if (blockIdx.x == 0) metrics->status = 0u;
+    }
+}
+
 // Metrics over caller-given per-row dlogp (the union of several ranks' rows):
 // active row i takes d = dlogp[row] widened to fp64 and the key |d| in fp32;
 // a non-finite value on an active row sets LPD_STATUS_NONFINITE.
@@ -403,7 +491,16 @@ __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, 
 cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int32_t *ids, float *out_lt,
                                  float *out_lr, float *out_d, lpd_metrics *metrics, WsHeader *hdr,
                                  int2 *rowid, cudaStream_t stream) {
-    select_active_kernel<<<1, 1024, 0, stream>>>(n_rows, mask, ids, out_lt, out_lr, out_d, metrics, hdr, rowid);
+    const int64_t blocks = (n_rows + kSelBlockRows - 1) / kSelBlockRows;
+    if (blocks < 2 || blocks > kSelMaxBlocks) {
+        select_active_kernel<<<1, 1024, 0, stream>>>(n_rows, mask, ids, out_lt, out_lr, out_d, metrics, hdr, rowid);
+        return cudaGetLastError();
+    }
+    count_active_kernel<<<static_cast<unsigned>(blocks), kSelBlockThreads, 0, stream>>>(n_rows, mask, hdr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    compact_active_kernel<<<static_cast<unsigned>(blocks), kSelBlockThreads, 0, stream>>>(
+        n_rows, mask, ids, out_lt, out_lr, out_d, metrics, hdr, rowid);
     return cudaGetLastError();
 }
 
