@@ -247,9 +247,14 @@ __device__ __forceinline__ void block_tree(Part *sh) {
 // with log(s_r / s_t) = log1p(-dd / s_t) when |dd| < s_t / 2 (dd = s_t - s_r
 // carried separately, see lpd_acc.cuh), which keeps dlogp accurate when the
 // two rows nearly agree and exactly 0 when they differ by a constant shift.
-__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const __grid_constant__ FinArgs a) {
+// One thread per active row in small blocks, so that a batch of a few
+// thousand rows still spreads over every SM (the fp64 row arithmetic is
+// latency-bound).
+constexpr int kFinalizeThreads = 64;
+
+__global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const __grid_constant__ FinArgs a) {
     const int64_t n_active = a.hdr->n_active;
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinalizeThreads + threadIdx.x;
     if (i >= n_active) return;
     const int2 rid = a.rowid[i];
     const int64_t r = rid.x, id = rid.y;
@@ -514,9 +519,9 @@ cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader
 }
 
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream) {
-    const int64_t blocks = (n_rows + kFinThreads - 1) / kFinThreads;
+    const int64_t blocks = (n_rows + kFinalizeThreads - 1) / kFinalizeThreads;
     if (blocks == 0) return cudaSuccess;
-    finalize_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(a);
+    finalize_kernel<<<static_cast<unsigned>(blocks), kFinalizeThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
