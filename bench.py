@@ -232,7 +232,7 @@ class Runner:
         else:
             ws = B.lpd_workspace_size(B.LPD_KIND_SCORE, n)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
-        self.launches_per_step = 5 if n > 0 else 2
+        self.launches_per_step = select_launches(n) + 4 if n > 0 else 2
         self.chain = None
         self.entropy = None      # [ent_train, ent_rollout] when timing lpd_score_entropy
         self.backward = None     # (grad, out_dlogits) when timing lpd_logprob_backward
@@ -367,6 +367,13 @@ def measured_tflops() -> dict:
     return {"tflops": 1700.0, "source": "fallback sustained"}
 
 
+def select_launches(n_rows: int) -> int:
+    """Kernels of stage 1 (active-row compaction): a count and a compaction
+    kernel for 2 to 31 blocks of 4096 rows, else one single-CTA kernel."""
+    blocks = -(-n_rows // 4096)
+    return 2 if 2 <= blocks <= 31 else 1
+
+
 def run_fused(args, w, world, rank):
     """The fused LM-head path: one lpd_score_fused call per step (with
     --transform, lpd_score_fused_transformed with that chain on both sides)."""
@@ -421,7 +428,8 @@ def run_fused(args, w, world, rank):
                      "peak_source": f"{peak['source']} bf16 GEMM", "span": "whole lpd_score_fused call" if chain is None
                      else "whole lpd_score_fused_transformed call",
                      "algorithmic_flops_per_launch": flops},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * args.steps, "clocks": clocks.summary(),
+        "cpu_baseline": None, "e2e": None, "gpu_launches": (select_launches(n) + 5) * args.steps,
+        "clocks": clocks.summary(),
         "impl": "lpd",
     }
     print(json.dumps(out), flush=True)
