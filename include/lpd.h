@@ -521,9 +521,12 @@ int lpd_attn_merge_order_drift(const void *out_parts, int32_t parts_dtype, const
  * n_rows > LPD_NOALLOC_MAX_ROWS, before touching the GPU.  It allocates
  * nothing.  The first call on each device (with that device current) looks up
  * the array's address, so make that first call before any stream capture on
- * the device.  All calls on a device share the array and it keeps the previous
- * call's contents (nothing in it needs to start at zero); calls whose work
- * overlaps on the GPU race on it, so order them on one stream. */
+ * the device; the address is cached per device context, so the first call
+ * after a device reset looks it up again.  All calls on a device share the
+ * array and it keeps the previous call's contents (nothing in it needs to
+ * start at zero).  The library does not serialise callers: calls whose work
+ * overlaps on the GPU race on the array, so the caller orders them (one
+ * stream, or events between streams). */
 int lpd_score_noalloc(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows,
                       int64_t vocab, const int32_t *token_ids, const uint8_t *action_mask,
                       double clip_lo, double clip_hi, float *out_logp_train,
