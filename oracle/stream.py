@@ -1,0 +1,151 @@
+"""The float64 oracle over large, device-resident workloads, on all host cores.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline and reference legs of ``bench.py`` may import this module.
+
+Scheduling only, no arithmetic: the listed rows of the input tensors are
+copied to host memory chunk by chunk (``torch`` is used for the device-to-host
+copy and nothing else), and a pool of host threads runs the oracle's serial
+C on each chunk.  ctypes releases the GIL for the duration of every C call, so
+the chunks run in parallel; each row still goes through exactly the serial
+float64 code of ``oracle.score_rows`` / ``oracle.score_sharded`` /
+``oracle.score_head_rows``, and the results are put back in the order of the
+listed rows.  Host memory in flight is bounded by ``2 * threads`` chunks.
+"""
+from __future__ import annotations
+
+import os
+from collections import deque
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import Result, load, score_head_rows, score_rows, score_sharded
+
+
+def host_threads(threads: int | None = None) -> int:
+    """Worker threads to use: all host cores unless told otherwise."""
+    return max(1, int(threads) if threads else (os.cpu_count() or 1))
+
+
+def _host(t) -> np.ndarray:
+    """Host numpy copy of a tensor for the oracle (bf16 as uint16 bits)."""
+    import torch
+
+    t = t.detach()
+    if t.dtype == torch.bfloat16:
+        return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().contiguous().numpy()
+
+
+def _run_chunks(chunks, work, threads: int | None):
+    """work(payload) for every (key, payload) that ``chunks`` yields, on a
+    bounded pool; returns {key: result}.  The generator (device copies) runs on
+    the calling thread while the pool scores earlier chunks."""
+    n = host_threads(threads)
+    out = {}
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        pending = deque()
+        for key, payload in chunks:
+            pending.append((key, pool.submit(work, payload)))
+            while len(pending) >= 2 * n:
+                k, f = pending.popleft()
+                out[k] = f.result()
+        while pending:
+            k, f = pending.popleft()
+            out[k] = f.result()
+    return out
+
+
+def _concat(parts: list[Result]) -> Result:
+    status = 0
+    for p in parts:
+        status |= p.status
+    return Result(np.concatenate([p.logp_train for p in parts]) if parts else np.zeros(0),
+                  np.concatenate([p.logp_rollout for p in parts]) if parts else np.zeros(0),
+                  np.concatenate([p.dlogp for p in parts]) if parts else np.zeros(0), status)
+
+
+def score_rows_device(train, rollout, token_ids, rows, chunk: int = 64, threads: int | None = None) -> Result:
+    """oracle.score_rows of the listed rows of device (or host) tensors
+    train/rollout [R, V] and token_ids [R]; per-row results in ``rows`` order."""
+    import torch
+
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dev = train.device
+    ids_all = token_ids.detach().cpu().numpy().astype(np.int32)
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            sel_np = rows[c:c + chunk]
+            sel = torch.as_tensor(sel_np, device=dev)
+            yield c, (_host(train.index_select(0, sel)), _host(rollout.index_select(0, sel)), ids_all[sel_np])
+
+    def work(p):
+        t, r, ids = p
+        return score_rows(t, r, ids, np.arange(t.shape[0]), lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    return _concat([res[k] for k in sorted(res)])
+
+
+def score_sharded_rows_device(train_shards, rollout_shards, v_ranges, token_ids, rows, order=None,
+                              chunk: int = 64, threads: int | None = None) -> Result:
+    """oracle.score_sharded of the listed rows (every listed row active),
+    shards merged in ``order`` (default: ascending vocab position)."""
+    import torch
+
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dev = train_shards[0].device
+    ids_all = token_ids.detach().cpu().numpy().astype(np.int32)
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            sel_np = rows[c:c + chunk]
+            sel = torch.as_tensor(sel_np, device=dev)
+            yield c, ([_host(x.index_select(0, sel)) for x in train_shards],
+                      [_host(x.index_select(0, sel)) for x in rollout_shards], ids_all[sel_np])
+
+    def work(p):
+        ts, rs, ids = p
+        return score_sharded(ts, rs, v_ranges, ids, np.ones(ids.size, np.uint8), order=order, lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    return _concat([res[k] for k in sorted(res)])
+
+
+def score_head_rows_parallel(hidden_train, hidden_rollout, weight, token_ids, rows, chunk: int = 4,
+                             threads: int | None = None) -> Result:
+    """oracle.score_head_rows (logits materialised in double) of the listed
+    rows; host arrays (bf16 bits as uint16), rows split over host threads."""
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            yield c, rows[c:c + chunk]
+
+    def work(sel):
+        return score_head_rows(hidden_train, hidden_rollout, weight, token_ids, sel, lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    return _concat([res[k] for k in sorted(res)])
+
+
+def score_rows_parallel(train, rollout, token_ids, rows, chunk: int = 64, threads: int | None = None) -> Result:
+    """oracle.score_rows of host arrays with the listed rows split over host
+    threads."""
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            yield c, rows[c:c + chunk]
+
+    def work(sel):
+        return score_rows(train, rollout, token_ids, sel, lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    return _concat([res[k] for k in sorted(res)])

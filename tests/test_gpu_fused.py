@@ -61,24 +61,51 @@ def test_fused_identical_inputs_exact_zero():
     assert res.metrics["approx_kl0"] == 0.0 and res.metrics["ratio0_mean"] == 1.0
 
 
-def test_fused_batch_composition_bitwise():
-    w = W.head(140, 256, 1300, seed=5, device=DEV)
-    full = run(w)
-    for start, total, off in ((0, 1, 0), (17, 7, 3), (100, 40, 33), (5, 300, 200)):
-        k = min(total - off, 7 if total > 1 else 1)
-        sel = slice(start, start + k)
-        g = torch.Generator(device=DEV).manual_seed(start)
-        ht = torch.randn((total, w.hidden), generator=g, device=DEV).to(torch.bfloat16)
-        hr = torch.randn((total, w.hidden), generator=g, device=DEV).to(torch.bfloat16)
-        ids = torch.randint(0, w.vocab, (total,), generator=g, device=DEV, dtype=torch.int32)
-        mask = torch.ones(total, dtype=torch.uint8, device=DEV)
-        ht[off:off + k] = w.hidden_train[sel]
-        hr[off:off + k] = w.hidden_rollout[sel]
-        ids[off:off + k] = w.token_ids[sel]
+def _embed_head(w, sel, k, n_left, n_before, n_after, n_right, seed):
+    """A batch holding the rows ``sel`` (k of them) of w after n_before active
+    garbage rows (so the picked rows start at compacted position n_before and
+    may straddle a 128-row tile), with n_after active garbage rows after them,
+    and n_left / n_right inactive garbage rows at the two ends.  Returns the
+    batch and the batch position of the first picked row."""
+    total = n_left + n_before + k + n_after + n_right
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    ht = torch.randn((total, w.hidden), generator=g, device=DEV).to(torch.bfloat16)
+    hr = torch.randn((total, w.hidden), generator=g, device=DEV).to(torch.bfloat16)
+    ids = torch.randint(0, w.vocab, (total,), generator=g, device=DEV, dtype=torch.int32)
+    mask = torch.ones(total, dtype=torch.uint8, device=DEV)
+    mask[:n_left] = 0
+    mask[total - n_right:] = 0
+    off = n_left + n_before
+    ht[off:off + k] = w.hidden_train[sel]
+    hr[off:off + k] = w.hidden_rollout[sel]
+    ids[off:off + k] = w.token_ids[sel]
+    return ht, hr, ids, mask, off
+
+
+# (first picked row, k, inactive left pad, active rows before, active rows
+# after, inactive right pad): batches of 1, 7 and 64, placed at the start of a
+# tile, at its last row, across the boundary between the first and second
+# 128-row tiles, and behind left and right padding
+HEAD_PLACEMENTS = [(0, 1, 0, 0, 0, 0), (5, 1, 3, 127, 0, 2), (9, 1, 0, 128, 40, 0), (0, 7, 0, 0, 0, 0),
+                   (7, 7, 2, 125, 0, 5), (20, 7, 9, 60, 100, 0), (0, 64, 0, 0, 0, 0), (0, 64, 4, 100, 30, 11),
+                   (0, 64, 0, 250, 0, 1)]
+
+
+def _head_batch_controls(w, full, picked, seed):
+    for j0, k, n_left, n_before, n_after, n_right in HEAD_PLACEMENTS:
+        sel = picked[j0:j0 + k]
+        ht, hr, ids, mask, off = _embed_head(w, sel, k, n_left, n_before, n_after, n_right, seed + j0 + 3 * k)
         res = run(w, ht, hr, ids, mask)
         for a, b in ((res.logp_train, full.logp_train), (res.logp_rollout, full.logp_rollout),
                      (res.dlogp, full.dlogp)):
-            assert torch.equal(a[off:off + k], b[sel])
+            assert torch.equal(a[off:off + k], b[sel]), (j0, k, n_left, n_before, n_after, n_right)
+
+
+def test_fused_batch_composition_bitwise():
+    w = W.head(300, 256, 1300, seed=5, device=DEV)
+    full = run(w)
+    picked = torch.arange(10, 74, device=DEV)
+    _head_batch_controls(w, full, picked, seed=5)
 
 
 def test_fused_matches_unfused_on_materialised_logits():
@@ -94,23 +121,40 @@ def test_fused_matches_unfused_on_materialised_logits():
         assert torch.max(torch.abs(a - b)).item() <= LOGP_ATOL
 
 
-def test_full_size_fused_sampled_rows():
+@pytest.mark.slow
+def test_full_size_fused_rows_and_batch_control():
+    """The fused LM-head workload itself (16384 tokens x H = 4096, W [151936,
+    4096]): 128 rows, one in every 128-row tile at a different position,
+    against the oracle's double-precision head on all host cores; then the
+    batch-composition control at this shape (every tile runs all 64 K blocks
+    of H = 4096): 64 rows rescored at batch 1, 7 and 64, across tile
+    boundaries and behind padding, bitwise equal to the full batch."""
+    from oracle import stream
+
     w = W.fused(device=DEV)
     res = run(w)
     assert res.metrics["n_active"] == w.n_rows and res.metrics["status"] == 0
-    rows = np.array([0, 1, 127, 128, 8191, 16383])
+    n_tiles = w.n_rows // 128
+    rows = np.array([128 * j + (37 * j) % 128 for j in range(n_tiles)])
+    rows[0], rows[-1] = 0, w.n_rows - 1
+    ref = stream.score_head_rows_parallel(to_oracle(w.hidden_train), to_oracle(w.hidden_rollout),
+                                          to_oracle(w.weight), w.token_ids.cpu().numpy(), rows)
     sel = torch.as_tensor(rows, device=DEV)
-    sub = W.HeadWorkload("sub", w.hidden_train[sel], w.hidden_rollout[sel], w.weight, w.token_ids[sel],
-                         w.action_mask[sel])
-    ref = oracle_rows(sub, np.arange(rows.size))
     for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout),
                       (res.dlogp, ref.dlogp)):
         g = got[sel].cpu().numpy().astype(np.float64)
         assert np.max(np.abs(g - want)) <= LOGP_ATOL
+    # the metrics over all 16384 tokens: the oracle's metric function of the
+    # GPU's per-token dlogp (the oracle's head costs ~2 s of one core per row)
     d = res.dlogp.cpu().numpy().astype(np.float64)
     prop = oracle.metrics(d, np.ones(w.n_rows, np.uint8), *w.clip)
     prop["status"] = 0
     assert_metrics_match(res.metrics, prop, d, np.ones(w.n_rows, np.uint8), w.clip, ambiguity=1e-6)
+    rng = np.random.default_rng(19)
+    picked = torch.as_tensor(np.sort(rng.choice(w.n_rows, size=64, replace=False)), device=DEV)
+    _head_batch_controls(w, res, picked, seed=23)
+    del w, res
+    torch.cuda.empty_cache()
 
 
 # ---- transform chains in the fused epilogue ("[WS2] Framework for ablation

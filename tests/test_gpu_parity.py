@@ -328,69 +328,7 @@ def test_sharded_vs_oracle(bounds):
     assert torch.equal(lt, lt3) and torch.equal(d, d3)
 
 
-# --------------------------------------------------------------- full size
-
-def _sampled_parity(w, n_sample=256, seed=0):
-    """Per-token parity on sampled active rows against the oracle, and the
-    metrics against the oracle's metric function applied to the GPU's own
-    per-token dlogp (a property that holds at any size)."""
-    res = run(w.train, w.rollout, w.token_ids, w.action_mask, w.clip)
-    mask = w.action_mask.cpu().numpy()
-    act_rows = np.flatnonzero(mask)
-    assert res.metrics["n_active"] == act_rows.size
-    assert res.metrics["status"] == 0
-    rng = np.random.default_rng(seed)
-    rows = np.sort(rng.choice(act_rows, size=min(n_sample, act_rows.size), replace=False))
-    rows = np.unique(np.concatenate([rows, act_rows[:2], act_rows[-2:]]))
-    sel = torch.as_tensor(rows, device=DEV)
-    ids = w.token_ids.cpu().numpy()
-    ref = oracle.score_rows(to_oracle(w.train[sel]), to_oracle(w.rollout[sel]), ids[rows],
-                            np.arange(rows.size), lib=None)
-    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout),
-                      (res.dlogp, ref.dlogp)):
-        g = got[sel].cpu().numpy().astype(np.float64)
-        assert np.max(np.abs(g - want)) <= LOGP_ATOL
-    d = res.dlogp.cpu().numpy().astype(np.float64)
-    prop = oracle.metrics(d, mask, *w.clip)
-    prop["status"] = 0
-    assert_metrics_match(res.metrics, prop, d, mask, w.clip, ambiguity=1e-6)
-    return res
-
-
-def test_full_size_qwen_vocab():
-    w = W.qwen(device=DEV)
-    _sampled_parity(w)
-    del w
-    torch.cuda.empty_cache()
-
-
-def test_full_size_llama_mixed_dtype():
-    w = W.llama(device=DEV)
-    _sampled_parity(w)
-    del w
-    torch.cuda.empty_cache()
-
-
-def test_full_size_sharded():
-    w = W.sharded(device=DEV)
-    (lt, lr, d, plt, plr), met = _sharded_call(w, perm=[2, 0, 3, 1])
-    assert met["n_active"] == w.n_rows and met["status"] == 0
-    rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(w.n_rows, size=128, replace=False))
-    sel = torch.as_tensor(rows, device=DEV)
-    ids = w.token_ids.cpu().numpy()[rows]
-    ref = oracle.score_sharded([to_oracle(x[sel]) for x in w.train], [to_oracle(x[sel]) for x in w.rollout],
-                               w.v_ranges, ids, np.ones(rows.size, np.uint8))
-    for got, want in ((lt, ref.logp_train), (lr, ref.logp_rollout), (d, ref.dlogp), (plt, ref.logp_train)):
-        g = got[sel].cpu().numpy().astype(np.float64)
-        assert np.max(np.abs(g - want)) <= LOGP_ATOL
-    dd = d.cpu().numpy().astype(np.float64)
-    prop = oracle.metrics(dd, np.ones(w.n_rows, np.uint8))
-    prop["status"] = 0
-    assert_metrics_match(met, prop, dd, np.ones(w.n_rows, np.uint8), ambiguity=1e-6)
-    del w
-    torch.cuda.empty_cache()
-
+# ------------------------------------------------------------- timeouts
 
 def test_stalled_pipeline_times_out_cleanly(monkeypatch):
     """LPD_STALL_ROW_PASS=1 makes one CTA of the row pass withhold its first
