@@ -40,3 +40,41 @@ def test_profile_lookup_follows_the_kernel_source():
     else:
         assert prof is None  # a stale capture is never reported as traffic
     assert bench.profiled_row_kernel("no_such_config") is None
+
+
+def test_launch_plan():
+    # one GPU, or a rank torchrun started with the matching world size: run here
+    assert bench.plan_launch(1, {}, 0) == "run"
+    assert bench.plan_launch(4, {"WORLD_SIZE": "4"}, 0) == "run"
+    # N > 1 outside torchrun: relaunch as N ranks, if N GPUs are visible
+    assert bench.plan_launch(2, {}, 8) == "relaunch"
+    with pytest.raises(SystemExit):
+        bench.plan_launch(9, {}, 8)
+    with pytest.raises(SystemExit):
+        bench.plan_launch(2, {"WORLD_SIZE": "4"}, 8)
+    with pytest.raises(SystemExit):
+        bench.plan_launch(0, {}, 8)
+
+
+def test_launch_command():
+    cmd = bench.launch_command(4, ["--gpus", "4", "--steps", "7"], 29512)
+    assert cmd[:3] == [sys.executable, "-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--nnodes=1" in cmd and "--master-port=29512" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-5:] == [str(ROOT / "bench.py"), "--gpus", "4", "--steps", "7"]
+
+
+def test_reference_arm_under_two_ranks_prints_one_line():
+    # the reference arm as the driver launches it for N = 2 (torchrun, CPU
+    # only): rank 0 alone scores and prints; n_gpus is the world size
+    import json
+
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2", "--master-addr",
+           "127.0.0.1", f"--master-port={bench.free_port()}", str(ROOT / "bench.py"), "--impl", "reference",
+           "--gpus", "2", "--config", "tiny", "--steps", "1", "--warmup", "3", "--ref-rows", "2"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["cpu_baseline"]["cores"] >= 1
