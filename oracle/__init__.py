@@ -53,6 +53,21 @@ class Metrics(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class LogpDrift(ctypes.Structure):
+    _fields_ = [
+        ("max_abs_dlogp_train", ctypes.c_double),
+        ("max_abs_dlogp_rollout", ctypes.c_double),
+        ("row_train", ctypes.c_int64),
+        ("row_rollout", ctypes.c_int64),
+        ("n_active", ctypes.c_int64),
+        ("n_differ", ctypes.c_int64),
+        ("frac_differ", ctypes.c_double),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
 class Shard(ctypes.Structure):
     _fields_ = [
         ("ptr", ctypes.c_void_p),
@@ -132,6 +147,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.lpdo_attn_merge.argtypes = [P, P, ctypes.c_int, I64, ctypes.c_int, ctypes.c_int, P, P, P]
     lib.lpdo_score_head_rows.restype = U32
     lib.lpdo_score_head_rows.argtypes = [P, P, P, I64, I64, P, P, I64, P, P, P]
+    lib.lpdo_logp_drift.restype = None
+    lib.lpdo_logp_drift.argtypes = [I64, P, P, P, P, P, P]
     return lib
 
 
@@ -368,3 +385,18 @@ def attn_merge(out_parts, lse_parts, order=None, lse_base2=False, lib=None):
     lse = np.zeros(n)
     lib.lpdo_attn_merge(_ptr(o), _ptr(l), K, n, d, int(bool(lse_base2)), _ptr(order), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def logp_drift(a_train, a_rollout, b_train, b_rollout, mask, lib=None) -> dict:
+    """Summary of how far per-token result b is from result a (float32
+    arrays, e.g. a permuted against the fixed shard merge order) over the
+    active rows: each side's max |b - a| with its lowest row, and the count and
+    fraction of active rows where they differ."""
+    lib = lib or load()
+    arrs = [np.ascontiguousarray(x, dtype=np.float32) for x in (a_train, a_rollout, b_train, b_rollout)]
+    m8 = np.ascontiguousarray(mask, dtype=np.uint8)
+    n = m8.shape[0]
+    assert all(x.shape == (n,) for x in arrs)
+    out = LogpDrift()
+    lib.lpdo_logp_drift(n, *(_ptr(x) for x in arrs), _ptr(m8), ctypes.addressof(out))
+    return out.as_dict()

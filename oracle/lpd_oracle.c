@@ -576,3 +576,78 @@ void lpdo_attn_merge(const float *out_parts, const float *lse_parts, int K, int6
         out_lse[i] = lse_base2 ? lse / ln2 : lse;
     }
 }
+
+/* ---- merge-order drift summary [LP] ---------------------------------------
+ * The LogProb knobs table (row 5) names the merge order of the per-shard
+ * partials as a drift source; the summary of that diagnostic compares two
+ * per-token results of the same rows, a (the fixed global shard order) and b
+ * (another merge order), over the active rows only:
+ *   max_abs_t / max_abs_r  the largest |b - a| of each side, formed in double
+ *                          from the float32 values; a NaN difference (either
+ *                          value NaN) counts as larger than any number;
+ *   row_t / row_r          the lowest active row attaining it (-1 with no
+ *                          active row);
+ *   n_differ               active rows where a and b are different numbers on
+ *                          either side (+0 and -0 are the same number, and two
+ *                          NaNs count as the same);
+ *   frac_differ            n_differ / n_active (0 with no active row). */
+typedef struct {
+    double max_abs_t;
+    double max_abs_r;
+    int64_t row_t;
+    int64_t row_r;
+    int64_t n_active;
+    int64_t n_differ;
+    double frac_differ;
+} lpdo_drift_summary;
+
+/* 1 when |b - a| of this row beats the best so far (ties keep the lower row,
+ * which was seen first) */
+static int drift_beats(double diff, double best, int have)
+{
+    if (!have)
+        return 1;
+    if (isnan(best))
+        return 0;
+    if (isnan(diff))
+        return 1;
+    return diff > best;
+}
+
+static int same_number(float a, float b)
+{
+    if (isnan(a) && isnan(b))
+        return 1;
+    return a == b;
+}
+
+void lpdo_logp_drift(int64_t n_rows, const float *a_t, const float *a_r, const float *b_t,
+                     const float *b_r, const uint8_t *mask, lpdo_drift_summary *out)
+{
+    out->max_abs_t = 0.0;
+    out->max_abs_r = 0.0;
+    out->row_t = -1;
+    out->row_r = -1;
+    out->n_active = 0;
+    out->n_differ = 0;
+    out->frac_differ = 0.0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        if (!mask[r])
+            continue;
+        double dt = fabs((double)b_t[r] - (double)a_t[r]);
+        double dr = fabs((double)b_r[r] - (double)a_r[r]);
+        if (drift_beats(dt, out->max_abs_t, out->row_t >= 0)) {
+            out->max_abs_t = dt;
+            out->row_t = r;
+        }
+        if (drift_beats(dr, out->max_abs_r, out->row_r >= 0)) {
+            out->max_abs_r = dr;
+            out->row_r = r;
+        }
+        out->n_active += 1;
+        if (!same_number(a_t[r], b_t[r]) || !same_number(a_r[r], b_r[r]))
+            out->n_differ += 1;
+    }
+    if (out->n_active > 0)
+        out->frac_differ = (double)out->n_differ / (double)out->n_active;
+}

@@ -598,4 +598,82 @@ def pin_attn_merge_masked_parts(lib):
     assert np.array_equal(out, np.zeros((1, 3))) and lse[0] == -np.inf
 
 
+
+# ---- merge-order drift summary ("[WS2] Framework for ablation experiment",
+# LogProb knobs table, row 5: the merge order of the shard partials as a drift
+# source).  Hand-built result pairs whose summary is known by construction.
+
+def pin_logp_drift_identical_and_empty(lib):
+    rng = np.random.default_rng(91)
+    a_t = rng.normal(-12, 1, 40).astype(np.float32)
+    a_r = rng.normal(-12, 1, 40).astype(np.float32)
+    mask = (rng.random(40) < 0.7).astype(np.uint8)
+    mask[:3] = 0
+    s = oracle.logp_drift(a_t, a_r, a_t.copy(), a_r.copy(), mask, lib=lib)
+    first = int(np.flatnonzero(mask)[0])
+    assert s["max_abs_dlogp_train"] == 0.0 and s["max_abs_dlogp_rollout"] == 0.0
+    assert s["row_train"] == first and s["row_rollout"] == first          # every active row ties at 0
+    assert s["n_active"] == int(mask.sum()) and s["n_differ"] == 0 and s["frac_differ"] == 0.0
+    s0 = oracle.logp_drift(a_t, a_r, a_t, a_r, np.zeros(40, np.uint8), lib=lib)
+    assert s0 == {"max_abs_dlogp_train": 0.0, "max_abs_dlogp_rollout": 0.0, "row_train": -1, "row_rollout": -1,
+                  "n_active": 0, "n_differ": 0, "frac_differ": 0.0}
+
+
+def pin_logp_drift_constructed(lib):
+    n = 12
+    a_t = np.full(n, -10.0, np.float32)
+    a_r = np.full(n, -11.0, np.float32)
+    b_t, b_r = a_t.copy(), a_r.copy()
+    mask = np.ones(n, np.uint8)
+    b_t[2] = -10.25          # |d| 0.25
+    b_t[5] = -9.5            # |d| 0.5, first of a tie
+    b_t[9] = -10.5           # |d| 0.5, the tie's later row
+    b_t[7] = -13.0           # |d| 3, but the row is masked out
+    mask[7] = 0
+    b_r[4] = -11.0 + 2.0 ** -20   # one float32 step apart: a tiny but real difference
+    a_r[6], b_r[6] = 0.0, -0.0    # +0 and -0 are the same number
+    s = oracle.logp_drift(a_t, a_r, b_t, b_r, mask, lib=lib)
+    assert s["max_abs_dlogp_train"] == 0.5 and s["row_train"] == 5
+    assert s["max_abs_dlogp_rollout"] == 2.0 ** -20 and s["row_rollout"] == 4
+    assert s["n_active"] == n - 1
+    assert s["n_differ"] == 4                               # rows 2, 4, 5, 9
+    assert s["frac_differ"] == 4 / (n - 1)
+    # differing on the rollout side only still counts the row
+    s2 = oracle.logp_drift(a_t, a_r, a_t, b_r, mask, lib=lib)
+    assert s2["n_differ"] == 1 and s2["max_abs_dlogp_train"] == 0.0
+
+
+def pin_logp_drift_nan_ranks_highest(lib):
+    a = np.array([-1.0, -2.0, np.nan, -4.0, np.nan], np.float32)
+    b = np.array([-1.5, -2.0, np.nan, -9.0, -5.0], np.float32)
+    mask = np.ones(5, np.uint8)
+    s = oracle.logp_drift(a, a, b, b, mask, lib=lib)
+    assert math.isnan(s["max_abs_dlogp_train"]) and s["row_train"] == 2    # lowest NaN row, above |d| = 5
+    # two NaNs are the same result; NaN against a number is a difference
+    assert s["n_differ"] == 3                                               # rows 0, 3, 4
+    mask[2] = 0
+    s2 = oracle.logp_drift(a, a, b, b, mask, lib=lib)
+    assert math.isnan(s2["max_abs_dlogp_train"]) and s2["row_train"] == 4
+
+
+def pin_logp_drift_of_shard_merge_orders(lib):
+    # the exact logp does not depend on the merge order: in double, the fixed
+    # and permuted merges agree to rounding, so their float32 results differ
+    # by at most one float32 step
+    rng = np.random.default_rng(92)
+    V, bounds = 3000, [(0, 700), (700, 701), (701, 2500), (2500, 3000)]
+    x = bf16_bits(rng.normal(0, 3, size=(30, V)).astype(np.float32))
+    y = bf16_bits(rng.normal(0, 3, size=(30, V)).astype(np.float32))
+    ids = rng.integers(0, V, 30).astype(np.int32)
+    mask = np.ones(30, np.uint8)
+    ts = [np.ascontiguousarray(x[:, a:b]) for a, b in bounds]
+    rs = [np.ascontiguousarray(y[:, a:b]) for a, b in bounds]
+    fixed = oracle.score_sharded(ts, rs, bounds, ids, mask, lib=lib)
+    perm = oracle.score_sharded(ts, rs, bounds, ids, mask, order=[3, 1, 0, 2], lib=lib)
+    f = [v.astype(np.float32) for v in (fixed.logp_train, fixed.logp_rollout, perm.logp_train, perm.logp_rollout)]
+    s = oracle.logp_drift(*f, mask, lib=lib)
+    step = float(np.max(np.spacing(np.abs(f[0]))))
+    assert s["n_active"] == 30 and s["max_abs_dlogp_train"] <= step and s["max_abs_dlogp_rollout"] <= step
+
+
 ALL_PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}

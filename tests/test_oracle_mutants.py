@@ -62,6 +62,13 @@ MUTANTS = {
     "attn_base2_unconverted": ("            if (lse_base2)\n                l *= ln2;\n            double w", "            double w"),
     "attn_masked_part_read": ("            if (l == -INFINITY)\n                continue;\n            if (lse_base2)\n                l *= ln2;\n            double w",
                               "            if (lse_base2)\n                l *= ln2;\n            double w"),
+    "drift_ties_high": ("    return diff > best;\n}", "    return diff >= best;\n}"),
+    "drift_mask_ignored": ("        if (!mask[r])\n            continue;\n        double dt", "        double dt"),
+    "drift_nan_ignored": ("    if (isnan(diff))\n        return 1;", "    if (isnan(diff))\n        return 0;"),
+    "drift_frac_denominator": ("(double)out->n_differ / (double)out->n_active", "(double)out->n_differ / (double)n_rows"),
+    "drift_one_side": ("if (!same_number(a_t[r], b_t[r]) || !same_number(a_r[r], b_r[r]))",
+                       "if (!same_number(a_t[r], b_t[r]))"),
+    "drift_nan_pairs_differ": ("    if (isnan(a) && isnan(b))\n        return 1;", "    if (isnan(a) && isnan(b))\n        return 0;"),
     "nonfinite_unflagged": ("return (isfinite(lse) && isfinite(xs)) ? 0u : LPDO_STATUS_NONFINITE;\n}\n\nstatic int",
                             "return 0u;\n}\n\nstatic int"),
 }
