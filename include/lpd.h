@@ -345,6 +345,43 @@ int lpd_score_sharded(const lpd_shard *train, const lpd_shard *rollout, int32_t 
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* Summary of the merge-order diagnostic ("[WS2] Framework for ablation
+ * experiment", LogProb knobs table, row 5: the merge order of the per-shard
+ * partials as a drift source), next to the per-token outputs it summarises.
+ * Two per-token results of the same rows are compared over the active rows:
+ * a = the fixed global shard order (out_logp_* of lpd_score_sharded), b = the
+ * permuted order (out_perm_logp_*), or any other pair of per-token logp results.
+ *   max_abs_dlogp_train / _rollout  largest |b - a| of each side (float32
+ *                        difference widened to double; a NaN difference, i.e.
+ *                        either value NaN, ranks above every number);
+ *   row_train / row_rollout  lowest active row attaining it (-1: no active row);
+ *   n_active             active rows (action_mask != 0);
+ *   n_differ             active rows where either side's b is a different
+ *                        number from a (+0 equals -0; two NaNs count as equal);
+ *   frac_differ          n_differ / n_active (0 with no active row).
+ * `scratch` is working space of the call; its contents afterwards mean
+ * nothing. */
+typedef struct {
+    double max_abs_dlogp_train;
+    double max_abs_dlogp_rollout;
+    int64_t row_train;
+    int64_t row_rollout;
+    int64_t n_active;
+    int64_t n_differ;
+    double frac_differ;
+    uint64_t scratch[4];
+} lpd_logp_drift;
+
+/* logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b: device float32
+ * [n_rows]; action_mask: device uint8 [n_rows]; out: device lpd_logp_drift
+ * (8-byte aligned), written asynchronously on `stream`.  Inactive rows are never
+ * read.  0 <= n_rows < 2^32 - 1 (else LPD_ERR_BAD_SIZE / LPD_ERR_UNSUPPORTED);
+ * NULL pointers give LPD_ERR_NULL_POINTER (the row arrays may be NULL when
+ * n_rows == 0).  No workspace; nothing is allocated. */
+int lpd_logp_drift_summary(int64_t n_rows, const float *logp_train_a, const float *logp_rollout_a,
+                           const float *logp_train_b, const float *logp_rollout_b,
+                           const uint8_t *action_mask, lpd_logp_drift *out, void *stream);
+
 /* ---- reduction topology arms ------------------------------------------------- */
 
 /* The three ways a vocab-parallel logprob can combine its shards

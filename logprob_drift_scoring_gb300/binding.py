@@ -95,13 +95,26 @@ class LpdMergeDrift(ctypes.Structure):
 
 MERGE_DRIFT_BYTES = ctypes.sizeof(LpdMergeDrift)
 
+
+class LpdLogpDrift(ctypes.Structure):
+    _fields_ = [("max_abs_dlogp_train", ctypes.c_double), ("max_abs_dlogp_rollout", ctypes.c_double),
+                ("row_train", ctypes.c_int64), ("row_rollout", ctypes.c_int64), ("n_active", ctypes.c_int64),
+                ("n_differ", ctypes.c_int64), ("frac_differ", ctypes.c_double), ("scratch", ctypes.c_uint64 * 4)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "scratch"}
+
+
+LOGP_DRIFT_BYTES = ctypes.sizeof(LpdLogpDrift)
+
 # every symbol include/lpd.h declares
 EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score", "lpd_score_host",
             "lpd_select_active",
             "lpd_token_logp", "lpd_drift_metrics", "lpd_score_sharded", "lpd_score_noalloc",
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_fused_transformed", "lpd_score_transformed",
             "lpd_score_entropy", "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
-            "lpd_topology_workspace_size", "lpd_score_sharded_topology", "lpd_drift_metrics_from_dlogp")
+            "lpd_topology_workspace_size", "lpd_score_sharded_topology", "lpd_drift_metrics_from_dlogp",
+            "lpd_logp_drift_summary")
 LPD_NOALLOC_MAX_ROWS = 32768
 LPD_ATTN_MAX_PARTS = 64
 
@@ -164,6 +177,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_attn_merge.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P]
         L.lpd_attn_merge_order_drift.restype = ctypes.c_int
         L.lpd_attn_merge_order_drift.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P]
+        L.lpd_logp_drift_summary.restype = ctypes.c_int
+        L.lpd_logp_drift_summary.argtypes = [I64, P, P, P, P, P, P, P]
         _LIB = L
     return _LIB
 
@@ -445,6 +460,20 @@ def lpd_attn_merge_order_drift(out_parts, lse_parts, order_a, order_b, out, out_
     _check(rc, "lpd_attn_merge_order_drift")
 
 
+def lpd_logp_drift_summary(logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b, action_mask, out,
+                           stream=None) -> None:
+    """Merge-order drift summary of per-token result b against result a over
+    the active rows (device float32 [n] each, uint8 mask, out: a device buffer
+    of LOGP_DRIFT_BYTES)."""
+    n = action_mask.shape[0]
+    for x in (logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b):
+        if x.shape[0] != n:
+            raise ValueError("per-token results and mask must have the same length")
+    rc = lib().lpd_logp_drift_summary(n, _ptr(logp_train_a), _ptr(logp_rollout_a), _ptr(logp_train_b),
+                                      _ptr(logp_rollout_b), _ptr(action_mask), _ptr(out), _stream(stream))
+    _check(rc, "lpd_logp_drift_summary")
+
+
 # ---- convenience: allocate with torch, call, read back ------------------------
 
 def read_merge_drift(buf) -> dict:
@@ -477,6 +506,21 @@ def attn_merge_order_drift(out_parts, lse_parts, order_a=None, order_b=None, lse
     drift = torch.empty(MERGE_DRIFT_BYTES, dtype=torch.uint8, device=dev)
     lpd_attn_merge_order_drift(out_parts, lse_parts, order_a, order_b, out, lse, rdo, rdl, drift, lse_base2, stream)
     return out, lse, rdo, rdl, read_merge_drift(drift)
+
+
+def read_logp_drift(buf) -> dict:
+    """Copy a device lpd_logp_drift record (uint8 tensor) to the host as a dict."""
+    host = buf.detach().to("cpu", copy=True).numpy().tobytes()
+    return LpdLogpDrift.from_buffer_copy(host).as_dict()
+
+
+def logp_drift_summary(logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b, action_mask, stream=None) -> dict:
+    """lpd_logp_drift_summary with a torch-allocated record, read back as a dict."""
+    import torch
+
+    out = torch.empty(LOGP_DRIFT_BYTES, dtype=torch.uint8, device=action_mask.device)
+    lpd_logp_drift_summary(logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b, action_mask, out, stream)
+    return read_logp_drift(out)
 
 
 def read_metrics(buf) -> dict:

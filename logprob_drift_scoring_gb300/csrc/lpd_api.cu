@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "lpd_internal.cuh"
+#include "lpd_xform.cuh"
 
 namespace lpd {
 
@@ -106,6 +107,44 @@ bool stall_requested() {
     return v && v[0] == '1' && v[1] == '\0';
 }
 
+// A side's chain in the reduced form of the kRowSoftcap pass: at most one
+// soft-cap, every scale behind it (softcap_p(a x) = a softcap_{p/a}(x)), the
+// product of all scales in *post.  False when the chain has more than one
+// soft-cap, or when the pre-multiplied series coefficients would leave the
+// range of normal floats (p far from 1); such chains take the general pass.
+bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
+    *out = SoftcapSide{};
+    double pre = 1.0, after = 1.0, cap = 0.0;
+    int n_cap = 0;
+    for (int k = 0; k < c.n_ops; ++k) {
+        if (c.kind[k] == LPD_OP_SCALE) {
+            (n_cap ? after : pre) *= static_cast<double>(c.param[k]);
+        } else {
+            ++n_cap;
+            cap = static_cast<double>(c.param[k]);
+        }
+    }
+    *post = pre * after;
+    if (n_cap == 0) return true;
+    if (n_cap > 1) return false;
+    const double p = cap / pre, r = pre / cap;
+    const double lo = 1e-36, hi = 1e36;
+    if (!(p > lo && p < hi && r * r > lo && r * r < hi)) return false;
+    out->on = 1;
+    out->p = static_cast<float>(p);
+    out->r = static_cast<float>(r);
+    out->r2 = static_cast<float>(r * r);
+    // |x| < 0.599 p gives fl(fl(x^2) / p^2) < 0.36 after every rounding
+    out->thr = static_cast<float>(0.599 * p);
+    double rk = r * r;
+    for (int k = 0; k < kSoftcapTerms; ++k, rk *= r * r) {
+        const double q = static_cast<double>(tanh_c(k)) * rk;
+        if (!(std::fabs(q) > lo && std::fabs(q) < hi)) return false;
+        out->q[k] = static_cast<float>(q);
+    }
+    return true;
+}
+
 // Stage 2: the streaming row pass, then the per-row finalise.
 // Optional extras of the row pass: a transform chain per side, or entropy outputs.
 struct RowExtras {
@@ -134,6 +173,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
                 if (ex.xform[side].kind[k] != LPD_OP_SCALE) scales_only = false;
                 prod[side] *= ex.xform[side].param[k];
             }
+        double post[2];
         if (scales_only) {
             // the product of scales rides in each side's exponent factor
             a.lt = static_cast<float>(static_cast<double>(prod[0]) * 1.4426950408889634);
@@ -143,6 +183,17 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
             lg_t = a.lt;
             lg_r = a.lr;
             mode = kRowScale;
+        } else if (reduce_softcap(ex.xform[0], &a.cap[0], &post[0]) &&
+                   reduce_softcap(ex.xform[1], &a.cap[1], &post[1])) {
+            // one soft-cap per side at most: the soft-cap on each value, the
+            // scales (moved behind it) in the exponent factor
+            a.lt = static_cast<float>(post[0] * 1.4426950408889634);
+            a.lr = static_cast<float>(post[1] * 1.4426950408889634);
+            scale_t = static_cast<float>(post[0]);
+            scale_r = static_cast<float>(post[1]);
+            lg_t = a.lt;
+            lg_r = a.lr;
+            mode = kRowSoftcap;
         }
     } else if (ex.ent_t || ex.ent_r) {
         mode = kRowEntropy;
@@ -705,6 +756,22 @@ size_t lpd_topology_workspace_size(int32_t topology, int64_t n_rows, int64_t voc
         default:
             return 0;
     }
+}
+
+int lpd_logp_drift_summary(int64_t n_rows, const float *logp_train_a, const float *logp_rollout_a,
+                           const float *logp_train_b, const float *logp_rollout_b, const uint8_t *action_mask,
+                           lpd_logp_drift *out, void *stream) {
+    if (n_rows < 0) return LPD_ERR_BAD_SIZE;
+    if (n_rows >= 0xffffffffll) return LPD_ERR_UNSUPPORTED;  // rows travel as 32 bits in the max keys
+    if (!out || (n_rows > 0 && (!logp_train_a || !logp_rollout_a || !logp_train_b || !logp_rollout_b ||
+                                !action_mask)))
+        return LPD_ERR_NULL_POINTER;
+    if (reinterpret_cast<uintptr_t>(out) % 8 || reinterpret_cast<uintptr_t>(logp_train_a) % 4 ||
+        reinterpret_cast<uintptr_t>(logp_rollout_a) % 4 || reinterpret_cast<uintptr_t>(logp_train_b) % 4 ||
+        reinterpret_cast<uintptr_t>(logp_rollout_b) % 4)
+        return LPD_ERR_ALIGNMENT;
+    return cuda_status(launch_logp_drift(n_rows, logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b,
+                                         action_mask, out, static_cast<cudaStream_t>(stream)));
 }
 
 int lpd_score_sharded_topology(const lpd_shard *train, const lpd_shard *rollout, int32_t n_shards, int64_t n_rows,

@@ -24,7 +24,7 @@ namespace lpd {
 // arithmetic order, so they are part of the batch-invariance contract:
 // changing them changes results (bitwise), but never makes them depend on the
 // batch.
-constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3;
+constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3, kRowSoftcap = 4;
 __host__ __device__ constexpr int row_warps(int mode) { return mode == kRowTransform ? 16 : 20; }
 constexpr int kConsumerWarps = 20;               // the largest W: the workspace's warp-state stride
 constexpr int kColsPerThread = 16;
@@ -118,9 +118,26 @@ struct Xform {
     float param[LPD_MAX_TRANSFORM_OPS];
 };
 
+// A side's chain with at most one soft-cap, in the reduced form the
+// kRowSoftcap pass evaluates: x -> softcap_p(x) (when `on`), and the product of
+// all the chain's scales applied afterwards through the exponent factor.  A
+// scale a before the soft-cap moves behind it, softcap_p(a x) =
+// a softcap_{p/a}(x), so p here is the chain's soft-cap divided by the scales
+// in front of it.  On |x| < 0.6 p the series p tanh(x / p) = x (1 + u Q(u)),
+// u = x^2, runs with the coefficients of the fitted tanh series pre-multiplied
+// by the powers of 1/p^2 (q[k] = c_k / p^(2k+2)); beyond, the exponential form.
+constexpr int kSoftcapTerms = 5;
+struct SoftcapSide {
+    int on;                 // 0: no soft-cap on this side (identity)
+    float p, r, r2;         // p, 1/p, 1/p^2
+    float thr;              // |x| below this is inside the series range for certain
+    float q[kSoftcapTerms];
+};
+
 struct RowArgs {
     Xform xt, xr;    // train and rollout chains (transform mode only)
-    float lt, lr;    // scale-only chains: each side's s log2 e (maxima kept unscaled)
+    SoftcapSide cap[2];  // train and rollout soft-caps (soft-cap mode only)
+    float lt, lr;    // scale-only and soft-cap chains: each side's s log2 e (maxima kept unscaled)
     Segment seg[kMaxSegments];
     int n_seg;
     int64_t vocab;
@@ -218,6 +235,10 @@ cudaError_t launch_attn_merge(const AttnMergeCall &c, cudaStream_t stream);
 // full rows (pitches in bytes).
 cudaError_t launch_gather_shards(const Segment *segs, int n_seg, int64_t n_rows, void *dst_t, int64_t pitch_t,
                                  int elt_t, void *dst_r, int64_t pitch_r, int elt_r, cudaStream_t stream);
+
+// Summary of per-token result b against result a over the active rows.
+cudaError_t launch_logp_drift(int64_t n_rows, const float *at, const float *ar, const float *bt, const float *br,
+                              const uint8_t *mask, lpd_logp_drift *out, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -31,6 +31,7 @@ def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(B.LpdMetrics) == 80
     assert ctypes.sizeof(B.LpdBackendInfo) == 32 + 48 + 16 + 32 + 16 + 96
     assert ctypes.sizeof(B.LpdMergeDrift) == 48
+    assert ctypes.sizeof(B.LpdLogpDrift) == 7 * 8 + 32
 
 
 def test_backend_info():
@@ -414,6 +415,24 @@ int main(void) {
     return 0;
 }
 """
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(n=-1), B.LPD_ERR_BAD_SIZE),
+    (dict(n=0xFFFFFFFF), B.LPD_ERR_UNSUPPORTED),
+    (dict(at=None), B.LPD_ERR_NULL_POINTER),
+    (dict(br=None), B.LPD_ERR_NULL_POINTER),
+    (dict(m=None), B.LPD_ERR_NULL_POINTER),
+    (dict(out=None), B.LPD_ERR_NULL_POINTER),
+    (dict(n=0, out=None), B.LPD_ERR_NULL_POINTER),
+    (dict(out=FAKE + 4), B.LPD_ERR_ALIGNMENT),
+    (dict(bt=FAKE + 2), B.LPD_ERR_ALIGNMENT),
+])
+def test_logp_drift_summary_validation(kwargs, code):
+    a = dict(n=8, at=FAKE, ar=FAKE, bt=FAKE, br=FAKE, m=FAKE, out=FAKE)
+    a.update(kwargs)
+    rc = B.lib().lpd_logp_drift_summary(a["n"], a["at"], a["ar"], a["bt"], a["br"], a["m"], a["out"], None)
+    assert rc == code
 
 
 def test_header_is_plain_c_and_links(tmp_path):

@@ -148,9 +148,15 @@ def test_full_size_sharded_every_row():
     assert ref.status == 0
     d_full, ref_m, errs = _per_token_and_metrics((lt, lr, d), mask, ref, w.clip)
     assert_metrics_match(met, ref_m, d_full, mask, w.clip, dlogp_err=errs[2])
-    # the permuted-order merge is a diagnostic: still within the logp bar
+    # the permuted-order merge is a diagnostic: still within the logp bar, and
+    # its GPU summary equals the oracle's summary of the same per-token values
     for g, want in ((plt, ref.logp_train), (plr, ref.logp_rollout)):
         assert np.max(np.abs(g.cpu().numpy().astype(np.float64)[act] - want)) <= LOGP_ATOL
+    summ = B.logp_drift_summary(lt, lr, plt, plr, w.action_mask)
+    want = oracle.logp_drift(lt.cpu().numpy(), lr.cpu().numpy(), plt.cpu().numpy(), plr.cpu().numpy(), mask)
+    assert summ == want, (summ, want)
+    print(f"sharded merge order {perm}: max |dlogp| train {summ['max_abs_dlogp_train']:.2e} rollout "
+          f"{summ['max_abs_dlogp_rollout']:.2e}, rows differing {summ['frac_differ']:.4f}")
     # batch-composition control on the sharded layout: picked rows of every
     # shard embedded in small batches, both the fixed and the permuted results
     rng = np.random.default_rng(18)

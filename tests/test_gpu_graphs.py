@@ -118,15 +118,18 @@ def test_sharded_topologies_and_union_metrics_in_a_graph():
     wss = [torch.empty(B.lpd_topology_workspace_size(t, n, 12000, 3, B.LPD_BF16, B.LPD_BF16), dtype=torch.uint8,
                        device=DEV) for t in range(3)]
     ws_u = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, n), dtype=torch.uint8, device=DEV)
+    summ = torch.empty(B.LOGP_DRIFT_BYTES, dtype=torch.uint8, device=DEV)
 
     def step():
         for t in range(3):
             B.lpd_score_sharded_topology(ts, rs, bounds, base.token_ids, base.action_mask, 0.8, 1.2, t, [2, 0, 1],
                                          *outs[t], mets[t], wss[t])
         B.lpd_drift_metrics_from_dlogp(outs[0][2], base.action_mask, 0.8, 1.2, mets[3], ws_u)
+        # two arms' per-token results summarised against each other
+        B.lpd_logp_drift_summary(outs[0][0], outs[0][1], outs[1][0], outs[1][1], base.action_mask, summ)
 
     flat = [o for arm in outs for o in arm]
-    _check_replays(ts + rs + [base.token_ids], ts2 + rs2 + [base2.token_ids], flat + mets, step)
+    _check_replays(ts + rs + [base.token_ids], ts2 + rs2 + [base2.token_ids], flat + mets + [summ], step)
 
 
 def test_fused_head_in_a_graph():

@@ -328,6 +328,77 @@ def test_sharded_vs_oracle(bounds):
     assert torch.equal(lt, lt3) and torch.equal(d, d3)
 
 
+def _summary_vs_oracle(a_t, a_r, b_t, b_r, mask):
+    """GPU lpd_logp_drift_summary against the oracle's summary of the same
+    float32 values: equal field by field (|b - a| of two floats within a factor
+    of two is exact in fp32, so even the maxima agree bitwise)."""
+    got = B.logp_drift_summary(a_t, a_r, b_t, b_r, mask)
+    want = oracle.logp_drift(*(x.cpu().numpy() for x in (a_t, a_r, b_t, b_r)), mask.cpu().numpy())
+    for k, v in want.items():
+        g = got[k]
+        assert (np.isnan(g) and np.isnan(v)) if isinstance(v, float) and np.isnan(v) else g == v, (k, g, v)
+    return got
+
+
+@pytest.mark.parametrize("bounds,perm", [
+    ([(0, 4096), (4096, 8192), (8192, 12288), (12288, 16384)], [3, 2, 1, 0]),
+    ([(0, 1000), (1000, 9000), (9000, 9001), (9001, 12000)], [2, 0, 3, 1]),
+    ([(0, 5000)], [0]),
+])
+def test_shard_merge_order_summary(bounds, perm):
+    """The merge-order diagnostic's summary ("[WS2] Framework for ablation
+    experiment", LogProb knobs table, row 5): the GPU summary of the fixed
+    against the permuted per-token result equals the oracle's summary of the
+    same values, and, both orders being within the logp bar of the oracle's
+    fixed-order and permuted-order results, the largest drift is within twice
+    the bar; a single shard, or the identity order, drifts by exactly 0."""
+    base, w = _small_sharded(bounds, rows=300, seed=31)
+    (lt, lr, d, plt, plr), met = _sharded_call(w, perm)
+    s = _summary_vs_oracle(lt, lr, plt, plr, w.action_mask)
+    assert s["n_active"] == met["n_active"]
+    mask = w.action_mask.cpu().numpy()
+    ref = oracle.score_sharded([to_oracle(x) for x in w.train], [to_oracle(x) for x in w.rollout], w.v_ranges,
+                               w.token_ids.cpu().numpy(), mask)
+    ref_p = oracle.score_sharded([to_oracle(x) for x in w.train], [to_oracle(x) for x in w.rollout], w.v_ranges,
+                                 w.token_ids.cpu().numpy(), mask, order=perm)
+    exact = oracle.logp_drift(*(v.astype(np.float32) for v in (ref.logp_train, ref.logp_rollout, ref_p.logp_train,
+                                                                ref_p.logp_rollout)), mask)
+    assert exact["max_abs_dlogp_train"] <= 1e-5 and exact["max_abs_dlogp_rollout"] <= 1e-5
+    assert s["max_abs_dlogp_train"] <= 2 * LOGP_ATOL and s["max_abs_dlogp_rollout"] <= 2 * LOGP_ATOL
+    if perm == sorted(perm):
+        assert s["n_differ"] == 0 and s["max_abs_dlogp_train"] == 0.0 and s["max_abs_dlogp_rollout"] == 0.0
+
+
+def test_logp_drift_summary_edges():
+    g = torch.Generator(device=DEV).manual_seed(32)
+    n = 70000
+    a_t = -12 + torch.randn(n, generator=g, device=DEV)
+    a_r = -12 + torch.randn(n, generator=g, device=DEV)
+    b_t, b_r = a_t.clone(), a_r.clone()
+    mask = (torch.rand(n, generator=g, device=DEV) < 0.8).to(torch.uint8)
+    # planted differences: a tie on the train side (lowest row wins), a bigger
+    # one on a masked row, one float32 step, +0 / -0, and NaN pairs
+    b_t[[100, 200, 60000]] += torch.tensor([0.5, 0.25, 0.5], device=DEV)
+    mask[[100, 200, 60000]] = 1
+    b_t[300] += 4.0
+    mask[300] = 0
+    b_r[5] = torch.nextafter(a_r[5], torch.tensor(0.0, device=DEV))
+    mask[5] = 1
+    a_r[7], b_r[7] = 0.0, -0.0
+    s = _summary_vs_oracle(a_t, a_r, b_t, b_r, mask)
+    assert s["row_train"] == 100 and s["n_differ"] == 4
+    # a NaN pair (both results NaN: the same) still ranks above every number
+    a_t[40000] = b_t[40000] = float("nan")
+    mask[40000] = 1
+    s = _summary_vs_oracle(a_t, a_r, b_t, b_r, mask)
+    assert np.isnan(s["max_abs_dlogp_train"]) and s["row_train"] == 40000 and s["n_differ"] == 4
+    # nothing active, and no rows at all
+    _summary_vs_oracle(a_t, a_r, b_t, b_r, torch.zeros_like(mask))
+    e = torch.empty(0, device=DEV)
+    s = _summary_vs_oracle(e, e, e, e, torch.empty(0, dtype=torch.uint8, device=DEV))
+    assert s["row_train"] == -1 and s["n_active"] == 0 and s["frac_differ"] == 0.0
+
+
 # ------------------------------------------------------------- timeouts
 
 def test_stalled_pipeline_times_out_cleanly(monkeypatch):
