@@ -169,13 +169,17 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
 
 // kMode: 0 plain, 1 with a general transform chain, 2 with the entropy sums,
 // 3 with a scale-only chain (each side's product of scales folded into its
-// exponent factor, so no tanh code and no extra arithmetic per element).
+// exponent factor, so no tanh code and no extra arithmetic per element), 4
+// with a chain of at most one soft-cap per side in its reduced form (the
+// soft-cap on each loaded value, the scales folded into the exponent factor
+// as in mode 3).
 template <class DT, class DR, bool kTma, int kMode>
 __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
     row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     constexpr bool kXform = kMode == kRowTransform;
     constexpr bool kEntropy = kMode == kRowEntropy;
     constexpr bool kScale = kMode == kRowScale;
+    constexpr bool kSoftcap = kMode == kRowSoftcap;
     constexpr int kWarps = row_warps(kMode);
     constexpr int kGroupCols = 4 * 32 * kWarps;
     constexpr int kTile = kColsPerThread * 32 * kWarps;
@@ -259,9 +263,20 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
     // Scale-only chains keep the logits unscaled: the scale s rides in the
     // factor to base-2 exponents, (x - m) s log2 e, and the finalise forms
     // s m and s x[id] in fp64.
-    const float lg_t = kScale ? a.lt : kLog2e, lg_r = kScale ? a.lr : kLog2e;
+    const float lg_t = (kScale || kSoftcap) ? a.lt : kLog2e, lg_r = (kScale || kSoftcap) ? a.lr : kLog2e;
     const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0}, cxr{xf_ops + (kXform ? LPD_MAX_TRANSFORM_OPS : 0),
                                                               kXform ? a.xr.n_ops : 0};
+    // one real logit of each side through that side's chain (modes 1 and 4)
+    auto tf_t = [&](float x) -> float {
+        if constexpr (kXform) return xform1(x, cxt);
+        else if constexpr (kSoftcap) return a.cap[0].on ? softcap_u1(x, a.cap[0]) : x;
+        else return x;
+    };
+    auto tf_r = [&](float x) -> float {
+        if constexpr (kXform) return xform1(x, cxr);
+        else if constexpr (kSoftcap) return a.cap[1].on ? softcap_u1(x, a.cap[1]) : x;
+        else return x;
+    };
     uint32_t it = 0;
     for (int64_t i = blockIdx.x; i < n_active; i += gridDim.x) {
         const int2 rid = a.rowid[i];
@@ -309,6 +324,10 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                             xform16(vt, cxt);
                             xform16(vr, cxr);
                         }
+                        if (kSoftcap) {
+                            if (a.cap[0].on) softcap16_u(vt, a.cap[0]);
+                            if (a.cap[1].on) softcap16_u(vr, a.cap[1]);
+                        }
                     } else {
                         // ragged last tile: the same vector loads, then the
                         // columns the bulk copy did not cover (a few bytes at the
@@ -333,16 +352,16 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                                     const int col = col0 + h;
                                     if (col >= nbt) x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                                     if (col >= nbr) y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
-                                    if (kXform && col < nv) {
-                                        x[h] = xform1(x[h], cxt);
-                                        y[h] = xform1(y[h], cxr);
+                                    if ((kXform || kSoftcap) && col < nv) {
+                                        x[h] = tf_t(x[h]);
+                                        y[h] = tf_r(y[h]);
                                     }
                                 }
                                 vt[p] = f2(x[0], x[1]);
                                 vr[p] = f2(y[0], y[1]);
-                            } else if (kXform) {
-                                vt[p] = f2(xform1(f2_lo(vt[p]), cxt), xform1(f2_hi(vt[p]), cxt));
-                                vr[p] = f2(xform1(f2_lo(vr[p]), cxr), xform1(f2_hi(vr[p]), cxr));
+                            } else if (kXform || kSoftcap) {
+                                vt[p] = f2(tf_t(f2_lo(vt[p])), tf_t(f2_hi(vt[p])));
+                                vr[p] = f2(tf_r(f2_lo(vr[p])), tf_r(f2_hi(vr[p])));
                             }
                         }
                     }
@@ -358,9 +377,9 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                             const int col = slot_col<kGroupCols>(t, 2 * p + h);
                             x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                             y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
-                            if (kXform && col < nv) {
-                                x[h] = xform1(x[h], cxt);
-                                y[h] = xform1(y[h], cxr);
+                            if ((kXform || kSoftcap) && col < nv) {
+                                x[h] = tf_t(x[h]);
+                                y[h] = tf_r(y[h]);
                             }
                         }
                         vt[p] = f2(x[0], x[1]);
@@ -372,7 +391,7 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                 accumulate16<kEntropy>(vt, vr, acc2, lg_t, lg_r);
                 return true;
             };
-            if constexpr (kXform) {
+            if constexpr (kXform || kSoftcap) {
                 // the transform chain's larger body: full tiles in a tight loop,
                 // the segment's ragged last tile after it (measured faster)
                 int64_t c0 = 0;
@@ -424,6 +443,7 @@ cudaError_t dispatch_path(const RowArgs &a, int dt, int dr, bool use_tma, cudaSt
 
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream) {
     if (mode == kRowTransform) return dispatch_path<1>(a, dtype_t, dtype_r, use_tma, stream);
+    if (mode == kRowSoftcap) return dispatch_path<4>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowEntropy) return dispatch_path<2>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowScale) return dispatch_path<3>(a, dtype_t, dtype_r, use_tma, stream);
     return dispatch_path<0>(a, dtype_t, dtype_r, use_tma, stream);

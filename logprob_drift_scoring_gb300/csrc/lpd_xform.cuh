@@ -101,6 +101,43 @@ __device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
     for (int q = 0; q < 8; ++q) v[q] = o[q];
 }
 
+// ---- the reduced single soft-cap (kRowSoftcap) --------------------------------
+// One value: the series on u = x^2 when u / p^2 < 0.36 (the same range as the
+// general form's z < 0.36), else p tanh(x / p) in the exponential form.
+__device__ __forceinline__ float softcap_u1(float x, const SoftcapSide &c) {
+    const float u = __fmul_rn(x, x);
+    if (__fmul_rn(u, c.r2) < kTanhZMax) {
+        float q = c.q[kSoftcapTerms - 1];
+#pragma unroll
+        for (int k = kSoftcapTerms - 2; k >= 0; --k) q = __fmaf_rn(q, u, c.q[k]);
+        return __fmaf_rn(x, __fmul_rn(u, q), x);
+    }
+    return __fmul_rn(c.p, tanh_exp(__fmul_rn(x, c.r)));
+}
+
+// Sixteen values in place.  When every |x| of the warp is below c.thr (set on
+// the host a little under 0.6 p, so that softcap_u1 would take its series for
+// each of them) the series runs packed with nothing else kept live; otherwise
+// each value takes softcap_u1.  Either way a value gets softcap_u1's bits.
+__device__ __forceinline__ void softcap16_u(f2_t *v, const SoftcapSide &c) {
+    float amax = fmaxf(fabsf(f2_lo(v[0])), fabsf(f2_hi(v[0])));
+#pragma unroll
+    for (int q = 1; q < 8; ++q) amax = max3(amax, fabsf(f2_lo(v[q])), fabsf(f2_hi(v[q])));
+    if (__all_sync(0xffffffffu, amax < c.thr)) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const f2_t u = mul2(v[q], v[q]);
+            f2_t w = f2(c.q[kSoftcapTerms - 1], c.q[kSoftcapTerms - 1]);
+#pragma unroll
+            for (int k = kSoftcapTerms - 2; k >= 0; --k) w = fma2(w, u, f2(c.q[k], c.q[k]));
+            v[q] = fma2(v[q], mul2(u, w), v[q]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = f2(softcap_u1(f2_lo(v[q]), c), softcap_u1(f2_hi(v[q]), c));
+    }
+}
+
 __device__ __forceinline__ float xform1(float x, const XformView &c) {
 #pragma unroll 1
     for (int k = 0; k < c.n; ++k) {

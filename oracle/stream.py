@@ -20,7 +20,7 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from . import Result, load, score_head_rows, score_rows, score_sharded
+from . import Result, load, score_head_rows, score_rows, score_sharded, score_transformed
 
 
 def host_threads(threads: int | None = None) -> int:
@@ -85,6 +85,31 @@ def score_rows_device(train, rollout, token_ids, rows, chunk: int = 64, threads:
     def work(p):
         t, r, ids = p
         return score_rows(t, r, ids, np.arange(t.shape[0]), lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    return _concat([res[k] for k in sorted(res)])
+
+
+def score_transformed_rows_device(train, rollout, token_ids, rows, train_ops=None, rollout_ops=None,
+                                  chunk: int = 64, threads: int | None = None) -> Result:
+    """oracle.score_transformed of the listed rows (every listed row active),
+    each side through its chain of logit transforms."""
+    import torch
+
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dev = train.device
+    ids_all = token_ids.detach().cpu().numpy().astype(np.int32)
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            sel_np = rows[c:c + chunk]
+            sel = torch.as_tensor(sel_np, device=dev)
+            yield c, (_host(train.index_select(0, sel)), _host(rollout.index_select(0, sel)), ids_all[sel_np])
+
+    def work(p):
+        t, r, ids = p
+        return score_transformed(t, r, ids, np.ones(ids.size, np.uint8), train_ops, rollout_ops, lib=lib)
 
     res = _run_chunks(chunks(), work, threads)
     return _concat([res[k] for k in sorted(res)])

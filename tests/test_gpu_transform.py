@@ -41,6 +41,9 @@ def _check(w, train_ops, rollout_ops, train=None, rollout=None):
     ([(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]),
     ([], [(SCALE, 1 / 0.7)]),                                       # temperature applied on one side only
     ([(SCALE, 1 / 0.7), (SOFTCAP, 30.0)], [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]),  # order mismatch
+    # two soft-caps, and a soft-cap far from 1: the general per-op pass
+    ([(SOFTCAP, 30.0), (SCALE, 2.0), (SOFTCAP, 25.0)], [(SOFTCAP, 30.0), (SCALE, 2.0), (SOFTCAP, 25.0)]),
+    ([(SOFTCAP, 3e4)], [(SCALE, 1 / 0.7), (SOFTCAP, 5.0)]),
 ])
 @pytest.mark.parametrize("shape", [(300, 3 * 8192 + 520, 0), (150, 12805, 3), (200, 5000, 0)])
 def test_transform_chain_vs_oracle(train_ops, rollout_ops, shape):
@@ -89,13 +92,19 @@ def test_vocab_padding_policies(policy):
         assert np.all(ref.logp_train[act] < other.logp_train[act])
 
 
-def test_softcap_tanh_accuracy_per_value():
+@pytest.mark.parametrize("ops", [
+    [(SOFTCAP, 30.0)],                                  # the reduced single soft-cap pass
+    [(SCALE, 0.5), (SOFTCAP, 15.0), (SCALE, 2.0)],      # the same function, scales moved behind the cap
+    [(SOFTCAP, 30.0), (SOFTCAP, 1e6)],                  # general per-op pass (the second cap moves f < 1e-8)
+])
+def test_softcap_tanh_accuracy_per_value(ops):
     """Rows [a, 0] under soft-cap 30: logp of column 0 is -log(1 + exp(-f(a)))
     with f(a) = 30 tanh(a / 30), whose sensitivity to f is at most 1.  The
     kernel's own tanh must keep f within a few ulp: the bar is 8 ulp of
     max(1, |f|) plus the float32 rounding of logp itself.  The values cover
     both forms of the tanh (|a| < 18 and beyond), the switch point, tiny and
-    saturating arguments and +-inf."""
+    saturating arguments and +-inf.  Each chain computes the same f, on the
+    reduced soft-cap pass or on the general one."""
     a = np.concatenate([np.linspace(-200, 200, 4001), 18 + np.linspace(-1e-3, 1e-3, 201),
                         -18 + np.linspace(-1e-3, 1e-3, 201), [1e-30, -1e-30, 1e-7, 3e3, -3e3, np.inf, -np.inf]])
     a = a.astype(np.float32)
@@ -105,7 +114,6 @@ def test_softcap_tanh_accuracy_per_value():
     t = torch.from_numpy(x).to(DEV)
     ids = torch.zeros(n, dtype=torch.int32, device=DEV)
     mask = torch.ones(n, dtype=torch.uint8, device=DEV)
-    ops = [(SOFTCAP, 30.0)]
     res = B.score(t, t, ids, mask, train_ops=ops, rollout_ops=ops)
     torch.cuda.synchronize()
     ref = oracle.score_transformed(x, x, np.zeros(n, np.int32), np.ones(n, np.uint8), ops, ops, 0.8, 1.2)
@@ -116,12 +124,15 @@ def test_softcap_tanh_accuracy_per_value():
     assert np.all(err <= tol), (float(a[np.argmax(err - tol)]), float(np.max(err - tol)))
 
 
-def test_softcap_load_paths_agree_bitwise():
-    # logits spread over both forms of the tanh within the same warps, stored
-    # with 16-byte aligned rows (bulk-copy ring) and with an odd row stride
-    # (plain loads): identical bits
-    base = W.synthetic(40, 3 * 4096 + 517, seed=19, device=DEV, row_pad=3, active_prob=1.0, sigma=20.0)
-    ops = [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)]
+@pytest.mark.parametrize("sigma", [20.0, 3.0])
+@pytest.mark.parametrize("ops", [[(SOFTCAP, 30.0), (SCALE, 1 / 0.7)],                # reduced soft-cap pass
+                                 [(SOFTCAP, 30.0), (SCALE, 1 / 0.7), (SOFTCAP, 40.0)]])  # general pass
+def test_softcap_load_paths_agree_bitwise(ops, sigma):
+    # logits spread over both forms of the tanh within the same warps (sigma
+    # 20), or all in the series range so that whole warps take the packed
+    # series (sigma 3), stored with 16-byte aligned rows (bulk-copy ring) and
+    # with an odd row stride (plain loads, one value at a time): identical bits
+    base = W.synthetic(40, 3 * 4096 + 517, seed=19, device=DEV, row_pad=3, active_prob=1.0, sigma=sigma)
     aligned = B.score(base.train, base.rollout, base.token_ids, base.action_mask, train_ops=ops, rollout_ops=ops)
     t2, r2 = base.train.contiguous(), base.rollout.contiguous()
     assert (t2.stride(0) * 2) % 16 != 0
@@ -133,24 +144,32 @@ def test_softcap_load_paths_agree_bitwise():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("ops", [[(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SCALE, 1 / 0.7)]])
-def test_full_size_transform_sampled_rows(ops):
+@pytest.mark.parametrize("ops", [[(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SCALE, 1 / 0.7)],
+                                 [(SOFTCAP, 30.0), (SCALE, 1 / 0.7), (SOFTCAP, 40.0)]])
+def test_full_size_transform_every_active_row(ops):
     """The Qwen workload with the chains the benchmark times (soft-cap then
-    temperature on the general path, temperature alone on the scale-only
-    path); sampled active rows against the oracle, and the metrics equal to
-    the oracle's metric function on the pass's own per-token values."""
+    temperature on the reduced soft-cap pass, temperature alone on the
+    scale-only pass, and a two-cap chain on the general pass): every active row
+    against the oracle on all host cores, the metrics against the oracle's
+    metric function of the oracle's own per-token dlogp."""
+    from oracle import stream
+
     w = W.qwen(device=DEV)
     res = B.score(w.train, w.rollout, w.token_ids, w.action_mask, w.clip, train_ops=ops, rollout_ops=ops)
     torch.cuda.synchronize()
     assert res.metrics["status"] == 0
     mask = w.action_mask.cpu().numpy()
-    rows = np.sort(np.random.default_rng(23).choice(np.flatnonzero(mask), size=48, replace=False))
-    sel = torch.as_tensor(rows, device=DEV)
-    ref = oracle.score_transformed(to_oracle(w.train[sel]), to_oracle(w.rollout[sel]), w.token_ids.cpu().numpy()[rows],
-                                   np.ones(rows.size, np.uint8), ops, ops, *w.clip)
+    act = np.flatnonzero(mask)
+    ref = stream.score_transformed_rows_device(w.train, w.rollout, w.token_ids, act, ops, ops)
+    errs = []
     for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout), (res.dlogp, ref.dlogp)):
-        assert np.max(np.abs(got[sel].cpu().numpy().astype(np.float64) - want)) <= LOGP_ATOL
-    d = res.dlogp.cpu().numpy().astype(np.float64)
-    prop = oracle.metrics(d, mask, *w.clip)
-    prop["status"] = 0
-    assert_metrics_match(res.metrics, prop, d, mask, w.clip, ambiguity=1e-6)
+        g = got.cpu().numpy().astype(np.float64)
+        errs.append(float(np.max(np.abs(g[act] - want))))
+    assert max(errs) <= LOGP_ATOL, errs
+    d = np.zeros(mask.size)
+    d[act] = ref.dlogp
+    ref_m = oracle.metrics(d, mask, *w.clip)
+    ref_m["status"] = ref.status
+    assert_metrics_match(res.metrics, ref_m, d, mask, w.clip, dlogp_err=errs[2])
+    del w, res
+    torch.cuda.empty_cache()

@@ -57,3 +57,14 @@ def test_threaded_head_rows_equal_serial():
     want = oracle.score_head_rows(ht, hr, wt, w.token_ids.numpy(), rows)
     got = stream.score_head_rows_parallel(ht, hr, wt, w.token_ids.numpy(), rows, chunk=2, threads=3)
     _same(got, want)
+
+
+def test_threaded_transformed_equal_serial():
+    w = W.synthetic(33, 500, seed=7, device="cpu", sigma=20.0, active_prob=1.0)
+    ops_t, ops_r = [(oracle.OP_SOFTCAP, 30.0), (oracle.OP_SCALE, 1.4)], [(oracle.OP_SCALE, 0.5)]
+    rows = np.array([32, 1, 2, 3, 10, 20])
+    want = oracle.score_transformed(to_oracle(w.train[rows]), to_oracle(w.rollout[rows]), w.token_ids.numpy()[rows],
+                                    np.ones(rows.size, np.uint8), ops_t, ops_r)
+    got = stream.score_transformed_rows_device(w.train, w.rollout, w.token_ids, rows, ops_t, ops_r, chunk=4,
+                                               threads=2)
+    _same(got, want)
