@@ -181,6 +181,12 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
+// max(|a|, |b|, |c|) in one instruction (NaN inputs are skipped)
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+    float r;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // ---- streaming form (row kernel and fused epilogue) -------------------------------
 // Streaming form of the state of lpd_acc.cuh: the three sums are kept as

@@ -134,11 +134,11 @@ bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
     out->p = static_cast<float>(p);
     out->r = static_cast<float>(r);
     out->r2 = static_cast<float>(r * r);
-    // |x| < 0.599 p gives fl(fl(x^2) / p^2) < 0.36 after every rounding
-    out->thr = static_cast<float>(0.599 * p);
+    // |x| < 0.449 p gives fl(fl(x^2) fl(1/p^2)) < 0.45^2 after every rounding
+    out->thr = static_cast<float>(0.449 * p);
     double rk = r * r;
     for (int k = 0; k < kSoftcapTerms; ++k, rk *= r * r) {
-        const double q = static_cast<double>(tanh_c(k)) * rk;
+        const double q = static_cast<double>(softcap_c(k)) * rk;
         if (!(std::fabs(q) > lo && std::fabs(q) < hi)) return false;
         out->q[k] = static_cast<float>(q);
     }

@@ -123,10 +123,10 @@ struct Xform {
 // all the chain's scales applied afterwards through the exponent factor.  A
 // scale a before the soft-cap moves behind it, softcap_p(a x) =
 // a softcap_{p/a}(x), so p here is the chain's soft-cap divided by the scales
-// in front of it.  On |x| < 0.6 p the series p tanh(x / p) = x (1 + u Q(u)),
-// u = x^2, runs with the coefficients of the fitted tanh series pre-multiplied
+// in front of it.  On |x| < 0.45 p the series p tanh(x / p) = x (1 + u Q(u)),
+// u = x^2, runs with the coefficients of its fitted tanh series pre-multiplied
 // by the powers of 1/p^2 (q[k] = c_k / p^(2k+2)); beyond, the exponential form.
-constexpr int kSoftcapTerms = 5;
+constexpr int kSoftcapTerms = 4;
 struct SoftcapSide {
     int on;                 // 0: no soft-cap on this side (identity)
     float p, r, r2;         // p, 1/p, 1/p^2

@@ -340,6 +340,40 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                             lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
                             lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
                         }
+                        if constexpr (kSoftcap) {
+                            // the soft-cap runs packed on all sixteen values, as
+                            // in a full tile: columns past the segment hold 0 while
+                            // it runs and become -inf afterwards
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) {
+                                const int col0 = slot_col<kGroupCols>(t, 2 * p);
+                                if (col0 >= nv) {
+                                    vt[p] = vr[p] = f2(0.f, 0.f);
+                                } else if (col0 + 1 >= min(nbt, nbr)) {
+                                    float x[2] = {f2_lo(vt[p]), f2_hi(vt[p])}, y[2] = {f2_lo(vr[p]), f2_hi(vr[p])};
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const int col = col0 + h;
+                                        if (col >= nbt) x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : 0.f;
+                                        if (col >= nbr) y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : 0.f;
+                                    }
+                                    vt[p] = f2(x[0], x[1]);
+                                    vr[p] = f2(y[0], y[1]);
+                                }
+                            }
+                            if (a.cap[0].on) softcap16_u(vt, a.cap[0]);
+                            if (a.cap[1].on) softcap16_u(vr, a.cap[1]);
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) {
+                                const int col0 = slot_col<kGroupCols>(t, 2 * p);
+                                if (col0 + 1 >= nv) {
+                                    const float lt = col0 < nv ? f2_lo(vt[p]) : -INFINITY;
+                                    const float lr = col0 < nv ? f2_lo(vr[p]) : -INFINITY;
+                                    vt[p] = f2(lt, -INFINITY);
+                                    vr[p] = f2(lr, -INFINITY);
+                                }
+                            }
+                        } else {
 #pragma unroll
                         for (int p = 0; p < 8; ++p) {
                             const int col0 = slot_col<kGroupCols>(t, 2 * p);  // the pair is col0, col0 + 1
@@ -352,17 +386,18 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                                     const int col = col0 + h;
                                     if (col >= nbt) x[h] = col < nv ? ldg_elem<DT>(tb + (c0 + col) * DT::kBytes) : -INFINITY;
                                     if (col >= nbr) y[h] = col < nv ? ldg_elem<DR>(rb + (c0 + col) * DR::kBytes) : -INFINITY;
-                                    if ((kXform || kSoftcap) && col < nv) {
+                                    if (kXform && col < nv) {
                                         x[h] = tf_t(x[h]);
                                         y[h] = tf_r(y[h]);
                                     }
                                 }
                                 vt[p] = f2(x[0], x[1]);
                                 vr[p] = f2(y[0], y[1]);
-                            } else if (kXform || kSoftcap) {
+                            } else if (kXform) {
                                 vt[p] = f2(tf_t(f2_lo(vt[p])), tf_t(f2_hi(vt[p])));
                                 vr[p] = f2(tf_r(f2_lo(vr[p])), tf_r(f2_hi(vr[p])));
                             }
+                        }
                         }
                     }
                     __syncwarp();
@@ -391,7 +426,7 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                 accumulate16<kEntropy>(vt, vr, acc2, lg_t, lg_r);
                 return true;
             };
-            if constexpr (kXform || kSoftcap) {
+            if constexpr (kXform) {
                 // the transform chain's larger body: full tiles in a tight loop,
                 // the segment's ragged last tile after it (measured faster)
                 int64_t c0 = 0;

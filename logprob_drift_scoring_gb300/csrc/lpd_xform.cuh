@@ -102,27 +102,43 @@ __device__ __forceinline__ void softcap16(f2_t *v, float p, float rcp) {
 }
 
 // ---- the reduced single soft-cap (kRowSoftcap) --------------------------------
-// One value: the series on u = x^2 when u / p^2 < 0.36 (the same range as the
-// general form's z < 0.36), else p tanh(x / p) in the exponential form.
+// Its own fit: degree 3 on |y| < 0.45 (csrc/tanh_coeffs.py 0.45 3: 0.67 ulp in
+// float32, one fused multiply-add less per value than the degree-4 fit above),
+// evaluated on u = x^2 with the coefficients pre-multiplied by the powers of
+// 1/p^2 (SoftcapSide::q), so p tanh(x / p) = x (1 + u Q(u)).  Beyond the range,
+// the exponential form above.  With logits of a few units and p around 30 the
+// exponential form is almost never needed.
+constexpr float kSoftcapZMax = 0.2025f;  // 0.45^2
+__host__ __device__ constexpr float softcap_c(int k) {
+    return k == 0 ? -3.333319426e-01f : k == 1 ? 1.332776695e-01f : k == 2 ? -5.322368443e-02f : 1.772576943e-02f;
+}
+
+__device__ __forceinline__ float softcap_series(float x, float u, const SoftcapSide &c) {
+    float q = c.q[kSoftcapTerms - 1];
+#pragma unroll
+    for (int k = kSoftcapTerms - 2; k >= 0; --k) q = __fmaf_rn(q, u, c.q[k]);
+    return __fmaf_rn(x, __fmul_rn(u, q), x);
+}
+
+// One value: the series when u / p^2 < 0.45^2, else the exponential form.
 __device__ __forceinline__ float softcap_u1(float x, const SoftcapSide &c) {
     const float u = __fmul_rn(x, x);
-    if (__fmul_rn(u, c.r2) < kTanhZMax) {
-        float q = c.q[kSoftcapTerms - 1];
-#pragma unroll
-        for (int k = kSoftcapTerms - 2; k >= 0; --k) q = __fmaf_rn(q, u, c.q[k]);
-        return __fmaf_rn(x, __fmul_rn(u, q), x);
-    }
-    return __fmul_rn(c.p, tanh_exp(__fmul_rn(x, c.r)));
+    return __fmul_rn(u, c.r2) < kSoftcapZMax ? softcap_series(x, u, c) : __fmul_rn(c.p, tanh_exp(__fmul_rn(x, c.r)));
 }
 
 // Sixteen values in place.  When every |x| of the warp is below c.thr (set on
-// the host a little under 0.6 p, so that softcap_u1 would take its series for
-// each of them) the series runs packed with nothing else kept live; otherwise
-// each value takes softcap_u1.  Either way a value gets softcap_u1's bits.
+// the host a little under 0.45 p, so that softcap_u1 takes its series for each
+// of them) the series runs packed, one value pair at a time.  Otherwise both
+// forms run and each value keeps the one softcap_u1 would pick.  Either way a
+// value gets softcap_u1's bits.
 __device__ __forceinline__ void softcap16_u(f2_t *v, const SoftcapSide &c) {
-    float amax = fmaxf(fabsf(f2_lo(v[0])), fabsf(f2_hi(v[0])));
-#pragma unroll
-    for (int q = 1; q < 8; ++q) amax = max3(amax, fabsf(f2_lo(v[q])), fabsf(f2_hi(v[q])));
+    const float a0 = max3_abs(f2_lo(v[0]), f2_hi(v[0]), f2_lo(v[1]));
+    const float a1 = max3_abs(f2_hi(v[1]), f2_lo(v[2]), f2_hi(v[2]));
+    const float a2 = max3_abs(f2_lo(v[3]), f2_hi(v[3]), f2_lo(v[4]));
+    const float a3 = max3_abs(f2_hi(v[4]), f2_lo(v[5]), f2_hi(v[5]));
+    const float a4 = max3_abs(f2_lo(v[6]), f2_hi(v[6]), f2_lo(v[7]));
+    const float amax = fmaxf(max3(a0, a1, a2), max3_abs(a3, a4, f2_hi(v[7])));
+    // NaN is skipped by the maximum; the series carries it through
     if (__all_sync(0xffffffffu, amax < c.thr)) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {

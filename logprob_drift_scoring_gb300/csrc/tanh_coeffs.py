@@ -1,8 +1,12 @@
-"""Derives the polynomial of the soft-cap tanh (lpd_xform.cuh).
+"""Derives the polynomials of the soft-cap tanh (lpd_xform.cuh).
 
-tanh(y) = y * (1 + z * P(z)), z = y^2, for z < 0.36 (|y| < 0.6).  P has
-degree 4 and is a weighted least-squares fit of (tanh(y)/y - 1) / z on 4000
-Chebyshev nodes of z in [0, 0.36].  The weight z * y / tanh(y) makes the
+tanh(y) = y * (1 + z * P(z)), z = y^2, on |y| < Y_MAX.  Two fits are used:
+degree 4 on |y| < 0.6 (the general per-op chain) and degree 3 on |y| < 0.45
+(the reduced single soft-cap pass, which evaluates the same series on x^2 with
+the coefficients pre-multiplied by powers of 1/p^2; one fused multiply-add
+less per value, and 0.67 ulp in float32 on its range).  Each P is a weighted
+least-squares fit of (tanh(y)/y - 1) / z on Chebyshev nodes of z in
+[0, Y_MAX^2].  The weight z * y / tanh(y) makes the
 residual the relative error of tanh, and 30 reweighting passes push the fit
 towards equal-ripple.  The coefficients are rounded to float32, and the script
 reports the worst error of a float32 Horner evaluation (one rounding per fused
@@ -11,6 +15,7 @@ multiply-add) against 40-digit tanh, in units in the last place: 0.63 ulp
 y (1 + z P) dominates once the fit is below it).
 
 Run: python tanh_coeffs.py   (needs numpy and mpmath; not used at build time)
+     python tanh_coeffs.py 0.45 3   (the reduced pass's fit)
 """
 import numpy as np
 from mpmath import mp, mpf, tanh as mtanh
@@ -60,6 +65,10 @@ def worst_ulp(cf, samples=20001):
 
 
 if __name__ == "__main__":
+    import sys
+
+    if len(sys.argv) == 3:
+        Y_MAX, DEGREE = float(sys.argv[1]), int(sys.argv[2])
     cf = fit()
     print("coefficients c0..c%d:" % DEGREE, ", ".join(f"{float(v):.9e}f" for v in cf))
     print("worst float32 error: %.3f ulp" % worst_ulp(cf))
