@@ -91,6 +91,8 @@ extern "C" {
 
 /* ---- result flags (lpd_metrics.flags) --------------------------------- */
 #define LPD_FLAG_NO_ACTIVE 1u /* zero active tokens: every metric is 0 */
+#define LPD_FLAG_NO_PERCENTILES 2u /* p95 / p99 not available (a record merged from
+                                    * per-rank records): NaN */
 
 /* ---- workspace kinds --------------------------------------------------- */
 #define LPD_KIND_SCORE 0   /* lpd_score and its stages */
@@ -264,6 +266,30 @@ int lpd_token_logp(const lpd_logits *train, const lpd_logits *rollout, int64_t n
 int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi,
                       lpd_metrics *out_metrics, void *workspace, size_t workspace_bytes,
                       void *stream);
+
+/* Global metrics of a data-parallel run from its per-rank records ("WS2
+ * Cross-Config Logprob Drift Contract", "Diagnostics": the same metrics per
+ * rank and globally), where only the small records are exchanged.  HOST call,
+ * no GPU work: per_rank is a host array of n_ranks lpd_metrics in rank order
+ * (each rank's lpd_score record, copied to the host), row_offsets an optional
+ * host int64[n_ranks] mapping each rank's local rows to global ones (NULL: all
+ * 0), out a host record.  Combined exactly, visiting ranks in rank order so
+ * the result does not depend on the collective that gathered them:
+ *   n_active    the sum;  status  the OR;
+ *   ratio0_mean, clipfrac0, approx_kl0, mean_abs_dlogp
+ *               means weighted by each rank's n_active (sum of a_k m_k in rank
+ *               order, divided by the total);
+ *   max_abs_dlogp, argmax_row
+ *               the largest per-rank maximum; ties go to the earlier rank,
+ *               whose rows come first; argmax_row + that rank's offset;
+ *   p95 / p99   NaN, with LPD_FLAG_NO_PERCENTILES: percentiles of the union are
+ *               not a function of per-rank ones (gather the per-token dlogp and
+ *               use lpd_drift_metrics_from_dlogp for them);
+ *   flags       LPD_FLAG_NO_ACTIVE when the total is 0 (every mean 0, argmax -1).
+ * Ranks with n_active == 0 contribute only their status.  Returns
+ * LPD_ERR_NULL_POINTER / LPD_ERR_BAD_SIZE (n_ranks < 1 or a negative count). */
+int lpd_merge_rank_metrics(const lpd_metrics *per_rank, const int64_t *row_offsets, int32_t n_ranks,
+                           lpd_metrics *out);
 
 /* Stage 3 over caller-given per-token values: the metrics record of the
  * rows with action_mask != 0, with d = dlogp[r] (float32, widened exactly) in

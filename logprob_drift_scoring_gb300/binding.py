@@ -32,6 +32,7 @@ LPD_STATUS_TOKEN_OOB = 1
 LPD_STATUS_NONFINITE = 2
 LPD_STATUS_TIMEOUT = 4
 LPD_FLAG_NO_ACTIVE = 1
+LPD_FLAG_NO_PERCENTILES = 2
 LPD_KIND_SCORE, LPD_KIND_SHARDED = 0, 1
 LPD_TOPO_ALLGATHER_PARTIALS_FIXED_MERGE, LPD_TOPO_ALLREDUCE_PARTIALS, LPD_TOPO_ALLGATHER_LOGITS = 0, 1, 2
 TOPOLOGIES = {"allgather_partials_fixed_merge": 0, "allreduce_partials": 1, "allgather_logits": 2}
@@ -114,7 +115,7 @@ EXPORTED = ("lpd_workspace_size", "lpd_backend_info", "lpd_strerror", "lpd_score
             "lpd_fused_workspace_size", "lpd_score_fused", "lpd_score_fused_transformed", "lpd_score_transformed",
             "lpd_score_entropy", "lpd_logprob_backward", "lpd_attn_merge", "lpd_attn_merge_order_drift",
             "lpd_topology_workspace_size", "lpd_score_sharded_topology", "lpd_drift_metrics_from_dlogp",
-            "lpd_logp_drift_summary")
+            "lpd_logp_drift_summary", "lpd_merge_rank_metrics")
 LPD_NOALLOC_MAX_ROWS = 32768
 LPD_ATTN_MAX_PARTS = 64
 
@@ -178,6 +179,8 @@ def lib() -> ctypes.CDLL:
         L.lpd_attn_merge_order_drift.restype = ctypes.c_int
         L.lpd_attn_merge_order_drift.argtypes = [P, I32, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P]
         L.lpd_logp_drift_summary.restype = ctypes.c_int
+        L.lpd_merge_rank_metrics.restype = ctypes.c_int
+        L.lpd_merge_rank_metrics.argtypes = [P, P, I32, P]
         L.lpd_logp_drift_summary.argtypes = [I64, P, P, P, P, P, P, P]
         _LIB = L
     return _LIB
@@ -521,6 +524,22 @@ def logp_drift_summary(logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_
     out = torch.empty(LOGP_DRIFT_BYTES, dtype=torch.uint8, device=action_mask.device)
     lpd_logp_drift_summary(logp_train_a, logp_rollout_a, logp_train_b, logp_rollout_b, action_mask, out, stream)
     return read_logp_drift(out)
+
+
+def merge_rank_metrics(per_rank: list[dict], row_offsets: list[int] | None = None) -> dict:
+    """lpd_merge_rank_metrics (a host call) on metrics records given as dicts
+    in rank order; returns the merged record as a dict."""
+    n = len(per_rank)
+    arr = (LpdMetrics * max(n, 1))()
+    for k, rec in enumerate(per_rank):
+        for name, _ in LpdMetrics._fields_:
+            setattr(arr[k], name, rec.get(name, 0))
+    offs = None if row_offsets is None else (ctypes.c_int64 * max(n, 1))(*[int(o) for o in row_offsets])
+    out = LpdMetrics()
+    rc = lib().lpd_merge_rank_metrics(ctypes.addressof(arr), None if offs is None else ctypes.addressof(offs), n,
+                                      ctypes.addressof(out))
+    _check(rc, "lpd_merge_rank_metrics")
+    return out.as_dict()
 
 
 def read_metrics(buf) -> dict:

@@ -125,7 +125,11 @@ bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
         }
     }
     *post = pre * after;
-    if (n_cap == 0) return true;
+    if (n_cap == 0) {
+        // no soft-cap: zero series coefficients leave every |x| < 1e18 as it is
+        out->thr = 1e18f;
+        return true;
+    }
     if (n_cap > 1) return false;
     const double p = cap / pre, r = pre / cap;
     const double lo = 1e-36, hi = 1e36;
@@ -519,6 +523,47 @@ int lpd_drift_metrics(int64_t n_rows, double clip_lo, double clip_hi, lpd_metric
         return rc;
     const Ws w = carve(workspace, n_rows, 1);
     return run_metrics(n_rows, clip_lo, clip_hi, out_metrics, w, static_cast<cudaStream_t>(stream));
+}
+
+int lpd_merge_rank_metrics(const lpd_metrics *per_rank, const int64_t *row_offsets, int32_t n_ranks,
+                           lpd_metrics *out) {
+    if (!per_rank || !out) return LPD_ERR_NULL_POINTER;
+    if (n_ranks < 1) return LPD_ERR_BAD_SIZE;
+    for (int k = 0; k < n_ranks; ++k)
+        if (per_rank[k].n_active < 0) return LPD_ERR_BAD_SIZE;
+    lpd_metrics m{};
+    m.argmax_row = -1;
+    double best = -1.0;
+    for (int k = 0; k < n_ranks; ++k) {
+        const lpd_metrics &r = per_rank[k];
+        m.status |= r.status;
+        const int64_t a = r.n_active;
+        if (a == 0) continue;
+        m.n_active += a;
+        const double w = static_cast<double>(a);
+        m.ratio0_mean += r.ratio0_mean * w;
+        m.clipfrac0 += r.clipfrac0 * w;
+        m.approx_kl0 += r.approx_kl0 * w;
+        m.mean_abs_dlogp += r.mean_abs_dlogp * w;
+        if (r.max_abs_dlogp > best) {  // strict: an earlier rank's rows come first
+            best = r.max_abs_dlogp;
+            m.max_abs_dlogp = best;
+            m.argmax_row = r.argmax_row + (row_offsets ? row_offsets[k] : 0);
+        }
+    }
+    if (m.n_active > 0) {
+        const double total = static_cast<double>(m.n_active);
+        m.ratio0_mean /= total;
+        m.clipfrac0 /= total;
+        m.approx_kl0 /= total;
+        m.mean_abs_dlogp /= total;
+        m.p95_abs_dlogp = m.p99_abs_dlogp = std::nan("");
+        m.flags = LPD_FLAG_NO_PERCENTILES;
+    } else {
+        m.flags = LPD_FLAG_NO_ACTIVE;
+    }
+    *out = m;
+    return LPD_OK;
 }
 
 int lpd_drift_metrics_from_dlogp(int64_t n_rows, const float *dlogp, const uint8_t *action_mask, double clip_lo,

@@ -8,10 +8,11 @@ per-rank metric records (torch.distributed, any backend) and combines them:
 
 * gather_rank_metrics: every rank's metrics record, in rank order;
 * merge_rank_metrics: the global values that can be combined exactly from the
-  records: the active-token count, the token-weighted means (ratio0_mean,
-  clipfrac0, approx_kl0, mean_abs_dlogp) and the worst token (largest
-  max_abs_dlogp, lowest global row on ties).  Percentiles of the union are not
-  a function of per-rank percentiles;
+  records (the library's lpd_merge_rank_metrics, a host call): the
+  active-token count, the token-weighted means (ratio0_mean, clipfrac0,
+  approx_kl0, mean_abs_dlogp) and the worst token (largest max_abs_dlogp,
+  lowest global row on ties).  Percentiles of the union are not a function of
+  per-rank percentiles;
 * gather_rank_rows / global_drift_metrics: every rank's per-token dlogp and
   mask (5 bytes a row) gathered in rank order, and the full metrics record of
   the union computed from them on the GPU (lpd_drift_metrics_from_dlogp),
@@ -22,8 +23,6 @@ collective's algorithm or arrival order ("[WS2] Framework for ablation
 experiment", LogProb knobs table, row 5: merge order as a drift source).
 """
 from __future__ import annotations
-
-MEAN_KEYS = ("ratio0_mean", "clipfrac0", "approx_kl0", "mean_abs_dlogp")
 
 
 def gather_rank_metrics(metrics: dict, *, rank_meta: dict | None = None, group=None) -> list[dict]:
@@ -41,30 +40,13 @@ def gather_rank_metrics(metrics: dict, *, rank_meta: dict | None = None, group=N
 
 
 def merge_rank_metrics(per_rank: list[dict], row_offsets: list[int] | None = None) -> dict:
-    """Global metrics from per-rank records taken in rank order.  row_offsets[k]
-    maps rank k's local row indices to global ones (default 0)."""
-    offsets = row_offsets or [0] * len(per_rank)
-    total = sum(int(r["n_active"]) for r in per_rank)
-    out = {"n_active": total, "status": 0, "flags": 0 if total else 1, "argmax_row": -1,
-           "max_abs_dlogp": 0.0}
-    for k in MEAN_KEYS:
-        out[k] = 0.0
-    best = -1.0
-    for r, off in zip(per_rank, offsets):
-        out["status"] |= int(r["status"])
-        a = int(r["n_active"])
-        if a == 0:
-            continue
-        for k in MEAN_KEYS:
-            out[k] += r[k] * a
-        if r["max_abs_dlogp"] > best:  # strict: earlier ranks hold lower global rows
-            best = r["max_abs_dlogp"]
-            out["max_abs_dlogp"] = best
-            out["argmax_row"] = int(r["argmax_row"]) + int(off)
-    if total:
-        for k in MEAN_KEYS:
-            out[k] /= total
-    return out
+    """Global metrics from per-rank records taken in rank order
+    (lpd_merge_rank_metrics: the arithmetic is the library's).  row_offsets[k]
+    maps rank k's local row indices to global ones (default 0).  p95/p99 come
+    back NaN with LPD_FLAG_NO_PERCENTILES set."""
+    from logprob_drift_scoring_gb300 import binding as B
+
+    return B.merge_rank_metrics(per_rank, row_offsets)
 
 
 def gather_rank_rows(local_dlogp, local_mask, group=None):
