@@ -324,10 +324,7 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                             xform16(vt, cxt);
                             xform16(vr, cxr);
                         }
-                        if (kSoftcap) {
-                            if (a.cap[0].on) softcap16_u(vt, a.cap[0]);
-                            if (a.cap[1].on) softcap16_u(vr, a.cap[1]);
-                        }
+                        if (kSoftcap) softcap32_u(vt, vr, a.cap[0], a.cap[1]);
                     } else {
                         // ragged last tile: the same vector loads, then the
                         // columns the bulk copy did not cover (a few bytes at the
@@ -361,8 +358,7 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
                                     vr[p] = f2(y[0], y[1]);
                                 }
                             }
-                            if (a.cap[0].on) softcap16_u(vt, a.cap[0]);
-                            if (a.cap[1].on) softcap16_u(vr, a.cap[1]);
+                            softcap32_u(vt, vr, a.cap[0], a.cap[1]);
 #pragma unroll
                             for (int p = 0; p < 8; ++p) {
                                 const int col0 = slot_col<kGroupCols>(t, 2 * p);

@@ -117,7 +117,7 @@ __device__ __forceinline__ float softcap_series(float x, float u, const SoftcapS
     float q = c.q[kSoftcapTerms - 1];
 #pragma unroll
     for (int k = kSoftcapTerms - 2; k >= 0; --k) q = __fmaf_rn(q, u, c.q[k]);
-    return __fmaf_rn(x, __fmul_rn(u, q), x);
+    return __fmaf_rn(__fmul_rn(x, u), q, x);
 }
 
 // One value: the series when u / p^2 < 0.45^2, else the exponential form.
@@ -126,31 +126,51 @@ __device__ __forceinline__ float softcap_u1(float x, const SoftcapSide &c) {
     return __fmul_rn(u, c.r2) < kSoftcapZMax ? softcap_series(x, u, c) : __fmul_rn(c.p, tanh_exp(__fmul_rn(x, c.r)));
 }
 
-// Sixteen values in place.  When every |x| of the warp is below c.thr (set on
-// the host a little under 0.45 p, so that softcap_u1 takes its series for each
-// of them) the series runs packed, one value pair at a time.  Otherwise both
-// forms run and each value keeps the one softcap_u1 would pick.  Either way a
-// value gets softcap_u1's bits.
-__device__ __forceinline__ void softcap16_u(f2_t *v, const SoftcapSide &c) {
+__device__ __forceinline__ float amax16(const f2_t *v) {
     const float a0 = max3_abs(f2_lo(v[0]), f2_hi(v[0]), f2_lo(v[1]));
     const float a1 = max3_abs(f2_hi(v[1]), f2_lo(v[2]), f2_hi(v[2]));
     const float a2 = max3_abs(f2_lo(v[3]), f2_hi(v[3]), f2_lo(v[4]));
     const float a3 = max3_abs(f2_hi(v[4]), f2_lo(v[5]), f2_hi(v[5]));
     const float a4 = max3_abs(f2_lo(v[6]), f2_hi(v[6]), f2_lo(v[7]));
-    const float amax = fmaxf(max3(a0, a1, a2), max3_abs(a3, a4, f2_hi(v[7])));
-    // NaN is skipped by the maximum; the series carries it through
-    if (__all_sync(0xffffffffu, amax < c.thr)) {
+    return fmaxf(max3(a0, a1, a2), max3_abs(a3, a4, f2_hi(v[7])));
+}
+
+// The series on one value pair: x + (x u) Q(u).
+__device__ __forceinline__ f2_t softcap_series2(f2_t x, const SoftcapSide &c) {
+    const f2_t u = mul2(x, x);
+    const f2_t xu = mul2(x, u);
+    f2_t w = f2(c.q[kSoftcapTerms - 1], c.q[kSoftcapTerms - 1]);
+#pragma unroll
+    for (int k = kSoftcapTerms - 2; k >= 0; --k) w = fma2(w, u, f2(c.q[k], c.q[k]));
+    return fma2(xu, w, x);
+}
+
+// Sixteen values of each side in place, both sides' soft-caps at once.  When
+// every |x| of the warp is below its side's c.thr (set on the host a little
+// under 0.45 p, so that softcap_u1 takes its series for each of them) the
+// series runs packed on both sides, one range test and one warp vote per
+// tile.  Otherwise each value takes softcap_u1.  Either way a value gets
+// softcap_u1's bits.  A side without a soft-cap carries zero coefficients (its
+// series is x + (x u) 0 = x for every |x| below its threshold of 1e18) and is
+// left alone on the slow path.
+__device__ __forceinline__ void softcap32_u(f2_t *vt, f2_t *vr, const SoftcapSide &ct, const SoftcapSide &cr) {
+    const float at = amax16(vt), ar = amax16(vr);
+    // NaN is skipped by the maxima; the series carries it through
+    if (__all_sync(0xffffffffu, at < ct.thr && ar < cr.thr)) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const f2_t u = mul2(v[q], v[q]);
-            f2_t w = f2(c.q[kSoftcapTerms - 1], c.q[kSoftcapTerms - 1]);
-#pragma unroll
-            for (int k = kSoftcapTerms - 2; k >= 0; --k) w = fma2(w, u, f2(c.q[k], c.q[k]));
-            v[q] = fma2(v[q], mul2(u, w), v[q]);
+            vt[q] = softcap_series2(vt[q], ct);
+            vr[q] = softcap_series2(vr[q], cr);
         }
     } else {
+        if (ct.on) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = f2(softcap_u1(f2_lo(v[q]), c), softcap_u1(f2_hi(v[q]), c));
+            for (int q = 0; q < 8; ++q) vt[q] = f2(softcap_u1(f2_lo(vt[q]), ct), softcap_u1(f2_hi(vt[q]), ct));
+        }
+        if (cr.on) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) vr[q] = f2(softcap_u1(f2_lo(vr[q]), cr), softcap_u1(f2_hi(vr[q]), cr));
+        }
     }
 }
 
