@@ -211,11 +211,12 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
     a.pick = w.pick;
     a.status = &met->status;
     a.stall = stall_requested() ? 1 : 0;
-    int rc = cuda_status(launch_rows(a, dt, dr, tma, mode, s));
+    const int warps = row_pass_warps(segs, n_seg, mode, tma);
+    int rc = cuda_status(launch_rows(a, dt, dr, tma, mode, warps, s));
     if (rc) return rc;
     FinArgs f{};
     f.n_seg = n_seg;
-    f.n_warps = row_warps(mode);
+    f.n_warps = warps;
     f.n_perm = n_perm;
     for (int j = 0; j < n_perm; ++j) f.perm[j] = static_cast<int8_t>(perm[j]);
     f.vocab = vocab;

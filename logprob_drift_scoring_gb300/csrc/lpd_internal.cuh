@@ -201,7 +201,14 @@ cudaError_t launch_select_active(int64_t n_rows, const uint8_t *mask, const int3
                                  float *out_lt, float *out_lr, float *out_d,
                                  lpd_metrics *metrics, WsHeader *hdr, int2 *rowid,
                                  cudaStream_t stream);
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream);
+// Consumer warps of the row pass for these segments (the mode's default, or
+// for the plain bulk-copy pass over several segments the count whose tiles
+// waste the fewest columns on the segments' last tiles: 20, 19 or 16); a
+// function of the segment lengths only, so every row keeps its arithmetic in
+// any batch.
+int row_pass_warps(const Segment *segs, int n_seg, int mode, bool use_tma);
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, int warps,
+                        cudaStream_t stream);
 cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t stream);
 cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader *hdr, const int2 *rowid,
                               double *dval, uint32_t *keys, uint32_t *status, cudaStream_t stream);

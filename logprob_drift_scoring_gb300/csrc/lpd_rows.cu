@@ -173,14 +173,14 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
 // with a chain of at most one soft-cap per side in its reduced form (the
 // soft-cap on each loaded value, the scales folded into the exponent factor
 // as in mode 3).
-template <class DT, class DR, bool kTma, int kMode>
-__global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
+template <class DT, class DR, bool kTma, int kMode, int kW>
+__global__ void __launch_bounds__(kW * 32 + 32, 1)
     row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     constexpr bool kXform = kMode == kRowTransform;
     constexpr bool kEntropy = kMode == kRowEntropy;
     constexpr bool kScale = kMode == kRowScale;
     constexpr bool kSoftcap = kMode == kRowSoftcap;
-    constexpr int kWarps = row_warps(kMode);
+    constexpr int kWarps = kW;
     constexpr int kGroupCols = 4 * 32 * kWarps;
     constexpr int kTile = kColsPerThread * 32 * kWarps;
     extern __shared__ __align__(1024) char smem[];
@@ -443,13 +443,13 @@ __global__ void __launch_bounds__(row_warps(kMode) * 32 + 32, 1)
     }
 }
 
-template <class DT, class DR, bool kTma, int kMode>
+template <class DT, class DR, bool kTma, int kMode, int kW = row_warps(kMode)>
 cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
-    constexpr int kThreads = row_warps(kMode) * 32 + 32;  // + producer warp
-    const int stage_bytes = kColsPerThread * 32 * row_warps(kMode) * (DT::kBytes + DR::kBytes);
+    constexpr int kThreads = kW * 32 + 32;  // + producer warp
+    const int stage_bytes = kColsPerThread * 32 * kW * (DT::kBytes + DR::kBytes);
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
-    auto kern = row_kernel<DT, DR, kTma, kMode>;
+    auto kern = row_kernel<DT, DR, kTma, kMode, kW>;
     static std::atomic<uint64_t> configured{0};
     const cudaError_t e = set_smem_once(kern, smem, configured);
     if (e != cudaSuccess) return e;
@@ -457,12 +457,12 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool kTma, int kMode>
+template <bool kTma, int kMode, int kW = row_warps(kMode)>
 cudaError_t dispatch(const RowArgs &a, int dt, int dr, cudaStream_t stream) {
-    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kMode>(a, stream);
-    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kMode>(a, stream);
-    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kMode>(a, stream);
-    return launch_typed<F32, F32, kTma, kMode>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kMode, kW>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kMode, kW>(a, stream);
+    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kMode, kW>(a, stream);
+    return launch_typed<F32, F32, kTma, kMode, kW>(a, stream);
 }
 
 template <int kMode>
@@ -472,7 +472,30 @@ cudaError_t dispatch_path(const RowArgs &a, int dt, int dr, bool use_tma, cudaSt
 
 }  // namespace
 
-cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, cudaStream_t stream) {
+int row_pass_warps(const Segment *segs, int n_seg, int mode, bool use_tma) {
+    if (mode != kRowPlain || !use_tma || n_seg < 2) return row_warps(mode);
+    // the plain bulk-copy pass over several vocab segments: the consumer-warp
+    // count (tile width 512 W) whose tiles cover the segments with the fewest
+    // columns; each segment's last tile is padded to a whole tile, which costs
+    // as much as real columns.  Ties keep the most warps.
+    int best = row_warps(mode);
+    int64_t best_cols = -1;
+    for (int w : {20, 19, 16}) {
+        const int64_t tile = static_cast<int64_t>(kColsPerThread) * 32 * w;
+        int64_t cols = 0;
+        for (int k = 0; k < n_seg; ++k) cols += (segs[k].len + tile - 1) / tile * tile;
+        if (best_cols < 0 || cols < best_cols) {
+            best = w;
+            best_cols = cols;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, int warps,
+                        cudaStream_t stream) {
+    if (mode == kRowPlain && use_tma && warps == 19) return dispatch<true, kRowPlain, 19>(a, dtype_t, dtype_r, stream);
+    if (mode == kRowPlain && use_tma && warps == 16) return dispatch<true, kRowPlain, 16>(a, dtype_t, dtype_r, stream);
     if (mode == kRowTransform) return dispatch_path<1>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowSoftcap) return dispatch_path<4>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowEntropy) return dispatch_path<2>(a, dtype_t, dtype_r, use_tma, stream);
