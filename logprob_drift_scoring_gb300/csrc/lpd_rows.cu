@@ -337,7 +337,38 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                             lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
                             lds4<DR>(stg + kStageT, g * kGroupCols + 4 * t, vr + 2 * g);
                         }
-                        if constexpr (kSoftcap) {
+                        constexpr bool kChain = kXform || kSoftcap;
+                        if (nbt == nv && nbr == nv) {
+                            // the copy holds every real column (the segment's
+                            // length in bytes is a multiple of 16 on both sides,
+                            // the same for every thread): columns past the end
+                            // are selected away without branches; a chain runs
+                            // packed on all sixteen values, as in a full tile,
+                            // with 0 in those columns, which become -inf after it
+                            const float fill = kChain ? 0.f : -INFINITY;
+#pragma unroll
+                            for (int p = 0; p < 8; ++p) {
+                                const int col0 = slot_col<kGroupCols>(t, 2 * p);
+                                const bool in0 = col0 < nv, in1 = col0 + 1 < nv;
+                                vt[p] = f2(in0 ? f2_lo(vt[p]) : fill, in1 ? f2_hi(vt[p]) : fill);
+                                vr[p] = f2(in0 ? f2_lo(vr[p]) : fill, in1 ? f2_hi(vr[p]) : fill);
+                            }
+                            if constexpr (kChain) {
+                                if constexpr (kXform) {
+                                    xform16(vt, cxt);
+                                    xform16(vr, cxr);
+                                } else {
+                                    softcap32_u(vt, vr, a.cap[0], a.cap[1]);
+                                }
+#pragma unroll
+                                for (int p = 0; p < 8; ++p) {
+                                    const int col0 = slot_col<kGroupCols>(t, 2 * p);
+                                    const bool in0 = col0 < nv, in1 = col0 + 1 < nv;
+                                    vt[p] = f2(in0 ? f2_lo(vt[p]) : -INFINITY, in1 ? f2_hi(vt[p]) : -INFINITY);
+                                    vr[p] = f2(in0 ? f2_lo(vr[p]) : -INFINITY, in1 ? f2_hi(vr[p]) : -INFINITY);
+                                }
+                            }
+                        } else if constexpr (kSoftcap) {
                             // the soft-cap runs packed on all sixteen values, as
                             // in a full tile: columns past the segment hold 0 while
                             // it runs and become -inf afterwards

@@ -20,7 +20,8 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from . import Result, load, score_head_rows, score_rows, score_sharded, score_transformed
+from . import (Result, entropy, load, logprob_backward_row, score_head_rows, score_rows, score_sharded,
+               score_transformed)
 
 
 def host_threads(threads: int | None = None) -> int:
@@ -174,3 +175,54 @@ def score_rows_parallel(train, rollout, token_ids, rows, chunk: int = 64, thread
 
     res = _run_chunks(chunks(), work, threads)
     return _concat([res[k] for k in sorted(res)])
+
+
+def entropy_rows_device(train, rollout, rows, chunk: int = 64, threads: int | None = None):
+    """oracle.entropy of the listed rows (every listed row active): the two
+    sides' softmax entropies, in ``rows`` order."""
+    import torch
+
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dev = train.device
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            sel = torch.as_tensor(rows[c:c + chunk], device=dev)
+            yield c, (_host(train.index_select(0, sel)), _host(rollout.index_select(0, sel)))
+
+    def work(p):
+        t, r = p
+        return entropy(t, r, np.ones(t.shape[0], np.uint8), lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    keys = sorted(res)
+    if not keys:
+        return np.zeros(0), np.zeros(0)
+    return np.concatenate([res[k][0] for k in keys]), np.concatenate([res[k][1] for k in keys])
+
+
+def backward_rows_device(logits, token_ids, grad, rows, chunk: int = 8, threads: int | None = None):
+    """oracle.logprob_backward_row of each listed row (grad[r] * d logp / d
+    logits), as a [len(rows), V] float64 array in ``rows`` order."""
+    import torch
+
+    lib = load()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dev = logits.device
+    ids = token_ids.detach().cpu().numpy().astype(np.int64)
+    g = grad.detach().double().cpu().numpy()
+
+    def chunks():
+        for c in range(0, rows.size, chunk):
+            sel_np = rows[c:c + chunk]
+            yield c, (_host(logits.index_select(0, torch.as_tensor(sel_np, device=dev))), sel_np)
+
+    def work(p):
+        x, sel_np = p
+        return np.stack([logprob_backward_row(np.ascontiguousarray(x[j]), int(ids[r]), float(g[r]), lib=lib)
+                         for j, r in enumerate(sel_np)])
+
+    res = _run_chunks(chunks(), work, threads)
+    keys = sorted(res)
+    return np.concatenate([res[k] for k in keys]) if keys else np.zeros((0, logits.shape[1]))

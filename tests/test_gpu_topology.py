@@ -150,25 +150,39 @@ def test_arms_edge_cases():
 
 
 @pytest.mark.slow
-def test_full_size_arms_on_sampled_rows():
+def test_full_size_arms_every_row():
     """The 4-way vocab split of 32768 rows x 151936 in the benchmark's launch
-    configuration; sampled rows of each arm against the oracle."""
+    configuration; every row of each arm against the oracle (all host cores).
+    The fixed-merge and all-gather arms keep the exact-difference carry, so
+    their metrics are held to the oracle's metric function of the oracle's own
+    dlogp; the all-reduce arm's dlogp carries up to 6e-6 of independent sum
+    rounding per token (module docstring), which alone moves approx_kl0 of this
+    workload (|dlogp| ~ 1e-3) by more than 1e-4 relative, so its metrics are
+    held to the oracle's metric function of its own per-token dlogp."""
+    from oracle import stream
+
     w = W.sharded(device=DEV)
-    rng = np.random.default_rng(7)
-    rows = np.sort(rng.choice(w.n_rows, size=96, replace=False))
-    sel = torch.as_tensor(rows, device=DEV)
-    t_rows = torch.cat([x[sel] for x in w.train], dim=1)
-    r_rows = torch.cat([x[sel] for x in w.rollout], dim=1)
-    ref = oracle.score_rows(to_oracle(t_rows), to_oracle(r_rows), w.token_ids.cpu().numpy()[rows],
-                            np.arange(rows.size))
+    rows = np.arange(w.n_rows)
+    ref = stream.score_sharded_rows_device(w.train, w.rollout, w.v_ranges, w.token_ids, rows)
+    mask = w.action_mask.cpu().numpy()
+    ref_m = oracle.metrics(ref.dlogp, mask, *w.clip)
+    ref_m["status"] = ref.status
     results = {}
     for topo in (FIXED, ALLREDUCE, ALLGATHER):
         res = _arm(w, topo)
         assert res.metrics["status"] == 0 and res.metrics["n_active"] == w.n_rows
         for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout)):
-            assert np.max(np.abs(got[sel].cpu().numpy().astype(np.float64) - want)) <= LOGP_ATOL
-        d_err = np.max(np.abs(res.dlogp[sel].cpu().numpy().astype(np.float64) - ref.dlogp))
-        assert d_err <= (ALLREDUCE_D_ATOL if topo == ALLREDUCE else LOGP_ATOL)
+            assert np.max(np.abs(got.cpu().numpy().astype(np.float64) - want)) <= LOGP_ATOL
+        d = res.dlogp.cpu().numpy().astype(np.float64)
+        d_err = float(np.max(np.abs(d - ref.dlogp)))
+        if topo == ALLREDUCE:
+            assert d_err <= ALLREDUCE_D_ATOL
+            prop = oracle.metrics(d, mask, *w.clip)
+            prop["status"] = 0
+            assert_metrics_match(res.metrics, prop, d, mask, w.clip, ambiguity=1e-6)
+        else:
+            assert d_err <= LOGP_ATOL
+            assert_metrics_match(res.metrics, ref_m, ref.dlogp, mask, w.clip, dlogp_err=d_err)
         results[topo] = res
     # the arms move the same numbers: topology drift is rounding only
     for topo in (ALLREDUCE, ALLGATHER):

@@ -68,3 +68,17 @@ def test_threaded_transformed_equal_serial():
     got = stream.score_transformed_rows_device(w.train, w.rollout, w.token_ids, rows, ops_t, ops_r, chunk=4,
                                                threads=2)
     _same(got, want)
+
+
+def test_threaded_entropy_and_backward_equal_serial():
+    w = W.synthetic(20, 300, seed=8, device="cpu", active_prob=1.0)
+    rows = np.array([19, 0, 5, 6, 7])
+    et, er = oracle.entropy(to_oracle(w.train[rows]), to_oracle(w.rollout[rows]), np.ones(rows.size, np.uint8))
+    gt, gr = stream.entropy_rows_device(w.train, w.rollout, rows, chunk=2, threads=3)
+    assert np.array_equal(gt, et) and np.array_equal(gr, er)
+    grad = torch.linspace(-2, 2, 20)
+    got = stream.backward_rows_device(w.train, w.token_ids, grad, rows, chunk=2, threads=2)
+    x = to_oracle(w.train)
+    for j, r in enumerate(rows):
+        want = oracle.logprob_backward_row(np.ascontiguousarray(x[r]), int(w.token_ids[r]), float(grad[r]))
+        assert np.array_equal(got[j], want)
