@@ -108,6 +108,27 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
     return false;
 }
 
+// ---- -inf tiles ------------------------------------------------------------
+// A whole tile's worth of -inf in each storage format, the source of the bulk
+// copies that pad a segment's last stage (constant data of the module).
+template <uint32_t kWord, int kWords>
+struct __align__(16) FillWords {
+    uint32_t w[kWords];
+    constexpr FillWords() : w{} {
+        for (int i = 0; i < kWords; ++i) w[i] = kWord;
+    }
+};
+constexpr int kMaxTileCols = kColsPerThread * 32 * kConsumerWarps;
+__device__ const FillWords<0xFF800000u, kMaxTileCols> g_neg_inf_f32;       // fp32 -inf
+__device__ const FillWords<0xFF80FF80u, kMaxTileCols / 2> g_neg_inf_bf16;  // bf16 -inf pairs
+
+template <class D>
+__device__ __forceinline__ const void *neg_inf_words();
+template <>
+__device__ __forceinline__ const void *neg_inf_words<Bf16>() { return g_neg_inf_bf16.w; }
+template <>
+__device__ __forceinline__ const void *neg_inf_words<F32>() { return g_neg_inf_f32.w; }
+
 // ---- element access ------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -173,7 +194,7 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
 // with a chain of at most one soft-cap per side in its reduced form (the
 // soft-cap on each loaded value, the scales folded into the exponent factor
 // as in mode 3).
-template <class DT, class DR, bool kTma, int kMode, int kW>
+template <class DT, class DR, bool kTma, int kMode, int kW, bool kMulti>
 __global__ void __launch_bounds__(kW * 32 + 32, 1)
     row_kernel(const __grid_constant__ RowArgs a, int n_stages) {
     constexpr bool kXform = kMode == kRowTransform;
@@ -212,6 +233,19 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
     }
     __syncthreads();
 
+    // The plain pass over several vocab segments (kMulti: every segment's last
+    // tile is ragged): when a segment's length in bytes is a multiple of 16 on
+    // both sides, the producer also copies -inf into the columns of its last
+    // stage past the segment's end (from the constant arrays above), so the
+    // consumers read that tile like any full one.  It gives every column the
+    // value the branch-free ragged path would (-inf past the end), so the bits
+    // are the same either way; passes over one segment (one ragged tile a row)
+    // are instantiated without it, as they measured slower with it.
+    constexpr bool kFillTail = kMulti && !kXform && !kSoftcap;
+    auto tail_filled = [&](const Segment &sg) {
+        return kFillTail && (sg.len * DT::kBytes) % 16 == 0 && (sg.len * DR::kBytes) % 16 == 0;
+    };
+
     if (warp == kWarps) {
         // ------------------------------------------------------ producer
         if (!kTma || lane != 0) return;
@@ -225,6 +259,7 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                 const Segment &sg = a.seg[k];
                 const char *tb = sg.t + r * sg.t_stride;
                 const char *rb = sg.r + r * sg.r_stride;
+                const bool fill = tail_filled(sg);
                 for (int64_t c0 = 0; c0 < sg.len; c0 += kTile) {
                     const uint32_t stage = it % n_stages, round = it / n_stages;
                     if (round > 0 && !wait_phase(&empty[stage], (round - 1) & 1, &abort_flag, a.status)) {
@@ -234,14 +269,21 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                     const int64_t nv = min(static_cast<int64_t>(kTile), sg.len - c0);
                     const uint32_t bt = static_cast<uint32_t>(nv * DT::kBytes) & ~15u;
                     const uint32_t br = static_cast<uint32_t>(nv * DR::kBytes) & ~15u;
+                    // -inf tails (multiples of 16 bytes when fill holds)
+                    const uint32_t ft = (fill && nv < kTile) ? kStageT - bt : 0u;
+                    const uint32_t fr = (fill && nv < kTile) ? kStageR - br : 0u;
                     char *st = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
-                    mbar_arrive_expect_tx(&full[stage], bt + br);
+                    mbar_arrive_expect_tx(&full[stage], bt + br + ft + fr);
                     // a.stall (tests of the timeout path only): CTA 0 never
                     // issues its first copy, so its consumers run into the
                     // bounded wait; no copy is in flight for that stage
                     const bool withhold = a.stall && it == 0 && blockIdx.x == 0;
-                    if (bt && !withhold) bulk_g2s(st, tb + c0 * DT::kBytes, bt, &full[stage], policy);
-                    if (br && !withhold) bulk_g2s(st + kStageT, rb + c0 * DR::kBytes, br, &full[stage], policy);
+                    if (!withhold) {
+                        if (bt) bulk_g2s(st, tb + c0 * DT::kBytes, bt, &full[stage], policy);
+                        if (br) bulk_g2s(st + kStageT, rb + c0 * DR::kBytes, br, &full[stage], policy);
+                        if (ft) bulk_g2s(st + bt, neg_inf_words<DT>(), ft, &full[stage], policy);
+                        if (fr) bulk_g2s(st + kStageT + br, neg_inf_words<DR>(), fr, &full[stage], policy);
+                    }
                     ++it;
                 }
             }
@@ -303,6 +345,7 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
             const char *tb = sg.t + r * sg.t_stride;
             const char *rb = sg.r + r * sg.r_stride;
             Acc2 acc2 = acc2_init();
+            const bool seg_filled = tail_filled(sg);
             auto tile = [&](const int64_t c0, auto tag) -> bool {
                 constexpr int kKind = decltype(tag)::kind;
                 const int nv = kKind == kTileFull ? kTile : static_cast<int>(min(static_cast<int64_t>(kTile), sg.len - c0));
@@ -314,7 +357,7 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                     const bool ok = wait_phase(&full[stage], round & 1, &abort_flag, a.status);
                     if (__any_sync(0xffffffffu, !ok)) return false;
                     const char *stg = ring + static_cast<size_t>(stage) * (kStageT + kStageR);
-                    if (kKind == kTileFull || (kKind == kTileAny && nv == kTile)) {
+                    if (kKind == kTileFull || (kKind == kTileAny && (nv == kTile || seg_filled))) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             lds4<DT>(stg, g * kGroupCols + 4 * t, vt + 2 * g);
@@ -474,13 +517,13 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
     }
 }
 
-template <class DT, class DR, bool kTma, int kMode, int kW = row_warps(kMode)>
+template <class DT, class DR, bool kTma, int kMode, int kW, bool kMulti>
 cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     constexpr int kThreads = kW * 32 + 32;  // + producer warp
     const int stage_bytes = kColsPerThread * 32 * kW * (DT::kBytes + DR::kBytes);
     const int n_stages = kTma ? min(16, kRingBytes / stage_bytes) : 0;
     const size_t smem = kTma ? 1024 + static_cast<size_t>(n_stages) * stage_bytes : 0;
-    auto kern = row_kernel<DT, DR, kTma, kMode, kW>;
+    auto kern = row_kernel<DT, DR, kTma, kMode, kW, kMulti>;
     static std::atomic<uint64_t> configured{0};
     const cudaError_t e = set_smem_once(kern, smem, configured);
     if (e != cudaSuccess) return e;
@@ -488,12 +531,12 @@ cudaError_t launch_typed(const RowArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool kTma, int kMode, int kW = row_warps(kMode)>
+template <bool kTma, int kMode, int kW = row_warps(kMode), bool kMulti = false>
 cudaError_t dispatch(const RowArgs &a, int dt, int dr, cudaStream_t stream) {
-    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kMode, kW>(a, stream);
-    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kMode, kW>(a, stream);
-    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kMode, kW>(a, stream);
-    return launch_typed<F32, F32, kTma, kMode, kW>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_BF16) return launch_typed<Bf16, Bf16, kTma, kMode, kW, kMulti>(a, stream);
+    if (dt == LPD_BF16 && dr == LPD_F32) return launch_typed<Bf16, F32, kTma, kMode, kW, kMulti>(a, stream);
+    if (dt == LPD_F32 && dr == LPD_BF16) return launch_typed<F32, Bf16, kTma, kMode, kW, kMulti>(a, stream);
+    return launch_typed<F32, F32, kTma, kMode, kW, kMulti>(a, stream);
 }
 
 template <int kMode>
@@ -525,8 +568,11 @@ int row_pass_warps(const Segment *segs, int n_seg, int mode, bool use_tma) {
 
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, int warps,
                         cudaStream_t stream) {
-    if (mode == kRowPlain && use_tma && warps == 19) return dispatch<true, kRowPlain, 19>(a, dtype_t, dtype_r, stream);
-    if (mode == kRowPlain && use_tma && warps == 16) return dispatch<true, kRowPlain, 16>(a, dtype_t, dtype_r, stream);
+    if (mode == kRowPlain && use_tma && a.n_seg > 1) {
+        if (warps == 19) return dispatch<true, kRowPlain, 19, true>(a, dtype_t, dtype_r, stream);
+        if (warps == 16) return dispatch<true, kRowPlain, 16, true>(a, dtype_t, dtype_r, stream);
+        return dispatch<true, kRowPlain, 20, true>(a, dtype_t, dtype_r, stream);
+    }
     if (mode == kRowTransform) return dispatch_path<1>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowSoftcap) return dispatch_path<4>(a, dtype_t, dtype_r, use_tma, stream);
     if (mode == kRowEntropy) return dispatch_path<2>(a, dtype_t, dtype_r, use_tma, stream);
