@@ -22,8 +22,11 @@
 //      (lpd_acc.cuh); the four states are merged in column order and written
 //      as that (row, vocab tile)'s partial (in the transform variant each
 //      side's logit chain is applied first, lpd_xform.cuh).  The accumulators
-//      fill tensor memory, so the next tile's MMAs wait for this drain; four
-//      warps per row cut that wait to a quarter.  Tiles are visited in groups of 8 row
+//      fill tensor memory, so the next tile's MMAs wait for this drain: four
+//      warps per row cut that wait to a quarter, each warp loads both sides'
+//      columns before one wait, and each frees its share as soon as its reads
+//      are done (the states travel to the row's lead warp through a separate
+//      shared-memory buffer).  Tiles are visited in groups of 8 row
 //      tiles so that the CTAs running together share their W tiles and hidden
 //      tiles in L2.
 //   3. head_finalize_kernel: one warp per active row merges its vocab-tile
@@ -156,16 +159,17 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this warp's 32 accumulator lanes (one row per
-// lane) into packed pairs.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, f2_t *v) {
-    uint32_t r[16];
+// lane), issued without waiting (tmem_wait_ld completes it).
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t *r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void unpack16(const uint32_t *r, f2_t *v) {
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = f2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
 }
@@ -208,8 +212,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     __shared__ uint64_t full[kStages], empty[kStages], tmem_full, tmem_empty, mma_done;
     // a row's column-half states, handed by the other warps of its lane
     // quadrant to the quadrant's lead warp (one phase per tile)
-    __shared__ uint64_t xchg_full[4];
-    __shared__ float xchg[kEpiSplit > 1 ? kEpiSplit - 1 : 1][5][kBM];
+    // two hand-over buffers, used by alternate tiles, each with its own barrier
+    // per quadrant, so the lead can free tensor memory before reading them
+    __shared__ uint64_t xchg_full[2][4];
+    __shared__ float xchg[2][kEpiSplit > 1 ? kEpiSplit - 1 : 1][5][kBM];
     __shared__ uint32_t tmem_base_slot;
     __shared__ int abort_flag;
     __shared__ float4 xf_ops[2 * LPD_MAX_TRANSFORM_OPS];
@@ -232,7 +238,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         mbar_init(&tmem_full, 1);
         mbar_init(&tmem_empty, kEpiWarps);
         mbar_init(&mma_done, 1);
-        for (int q = 0; q < 4; ++q) mbar_init(&xchg_full[q], (kEpiSplit - 1) * 32);
+        for (int b = 0; b < 2; ++b)
+            for (int q = 0; q < 4; ++q) mbar_init(&xchg_full[b][q], (kEpiSplit - 1) * 32);
         if (kXform) {
             xform_table(a.xt, xf_ops);
             xform_table(a.xr, xf_ops + LPD_MAX_TRANSFORM_OPS);
@@ -320,11 +327,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         // ------------------------------------------------------------ epilogue
         // Warp w reads tensor-memory lanes [32 (w % 4), +32): one row per lane.
         // The kEpiSplit warps of a quadrant take consecutive kEpiCols-column
-        // ranges of the tile; the others hand their row states to the lead
-        // (split 0) through shared memory, and the lead merges them in column
-        // order, frees the accumulators and writes the tile's partial.  The
-        // lead frees them only after reading the hand-over, so a helper cannot
-        // overwrite it (its next tile needs the next MMA, which needs the free).
+        // ranges of the tile, each freeing the accumulators as soon as its own
+        // reads are done; the others hand their row states to the lead (split
+        // 0) through shared memory (two buffers, alternate tiles), and the lead
+        // merges them in column order and writes the tile's partial.
         const int quad = warp & 3;
         const int split = (warp - 2) >> 2;
         const int row_in_tile = quad * 32 + lane;
@@ -346,8 +352,15 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll 1
             for (int c = split * kEpiCols; c < (split + 1) * kEpiCols; c += 16) {
                 f2_t vt[8], vr[8];
-                tmem_ld16(lane_addr + c, vt);
-                tmem_ld16(lane_addr + kBN + c, vr);
+                {
+                    // both sides' loads in flight together, one wait
+                    uint32_t rt[16], rr[16];
+                    tmem_ld16_issue(lane_addr + c, rt);
+                    tmem_ld16_issue(lane_addr + kBN + c, rr);
+                    tmem_wait_ld();
+                    unpack16(rt, vt);
+                    unpack16(rr, vr);
+                }
                 if (kXform) {
                     xform16(vt, cxt);
                     xform16(vr, cxr);
@@ -378,24 +391,31 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             Acc r = acc2_fold(acc);
             tc_fence_before();
             __syncwarp();
+            // this warp's accumulator reads are complete: its share of tensor
+            // memory is free for the next tile's MMAs (the lead included: the
+            // hand-over goes through a buffer of its own, see below)
+            if (lane == 0) mbar_arrive(&tmem_empty);
+            // Hand-over buffer of this tile.  A helper reuses it two tiles later,
+            // which needs the MMAs of the tile after this one, which need the
+            // lead's free of that tile, which comes after the lead read this one.
+            const int xb = static_cast<int>(local & 1);
             if (split > 0) {
-                // helper: its accumulator reads are done; hand the state over
-                float *x = &xchg[split - 1][0][0];
+                // helper: hand the state over to the quadrant's lead
+                float *x = &xchg[xb][split - 1][0][0];
                 x[0 * kBM + row_in_tile] = r.mt;
                 x[1 * kBM + row_in_tile] = r.st;
                 x[2 * kBM + row_in_tile] = r.dd;
                 x[3 * kBM + row_in_tile] = r.mr;
                 x[4 * kBM + row_in_tile] = r.sr;
-                if (lane == 0) mbar_arrive(&tmem_empty);
-                mbar_arrive(&xchg_full[quad]);
+                mbar_arrive(&xchg_full[xb][quad]);
                 continue;
             }
             if (kEpiSplit > 1) {
-                const bool got = wait_phase(&xchg_full[quad], local & 1, &abort_flag, a.status);
+                const bool got = wait_phase(&xchg_full[xb][quad], (local >> 1) & 1, &abort_flag, a.status);
                 if (__any_sync(0xffffffffu, !got)) break;
 #pragma unroll
                 for (int h = 0; h < kEpiSplit - 1; ++h) {
-                    const float *x = &xchg[h][0][0];
+                    const float *x = &xchg[xb][h][0][0];
                     Acc o;
                     o.mt = x[0 * kBM + row_in_tile];
                     o.st = x[1 * kBM + row_in_tile];
@@ -407,8 +427,6 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                 }
                 __syncwarp();
             }
-            // accumulators drained and hand-over read: the MMA warp may reuse both
-            if (lane == 0) mbar_arrive(&tmem_empty);
             if (valid) {
                 const int64_t o = i * n_n + n;
                 a.part_a[o] = make_float4(r.mt, r.st, r.dd, r.mr);
