@@ -894,6 +894,38 @@ def run_reference_attn(args, world):
     return out
 
 
+def run_link_probe(args):
+    """Host-link bandwidth that bounds the e2e legs: pinned (cudaHostAlloc)
+    host->device and device->host copies of --link-gib GiB, one cudaMemcpyAsync
+    each, timed with CUDA events on the copying stream (best and median of
+    --steps copies after --warmup)."""
+    import torch
+
+    n = int(args.link_gib * (1 << 30))
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {"metric": "pinned host<->device copy bandwidth", "unit": "GB/s", "bytes_per_copy": n, "impl": "lpd",
+           "steps": args.steps, "warmup": args.warmup}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        times = []
+        for k in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        times.sort()
+        out[name] = {"best_gbs": round(n / (times[0] / 1e3) / 1e9, 1),
+                     "median_gbs": round(n / (times[len(times) // 2] / 1e3) / 1e9, 1),
+                     "slowest_gbs": round(n / (times[-1] / 1e3) / 1e9, 1)}
+    print(json.dumps(out), flush=True)
+    return out
+
+
 def free_port() -> int:
     import socket
 
@@ -949,6 +981,9 @@ def main(argv=None):
                     help="sharded config: time lpd_score_sharded_topology with this reduction arm")
     ap.add_argument("--drift", action="store_true",
                     help="attn config: time lpd_attn_merge_order_drift instead of lpd_attn_merge")
+    ap.add_argument("--link-probe", action="store_true",
+                    help="measure pinned host<->device copy bandwidth (the e2e legs' bound) instead")
+    ap.add_argument("--link-gib", type=float, default=4.0, help="link probe: GiB per copy")
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases only)")
     ap.add_argument("--seq", type=int, default=None, help="override T (small profiling cases only)")
     args = ap.parse_args(argv)
@@ -964,6 +999,8 @@ def main(argv=None):
     plan_launch(args.gpus, dict(os.environ), 0)
     if args.impl == "reference":
         return run_reference(args)
+    if args.link_probe:
+        return run_link_probe(args)
     return run_ours(args)
 
 
