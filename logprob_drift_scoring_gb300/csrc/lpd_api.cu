@@ -107,48 +107,6 @@ bool stall_requested() {
     return v && v[0] == '1' && v[1] == '\0';
 }
 
-// A side's chain in the reduced form of the kRowSoftcap pass: at most one
-// soft-cap, every scale behind it (softcap_p(a x) = a softcap_{p/a}(x)), the
-// product of all scales in *post.  False when the chain has more than one
-// soft-cap, or when the pre-multiplied series coefficients would leave the
-// range of normal floats (p far from 1); such chains take the general pass.
-bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
-    *out = SoftcapSide{};
-    double pre = 1.0, after = 1.0, cap = 0.0;
-    int n_cap = 0;
-    for (int k = 0; k < c.n_ops; ++k) {
-        if (c.kind[k] == LPD_OP_SCALE) {
-            (n_cap ? after : pre) *= static_cast<double>(c.param[k]);
-        } else {
-            ++n_cap;
-            cap = static_cast<double>(c.param[k]);
-        }
-    }
-    *post = pre * after;
-    if (n_cap == 0) {
-        // no soft-cap: zero series coefficients leave every |x| < 1e18 as it is
-        out->thr = 1e18f;
-        return true;
-    }
-    if (n_cap > 1) return false;
-    const double p = cap / pre, r = pre / cap;
-    const double lo = 1e-36, hi = 1e36;
-    if (!(p > lo && p < hi && r * r > lo && r * r < hi)) return false;
-    out->on = 1;
-    out->p = static_cast<float>(p);
-    out->r = static_cast<float>(r);
-    out->r2 = static_cast<float>(r * r);
-    // |x| < 0.449 p gives fl(fl(x^2) fl(1/p^2)) < 0.45^2 after every rounding
-    out->thr = static_cast<float>(0.449 * p);
-    double rk = r * r;
-    for (int k = 0; k < kSoftcapTerms; ++k, rk *= r * r) {
-        const double q = static_cast<double>(softcap_c(k)) * rk;
-        if (!(std::fabs(q) > lo && std::fabs(q) < hi)) return false;
-        out->q[k] = static_cast<float>(q);
-    }
-    return true;
-}
-
 // Stage 2: the streaming row pass, then the per-row finalise.
 // Optional extras of the row pass: a transform chain per side, or entropy outputs.
 struct RowExtras {

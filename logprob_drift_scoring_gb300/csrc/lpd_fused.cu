@@ -190,7 +190,9 @@ struct HeadArgs {
     float *part_b;         // [A_pad, n_tiles_n] sr
     float2 *pick;          // [A_pad] selected logits
     uint32_t *status;
-    Xform xt, xr;          // transform chains (the kXform kernel only)
+    Xform xt, xr;          // transform chains (the general-chain kernel only)
+    SoftcapSide cap[2];    // reduced soft-caps (the soft-cap kernel only)
+    float lt, lr;          // each side's factor to base-2 exponents: s log2 e (scales folded), else log2 e
 };
 
 __device__ __forceinline__ void tile_coords(int64_t t, int n_m, int n_n, int &m, int &n) {
@@ -202,10 +204,14 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_m, int n_n, int &m,
     n = static_cast<int>(local / gm);
 }
 
-// kXform: each side's transform chain is applied to the accumulator values
-// right after they leave tensor memory, before the vocab-tail mask, so the
-// selected logit and the sums see transformed values and padding stays -inf.
-template <bool kXform>
+// kChain: 0 no transform; 1 each side's general chain (per-op loop); 2 the
+// reduced form of chains with at most one soft-cap per side (the soft-cap on
+// each value, the scales folded into the exponent factor); 3 scales only
+// (folded into the exponent factor, no per-value work).  The transform runs on
+// the accumulator values right after they leave tensor memory, before the
+// vocab-tail mask, so the selected logit and the sums see transformed values
+// and padding stays -inf; the finalise applies the folded scales in fp64.
+template <int kChain>
 __global__ void __launch_bounds__(kHeadThreads, 1)
     head_kernel(const __grid_constant__ HeadMaps maps, const __grid_constant__ HeadArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         mbar_init(&mma_done, 1);
         for (int b = 0; b < 2; ++b)
             for (int q = 0; q < 4; ++q) mbar_init(&xchg_full[b][q], (kEpiSplit - 1) * 32);
-        if (kXform) {
+        if (kChain == 1) {
             xform_table(a.xt, xf_ops);
             xform_table(a.xr, xf_ops + LPD_MAX_TRANSFORM_OPS);
         }
@@ -334,8 +340,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int quad = warp & 3;
         const int split = (warp - 2) >> 2;
         const int row_in_tile = quad * 32 + lane;
-        const XformView cxt{xf_ops, kXform ? a.xt.n_ops : 0},
-            cxr{xf_ops + LPD_MAX_TRANSFORM_OPS, kXform ? a.xr.n_ops : 0};
+        const XformView cxt{xf_ops, kChain == 1 ? a.xt.n_ops : 0},
+            cxr{xf_ops + LPD_MAX_TRANSFORM_OPS, kChain == 1 ? a.xr.n_ops : 0};
+        const float lg_t = kChain >= 2 ? a.lt : kLog2e, lg_r = kChain >= 2 ? a.lr : kLog2e;
         uint32_t local = 0;
         for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
             const bool ok = wait_phase(&tmem_full, local & 1, &abort_flag, a.status);
@@ -361,10 +368,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     unpack16(rt, vt);
                     unpack16(rr, vr);
                 }
-                if (kXform) {
+                if (kChain == 1) {
                     xform16(vt, cxt);
                     xform16(vr, cxr);
                 }
+                if (kChain == 2) softcap32_u(vt, vr, a.cap[0], a.cap[1]);
                 const int64_t col0 = c_base + c;
                 if (col0 + 16 > a.vocab) {  // vocab tail: columns past V are not logits
 #pragma unroll
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     }
                     a.pick[i] = make_float2(xt, xr);
                 }
-                accumulate16(vt, vr, acc);
+                accumulate16(vt, vr, acc, lg_t, lg_r);
             }
             Acc r = acc2_fold(acc);
             tc_fence_before();
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                     o.mr = x[3 * kBM + row_in_tile];
                     o.sr = x[4 * kBM + row_in_tile];
                     o.ht = o.hr = 0.f;
-                    merge_acc<false>(r, o);
+                    merge_acc<false>(r, o, lg_t, lg_r);
                 }
                 __syncwarp();
             }
@@ -478,6 +486,7 @@ __global__ void __launch_bounds__(256) gather_hidden_kernel(const WsHeader *hdr,
 __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr, const int2 *rowid,
                                                            const float4 *part_a, const float *part_b,
                                                            const float2 *pick, int n_n, int64_t vocab,
+                                                           float scale_t, float scale_r, float lg_t, float lg_r,
                                                            float *out_lt, float *out_lr, float *out_d,
                                                            double *dval, uint32_t *keys, uint32_t *status) {
     const int64_t n_active = hdr->n_active;
@@ -494,7 +503,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.mr = p.w;
         o.sr = part_b[i * n_n + n];
         o.ht = o.hr = 0.f;
-        merge_acc<false>(acc, o);
+        merge_acc<false>(acc, o, lg_t, lg_r);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         o.mr = __shfl_xor_sync(0xffffffffu, acc.mr, off);
         o.sr = __shfl_xor_sync(0xffffffffu, acc.sr, off);
         o.ht = o.hr = 0.f;
-        merge_acc<false>(acc, o);
+        merge_acc<false>(acc, o, lg_t, lg_r);
     }
     if (lane != 0) return;
     const int2 rid = rowid[i];
@@ -518,13 +527,15 @@ __global__ void __launch_bounds__(256) head_finalize_kernel(const WsHeader *hdr,
         if (out_lt) out_lt[r] = CUDART_NAN_F;
         if (out_lr) out_lr[r] = CUDART_NAN_F;
     } else {
+        // folded scales (1 without a chain): lse = s m + ln(sum), x[id] -> s x[id], exact in fp64
         const float2 xs = pick[i];
-        const double lse_t = static_cast<double>(acc.mt) + log(static_cast<double>(acc.st));
-        const double lse_r = static_cast<double>(acc.mr) + log(static_cast<double>(acc.sr));
-        const double xt = xs.x, xr = xs.y;
+        const double mt = static_cast<double>(scale_t) * acc.mt, mr = static_cast<double>(scale_r) * acc.mr;
+        const double lse_t = mt + log(static_cast<double>(acc.st));
+        const double lse_r = mr + log(static_cast<double>(acc.sr));
+        const double xt = static_cast<double>(scale_t) * xs.x, xr = static_cast<double>(scale_r) * xs.y;
         const double st = acc.st, sr = acc.sr, dd = acc.dd;
         const double l_ratio = fabs(dd) < 0.5 * st ? log1p(-dd / st) : log(sr / st);
-        d = ((xt - xr) - (static_cast<double>(acc.mt) - static_cast<double>(acc.mr))) + l_ratio;
+        d = ((xt - xr) - (mt - mr)) + l_ratio;
         if (!(isfinite(lse_t) && isfinite(lse_r) && isfinite(xt) && isfinite(xr))) bad |= LPD_STATUS_NONFINITE;
         if (out_lt) out_lt[r] = static_cast<float>(xt - lse_t);
         if (out_lr) out_lr[r] = static_cast<float>(xr - lse_r);
@@ -620,21 +631,43 @@ cudaError_t launch_fused(const FusedCall &c, cudaStream_t stream) {
     a.status = c.status;
     a.xt = c.xt;
     a.xr = c.xr;
-    const bool xf = c.xt.n_ops > 0 || c.xr.n_ops > 0;
+    a.lt = a.lr = kLog2e;
+    // the chain's form: none, scales only, at most one soft-cap per side
+    // (reduced), or general
+    int chain = 0;
+    float scale_t = 1.f, scale_r = 1.f;
+    if (c.xt.n_ops > 0 || c.xr.n_ops > 0) {
+        double post[2];
+        chain = 1;
+        if (reduce_softcap(c.xt, &a.cap[0], &post[0]) && reduce_softcap(c.xr, &a.cap[1], &post[1])) {
+            chain = (a.cap[0].on || a.cap[1].on) ? 2 : 3;
+            a.lt = static_cast<float>(post[0] * 1.4426950408889634);
+            a.lr = static_cast<float>(post[1] * 1.4426950408889634);
+            scale_t = static_cast<float>(post[0]);
+            scale_r = static_cast<float>(post[1]);
+        }
+    }
     const size_t smem = static_cast<size_t>(kStages) * kStage + 1024;
-    static std::atomic<uint64_t> configured_plain{0}, configured_xform{0};
-    if ((e = xf ? set_smem_once(head_kernel<true>, smem, configured_xform)
-                : set_smem_once(head_kernel<false>, smem, configured_plain)) != cudaSuccess)
-        return e;
-    if (xf)
-        head_kernel<true><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
-    else
-        head_kernel<false><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a);
+    static std::atomic<uint64_t> configured[4];
+    switch (chain) {
+        case 0: e = set_smem_once(head_kernel<0>, smem, configured[0]); break;
+        case 1: e = set_smem_once(head_kernel<1>, smem, configured[1]); break;
+        case 2: e = set_smem_once(head_kernel<2>, smem, configured[2]); break;
+        default: e = set_smem_once(head_kernel<3>, smem, configured[3]); break;
+    }
+    if (e != cudaSuccess) return e;
+    switch (chain) {
+        case 0: head_kernel<0><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a); break;
+        case 1: head_kernel<1><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a); break;
+        case 2: head_kernel<2><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a); break;
+        default: head_kernel<3><<<device_sm_count(), kHeadThreads, smem, stream>>>(maps, a); break;
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const unsigned fin_blocks = static_cast<unsigned>((c.n_rows + 7) / 8);
     head_finalize_kernel<<<fin_blocks, 256, 0, stream>>>(
-        hdr, rowid, part_a, part_b, pick, L.n_tiles_n, c.vocab, c.out_lt, c.out_lr, c.out_d,
+        hdr, rowid, part_a, part_b, pick, L.n_tiles_n, c.vocab, scale_t, scale_r, a.lt, a.lr, c.out_lt, c.out_lr,
+        c.out_d,
         reinterpret_cast<double *>(ws + L.base.dval), reinterpret_cast<uint32_t *>(ws + L.base.keys), c.status);
     return cudaGetLastError();
 }

@@ -1,9 +1,12 @@
 // Logit transform chains ("[WS2] Framework for ablation experiment", LogProb
 // knobs table, row 7: temperature, soft-cap, logit scale), applied in fp32 to
 // each real logit before any softmax arithmetic.  Shared by the streaming row
-// kernel and the fused LM-head epilogue, so a logit gets the same transformed
-// bits on either path.
+// kernel and the fused LM-head epilogue, which pick the same form for a chain
+// (scales only, at most one soft-cap per side, or the general per-op loop), so
+// a logit gets the same transformed bits on either path.
 #pragma once
+
+#include <cmath>
 
 #include "lpd_acc.cuh"
 #include "lpd_internal.cuh"
@@ -172,6 +175,48 @@ __device__ __forceinline__ void softcap32_u(f2_t *vt, f2_t *vr, const SoftcapSid
             for (int q = 0; q < 8; ++q) vr[q] = f2(softcap_u1(f2_lo(vr[q]), cr), softcap_u1(f2_hi(vr[q]), cr));
         }
     }
+}
+
+// (host) A side's chain in the reduced form of the soft-cap passes: at most one
+// soft-cap, every scale behind it (softcap_p(a x) = a softcap_{p/a}(x)), the
+// product of all scales in *post.  False when the chain has more than one
+// soft-cap, or when the pre-multiplied series coefficients would leave the
+// range of normal floats (p far from 1); such chains take the general pass.
+inline bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
+    *out = SoftcapSide{};
+    double pre = 1.0, after = 1.0, cap = 0.0;
+    int n_cap = 0;
+    for (int k = 0; k < c.n_ops; ++k) {
+        if (c.kind[k] == LPD_OP_SCALE) {
+            (n_cap ? after : pre) *= static_cast<double>(c.param[k]);
+        } else {
+            ++n_cap;
+            cap = static_cast<double>(c.param[k]);
+        }
+    }
+    *post = pre * after;
+    if (n_cap == 0) {
+        // no soft-cap: zero series coefficients leave every |x| < 1e18 as it is
+        out->thr = 1e18f;
+        return true;
+    }
+    if (n_cap > 1) return false;
+    const double p = cap / pre, r = pre / cap;
+    const double lo = 1e-36, hi = 1e36;
+    if (!(p > lo && p < hi && r * r > lo && r * r < hi)) return false;
+    out->on = 1;
+    out->p = static_cast<float>(p);
+    out->r = static_cast<float>(r);
+    out->r2 = static_cast<float>(r * r);
+    // |x| < 0.449 p gives fl(fl(x^2) fl(1/p^2)) < 0.45^2 after every rounding
+    out->thr = static_cast<float>(0.449 * p);
+    double rk = r * r;
+    for (int k = 0; k < kSoftcapTerms; ++k, rk *= r * r) {
+        const double q = static_cast<double>(softcap_c(k)) * rk;
+        if (!(std::fabs(q) > lo && std::fabs(q) < hi)) return false;
+        out->q[k] = static_cast<float>(q);
+    }
+    return true;
 }
 
 __device__ __forceinline__ float xform1(float x, const XformView &c) {

@@ -180,6 +180,8 @@ CHAINS = [
     ([(SCALE, 30.0), (SOFTCAP, 10.0)], [(SCALE, 30.0), (SOFTCAP, 10.0)]),  # both tanh ranges
     ([], [(SCALE, 1 / 0.7)]),                                      # temperature on one side only
     ([(SCALE, 2.0), (SOFTCAP, 1.0)], [(SOFTCAP, 1.0), (SCALE, 2.0)]),     # order mismatch
+    # two soft-caps per side: the general per-op chain in the epilogue
+    ([(SOFTCAP, 3.0), (SCALE, 1.5), (SOFTCAP, 4.0)], [(SOFTCAP, 3.0), (SCALE, 1.5), (SOFTCAP, 4.0)]),
 ]
 
 
