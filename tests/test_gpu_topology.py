@@ -70,6 +70,8 @@ LAYOUTS = {
     "four_equal": ([(0, 4096), (4096, 8192), (8192, 12288), (12288, 16384)], 0, None),
     "ragged_padded": ([(0, 1000), (1000, 9000), (9000, 9001), (9001, 12003)], 5, None),
     "mixed_dtype": ([(0, 3001), (3001, 7000)], 0, torch.float32),
+    # 16-byte multiples on both sides: the -inf tail copies with mixed dtypes
+    "mixed_dtype_filled_tails": ([(0, 4096), (4096, 9000), (9000, 9016)], 0, torch.float32),
     "one_shard": ([(0, 5000)], 0, None),
 }
 

@@ -52,6 +52,20 @@ def test_transform_chain_vs_oracle(train_ops, rollout_ops, shape):
     _check(w, train_ops, rollout_ops)
 
 
+@pytest.mark.parametrize("dt,dr", [(torch.bfloat16, torch.float32), (torch.float32, torch.bfloat16),
+                                   (torch.float32, torch.float32)])
+@pytest.mark.parametrize("ops", [[(SOFTCAP, 30.0), (SCALE, 1 / 0.7)],                   # reduced soft-cap pass
+                                 [(SOFTCAP, 30.0), (SCALE, 1 / 0.7), (SOFTCAP, 40.0)],  # general pass
+                                 [(SCALE, 1 / 0.7)]])                                    # scales only
+@pytest.mark.parametrize("vocab,pad", [(3 * 10240 + 520, 0), (12805, 3)])
+def test_transform_chain_mixed_dtypes_vs_oracle(dt, dr, ops, vocab, pad):
+    # every dtype pairing of each chain form, on 16-byte aligned rows (bulk
+    # copies, full and ragged tiles) and on rows that are not (plain loads)
+    w = W.synthetic(120, vocab, seed=vocab + pad, device=DEV, dtype_train=dt, dtype_rollout=dr, row_pad=pad,
+                    spike_frac=0.05, spike=40.0)
+    _check(w, ops, ops)
+
+
 def test_identity_chain_is_bitwise_lpd_score():
     w = W.synthetic(250, 20000, seed=31, device=DEV)
     plain = B.score(w.train, w.rollout, w.token_ids, w.action_mask)
