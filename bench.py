@@ -407,6 +407,27 @@ def select_launches(n_rows: int) -> int:
     return 2 if 2 <= blocks <= 31 else 1
 
 
+def time_cpu_oracle_head(w, rows: int = 64) -> dict:
+    """The float64 oracle's LM-head scorer (logits materialised in double) as
+    it stands, on every host core, over `rows` rows of this workload spread
+    over its row tiles (oracle/stream.py schedules; each row is serial C)."""
+    import numpy as np
+
+    from oracle import stream
+
+    threads = stream.host_threads()
+    n = w.n_rows
+    sel = np.linspace(0, n - 1, num=min(rows, n)).astype(np.int64)
+    ht, hr, W = oracle_host(w.hidden_train.cpu()), oracle_host(w.hidden_rollout.cpu()), oracle_host(w.weight.cpu())
+    t0 = time.perf_counter()
+    stream.score_head_rows_parallel(ht, hr, W, w.token_ids.cpu().numpy(), sel, chunk=2, threads=threads)
+    elapsed = time.perf_counter() - t0
+    return {"value": round(sel.size / elapsed, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "host": host_cpu(), "seconds": round(elapsed, 2),
+            "sample": f"{sel.size} rows of this workload (both sides, H={w.hidden}, V={w.vocab}), one host thread "
+                      f"per core running the serial float64 head and scorer"}
+
+
 def run_fused(args, w, world, rank):
     """The fused LM-head path: one lpd_score_fused call per step (with
     --transform, lpd_score_fused_transformed with that chain on both sides)."""
@@ -446,6 +467,54 @@ def run_fused(args, w, world, rank):
     flops = 2.0 * 2.0 * n_active * w.hidden * w.vocab  # both sides
     peak = measured_tflops(ms * args.steps / 1e3)
     achieved = flops / (ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        # per step: both sides' hidden states, ids and mask from pinned host
+        # memory to the device (the head W stays resident, like model weights),
+        # the call, and the metrics record back
+        pinned = True
+        try:
+            host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for t in (w.hidden_train, w.hidden_rollout, w.token_ids, w.action_mask)]
+            met_host = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, pin_memory=True)
+        except RuntimeError:
+            host = [torch.empty(t.shape, dtype=t.dtype)
+                    for t in (w.hidden_train, w.hidden_rollout, w.token_ids, w.action_mask)]
+            met_host = torch.empty(B.METRICS_BYTES, dtype=torch.uint8)
+            pinned = False
+        for h, t in zip(host, (w.hidden_train, w.hidden_rollout, w.token_ids, w.action_mask)):
+            h.copy_(t)
+        dbuf = [torch.empty_like(t) for t in (w.hidden_train, w.hidden_rollout, w.token_ids, w.action_mask)]
+
+        def one():
+            for d, h in zip(dbuf, host):
+                d.copy_(h, non_blocking=True)
+            if chain is None:
+                B.lpd_score_fused(dbuf[0], dbuf[1], w.weight, dbuf[2], dbuf[3], *w.clip, *outs, met, ws)
+            else:
+                B.lpd_score_fused_transformed(dbuf[0], dbuf[1], w.weight, chain, chain, dbuf[2], dbuf[3], *w.clip,
+                                              *outs, met, ws)
+            met_host.copy_(met, non_blocking=True)
+
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.e2e_steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        ems = barrier_max(e0.elapsed_time(e1) / args.e2e_steps, world)
+        e2e = {"value": round(world * n_active / (ems / 1e3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+               "d2h_bytes_per_step": B.METRICS_BYTES, "ms_per_step": round(ems, 3), "pinned": pinned,
+               "steps": args.e2e_steps, "copies": "hidden states of both sides, ids, mask (W resident)"}
+        del dbuf, host
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_cpu_oracle_head(w)
     if rank != 0:
         return None
     out = {
@@ -462,7 +531,7 @@ def run_fused(args, w, world, rank):
                      "span": "whole lpd_score_fused call" if chain is None
                      else "whole lpd_score_fused_transformed call",
                      "algorithmic_flops_per_launch": flops},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": (select_launches(n) + 5) * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (select_launches(n) + 5) * args.steps,
         "clocks": clocks.summary(),
         "impl": "lpd",
     }
@@ -481,26 +550,27 @@ def attn_bytes(w, drift: bool) -> int:
 
 
 def time_cpu_oracle_attn(target_s: float = 12.0, seed: int = 1234):
-    """The float64 oracle merge as it stands, single-threaded, on a shorter
-    sequence of the same recipe (rows per second scale with rows)."""
-    import oracle
+    """The float64 oracle merge as it stands, on every host core (rows split
+    into chunks over one thread per core), on a shorter sequence of the same
+    recipe (rows per second scale with rows)."""
+    from oracle import stream
     from logprob_drift_scoring_gb300 import workloads as W
 
-    lib = oracle.load()
+    threads = stream.host_threads()
     probe = W.attn_partials(64, 32, 128, 8, seed=seed, device="cpu")
     t0 = time.perf_counter()
-    oracle.attn_merge(probe.out_parts.numpy(), probe.lse_parts.numpy(), lib=lib)
+    stream.attn_merge_parallel(probe.out_parts.numpy(), probe.lse_parts.numpy(), threads=threads)
     per_row = (time.perf_counter() - t0) / probe.n_rows
     tokens = int(max(64, min(8192, target_s / max(per_row, 1e-12) / 32)))
     tokens -= tokens % 8
     w = W.attn_partials(tokens, 32, 128, 8, seed=seed + 1, device="cpu")
     parts, lse = w.out_parts.numpy(), w.lse_parts.numpy()
     t0 = time.perf_counter()
-    oracle.attn_merge(parts, lse, lib=lib)
+    stream.attn_merge_parallel(parts, lse, threads=threads)
     elapsed = time.perf_counter() - t0
-    return {"value": w.n_rows / elapsed, "unit": ATTN_UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
+    return {"value": w.n_rows / elapsed, "unit": ATTN_UNIT, "cores": threads, "kind": "oracle", "host": host_cpu(),
             "sample": f"{w.n_rows} rows (T={tokens} x 32 heads, K=8 causal, head_dim 128) of the attn recipe, "
-                      f"float64 serial C, {elapsed:.1f} s"}
+                      f"float64 C on {threads} host threads, {elapsed:.1f} s"}
 
 
 def run_attn(args, w, world, rank):

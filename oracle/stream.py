@@ -20,8 +20,8 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-from . import (Result, entropy, load, logprob_backward_row, score_head_rows, score_rows, score_sharded,
-               score_transformed)
+from . import (Result, attn_merge, entropy, load, logprob_backward_row, score_head_rows, score_rows,
+               score_sharded, score_transformed)
 
 
 def host_threads(threads: int | None = None) -> int:
@@ -226,3 +226,25 @@ def backward_rows_device(logits, token_ids, grad, rows, chunk: int = 8, threads:
     res = _run_chunks(chunks(), work, threads)
     keys = sorted(res)
     return np.concatenate([res[k] for k in keys]) if keys else np.zeros((0, logits.shape[1]))
+
+
+def attn_merge_parallel(out_parts, lse_parts, order=None, lse_base2=False, chunk: int = 4096,
+                        threads: int | None = None):
+    """oracle.attn_merge of host arrays ([K, n, d], [K, n]) with the rows split
+    into chunks over host threads; (out [n, d], lse [n]) in row order."""
+    lib = load()
+    n = lse_parts.shape[1]
+
+    def chunks():
+        for c in range(0, n, chunk):
+            yield c, (out_parts[:, c:c + chunk], lse_parts[:, c:c + chunk])   # views; copied by the worker
+
+    def work(p):
+        o, l = p
+        return attn_merge(np.ascontiguousarray(o), np.ascontiguousarray(l), order, lse_base2, lib=lib)
+
+    res = _run_chunks(chunks(), work, threads)
+    keys = sorted(res)
+    if not keys:
+        return np.zeros((0, out_parts.shape[2])), np.zeros(0)
+    return np.concatenate([res[k][0] for k in keys]), np.concatenate([res[k][1] for k in keys])

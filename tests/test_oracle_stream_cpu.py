@@ -82,3 +82,11 @@ def test_threaded_entropy_and_backward_equal_serial():
     for j, r in enumerate(rows):
         want = oracle.logprob_backward_row(np.ascontiguousarray(x[r]), int(w.token_ids[r]), float(grad[r]))
         assert np.array_equal(got[j], want)
+
+
+def test_threaded_attention_merge_equals_serial():
+    a = W.attn_partials(40, 3, 8, 5, seed=9, device="cpu", masked_fill=float("nan"))
+    parts, lse = a.out_parts.numpy(), a.lse_parts.numpy()
+    want = oracle.attn_merge(parts, lse, [4, 0, 3, 1, 2])
+    got = stream.attn_merge_parallel(parts, lse, [4, 0, 3, 1, 2], chunk=7, threads=3)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
