@@ -11,8 +11,10 @@
 // blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams each row
 // through a ring of shared-memory stages with 1-D bulk copies (TMA,
 // cp.async.bulk, completion on an mbarrier); every stage holds the same tile of
-// 16 * 32 W columns of both sides (W = row_warps(mode) consumer warps: 20, so
-// 10240 columns, or 16 for the general transform chain).  The W warps read the
+// 16 * 32 W columns of both sides (W consumer warps: 20, so 10240 columns; 16
+// for the general transform chain; 19, 20 or 16 for the plain pass over
+// several vocab segments, whichever pads the segments' last tiles least, see
+// row_pass_warps).  The W warps read the
 // stage, and thread t owns columns [G g + 4t, G g + 4t + 4), g = 0..3, G =
 // 128 W, of every tile.  Each thread keeps an online (max, sum exp) pair per
 // side in fp32 plus the sum of the two sides' term differences; at the end of
@@ -188,6 +190,8 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
     return x;
 }
 
+// kW: consumer warps.  kMulti: the plain pass over several vocab segments,
+// with the -inf tail copies.
 // kMode: 0 plain, 1 with a general transform chain, 2 with the entropy sums,
 // 3 with a scale-only chain (each side's product of scales folded into its
 // exponent factor, so no tanh code and no extra arithmetic per element), 4
