@@ -154,7 +154,7 @@ __device__ __forceinline__ f2_t softcap_series2(f2_t x, const SoftcapSide &c) {
 // series runs packed on both sides, one range test and one warp vote per
 // tile.  Otherwise each value takes softcap_u1.  Either way a value gets
 // softcap_u1's bits.  A side without a soft-cap carries zero coefficients (its
-// series is x + (x u) 0 = x for every |x| below its threshold of 1e18) and is
+// series is x + (x u) 0 = x for every |x| below its threshold of 1e12) and is
 // left alone on the slow path.
 __device__ __forceinline__ void softcap32_u(f2_t *vt, f2_t *vr, const SoftcapSide &ct, const SoftcapSide &cr) {
     const float at = amax16(vt), ar = amax16(vr);
@@ -196,8 +196,10 @@ inline bool reduce_softcap(const Xform &c, SoftcapSide *out, double *post) {
     }
     *post = pre * after;
     if (n_cap == 0) {
-        // no soft-cap: zero series coefficients leave every |x| < 1e18 as it is
-        out->thr = 1e18f;
+        // no soft-cap: zero series coefficients leave every |x| below the
+        // threshold as it is (x + (x u) 0; x u = x^3 stays finite below 1e12),
+        // larger values take the slow path, which leaves this side alone
+        out->thr = 1e12f;
         return true;
     }
     if (n_cap > 1) return false;

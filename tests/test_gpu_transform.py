@@ -66,6 +66,36 @@ def test_transform_chain_mixed_dtypes_vs_oracle(dt, dr, ops, vocab, pad):
     _check(w, ops, ops)
 
 
+def test_reduced_pass_side_without_cap_keeps_huge_logits():
+    """A soft-cap on the train side only: the rollout side runs the identity
+    series, whose x^3 would overflow above ~7e12, so such values must take the
+    slow path (which leaves that side alone).  Huge values of both signs and
+    -inf on both sides; per-token logp against the oracle within 1e-4 plus
+    float32 rounding of the value itself (a logp near -1e30 carries ulps of
+    1e23), and no NaN anywhere (the drift metrics of such rows are infinite on
+    both sides, so they are not compared)."""
+    w = W.synthetic(64, 3000, seed=37, device=DEV, active_prob=1.0)
+    t, r = w.train.float().contiguous(), w.rollout.float().contiguous()
+    g = torch.Generator(device=DEV).manual_seed(38)
+    for x in (t, r):
+        rows = torch.randint(0, 64, (20,), generator=g, device=DEV)
+        cols = torch.randint(0, 3000, (20,), generator=g, device=DEV)
+        x[rows, cols] = torch.tensor([1e13, -1e13, 3e30, -3e30, float("-inf")] * 4, device=DEV)
+    ids = torch.remainder(w.token_ids, 3000)
+    sel = torch.arange(64, device=DEV)
+    mask = (torch.isfinite(t[sel, ids.long()]) & torch.isfinite(r[sel, ids.long()])).to(torch.uint8)
+    ops_t, ops_r = [(SOFTCAP, 30.0), (SCALE, 1 / 0.7)], [(SCALE, 1 / 0.7)]
+    res = B.score(t, r, ids, mask, train_ops=ops_t, rollout_ops=ops_r)
+    torch.cuda.synchronize()
+    m = mask.cpu().numpy()
+    ref = oracle.score_transformed(t.cpu().numpy(), r.cpu().numpy(), ids.cpu().numpy(), m, ops_t, ops_r)
+    act = m != 0
+    for got, want in ((res.logp_train, ref.logp_train), (res.logp_rollout, ref.logp_rollout)):
+        gn = got.cpu().numpy().astype(np.float64)
+        assert not np.any(np.isnan(gn))
+        assert np.all(np.abs(gn[act] - want[act]) <= LOGP_ATOL + 2.0 ** -22 * np.abs(want[act]))
+
+
 def test_identity_chain_is_bitwise_lpd_score():
     w = W.synthetic(250, 20000, seed=31, device=DEV)
     plain = B.score(w.train, w.rollout, w.token_ids, w.action_mask)
