@@ -241,7 +241,11 @@ __device__ __forceinline__ f2_t tree8(const f2_t *e) {
 // rescaled at most once per chunk; the sixteen terms of each sum are added in a
 // fixed pairwise tree.  -inf columns (masked tails) contribute exactly 0; the
 // -FLT_MAX floor keeps (x - m) defined for rows that are -inf everywhere.
-template <bool kEntropy = false>
+// kClamp (entropy sums only): clamp each term's exponent to a finite floor
+// before forming e * a, so that -inf columns add 0 instead of 0 * -inf = NaN.
+// Without it a -inf column turns the sum into NaN, which the caller must then
+// recompute (the row kernel does, for the warps whose sum came out NaN).
+template <bool kEntropy = false, bool kClamp = true>
 __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc2 &a, float lt = kLog2e,
                                              float lr = kLog2e) {
     const float cmt = max16(vt), cmr = max16(vr);
@@ -269,12 +273,15 @@ __device__ __forceinline__ void accumulate16(const f2_t *vt, const f2_t *vr, Acc
         et[p] = ex2_2(xt);
         er[p] = ex2_2(xr);
         dq[p] = sub2(et[p], er[p]);
-        if (kEntropy) {
+        if (kEntropy && kClamp) {
             // -inf columns give e = 0 and a = -inf; clamping a to a finite
             // floor makes their product 0 instead of NaN (finite terms are
             // never below the floor: their e would be 0 anyway)
             a.ht = fma2(et[p], f2(fmaxf(f2_lo(xt), -1e30f), fmaxf(f2_hi(xt), -1e30f)), a.ht);
             a.hr = fma2(er[p], f2(fmaxf(f2_lo(xr), -1e30f), fmaxf(f2_hi(xr), -1e30f)), a.hr);
+        } else if (kEntropy) {
+            a.ht = fma2(et[p], xt, a.ht);
+            a.hr = fma2(er[p], xr, a.hr);
         }
     }
     a.st = add2(a.st, tree8(et));

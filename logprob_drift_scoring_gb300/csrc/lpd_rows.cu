@@ -190,6 +190,28 @@ __device__ __forceinline__ float select16(const f2_t *v, int q) {
     return x;
 }
 
+// Sum over consumer thread t's columns of one row segment (its slots of every
+// tile, read from global memory) of e * max(a, -1e30), a = (x - m) l and
+// e = 2^a, then over the warp in a fixed xor butterfly: the entropy sum of a
+// warp state relative to the warp's maximum m, with -inf logits adding 0.
+template <class D, int kTile, int kGroupCols>
+__device__ __noinline__ float entropy_terms(const char *row, int64_t len, float m, float l, int t) {
+    float h = 0.f;
+    for (int64_t c0 = 0; c0 < len; c0 += kTile) {
+#pragma unroll
+        for (int q = 0; q < kColsPerThread; ++q) {
+            const int64_t col = c0 + slot_col<kGroupCols>(t, q);
+            if (col < len) {
+                const float x = __fmul_rn(__fsub_rn(ldg_elem<D>(row + col * D::kBytes), m), l);
+                h = __fmaf_rn(ex2(x), fmaxf(x, -1e30f), h);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) h = __fadd_rn(h, __shfl_xor_sync(0xffffffffu, h, off));
+    return h;
+}
+
 // kW: consumer warps.  kMulti: the plain pass over several vocab segments,
 // with the -inf tail copies.
 // kMode: 0 plain, 1 with a general transform chain, 2 with the entropy sums,
@@ -497,12 +519,15 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                 }
                 if (pick_mine && k == pick_seg && c0 == pick_c0)
                     a.pick[i] = make_float2(select16(vt, pick_slot), select16(vr, pick_slot));
-                accumulate16<kEntropy>(vt, vr, acc2, lg_t, lg_r);
+                // entropy sums: full tiles skip the clamp of -inf exponents
+                // (a -inf logit there leaves a NaN sum, recomputed below)
+                accumulate16<kEntropy, kKind != kTileFull>(vt, vr, acc2, lg_t, lg_r);
                 return true;
             };
-            if constexpr (kXform) {
-                // the transform chain's larger body: full tiles in a tight loop,
-                // the segment's ragged last tile after it (measured faster)
+            if constexpr (kXform || kEntropy) {
+                // full tiles in a tight loop, the segment's ragged last tile
+                // after it (measured faster for the transform chain's larger
+                // body; for the entropy sums, only the last tile clamps)
                 int64_t c0 = 0;
                 for (; c0 + kTile <= sg.len; c0 += kTile)
                     if (!tile(c0, TileTag<kTileFull>{})) return;
@@ -511,7 +536,16 @@ __global__ void __launch_bounds__(kW * 32 + 32, 1)
                 for (int64_t c0 = 0; c0 < sg.len; c0 += kTile)
                     if (!tile(c0, TileTag<kTileAny>{})) return;
             }
-            const Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2), lg_t, lg_r);
+            Acc acc = warp_reduce_acc<kEntropy>(acc2_fold(acc2), lg_t, lg_r);
+            if constexpr (kEntropy) {
+                // A -inf logit in a full tile made this warp's entropy sum NaN
+                // (0 * -inf, see accumulate16): the warp sums its columns'
+                // terms again, clamped, relative to its final maxima (the same
+                // quantity; the test is warp-uniform, every lane holds the
+                // reduced sums).  NaN logits stay NaN.
+                if (isnan(acc.ht)) acc.ht = entropy_terms<DT, kTile, kGroupCols>(tb, sg.len, acc.mt, lg_t, t);
+                if (isnan(acc.hr)) acc.hr = entropy_terms<DR, kTile, kGroupCols>(rb, sg.len, acc.mr, lg_r, t);
+            }
             if (lane == 0) {
                 float4 *dst = a.part + ((i * a.n_seg + k) * kConsumerWarps + warp) * 2;
                 dst[0] = make_float4(acc.mt, acc.st, acc.dd, acc.mr);

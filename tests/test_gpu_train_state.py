@@ -52,6 +52,45 @@ def test_entropy_vs_oracle(rows, vocab, dr, pad):
     assert met == plain.metrics
 
 
+@pytest.mark.parametrize("rows,vocab,dr,pad", [
+    (24, 151936, torch.bfloat16, 0),     # bulk-copy path, ragged last tile
+    (24, 12805, torch.float32, 3),       # unaligned rows: plain loads
+])
+def test_entropy_with_neg_inf_logits(rows, vocab, dr, pad):
+    """-inf logits inside full tiles (a masked vocabulary): their softmax terms
+    are 0 and add nothing to the entropy.  Rows without -inf give the same bits
+    as in a batch with no -inf at all."""
+    w = W.synthetic(rows, vocab, seed=vocab + 1, device=DEV, dtype_rollout=dr, row_pad=pad, active_prob=1.0)
+    g = torch.Generator().manual_seed(11)
+    tr, ro = w.train.clone(), w.rollout.clone()
+    ninf = float("-inf")
+    scatter = torch.rand(vocab, generator=g) < 0.1
+    tr[0, scatter.to(DEV)] = ninf                         # scattered, train side
+    ro[1, : vocab // 2] = ninf                            # a leading block, rollout side
+    tr[2, vocab // 3: vocab // 3 + 5000] = ninf           # a middle block, both sides
+    ro[2, vocab // 3: vocab // 3 + 5000] = ninf
+    keep = torch.zeros(vocab, dtype=torch.bool)
+    keep[torch.randint(0, vocab, (40,), generator=g)] = True
+    tr[3, ~keep.to(DEV)] = ninf                           # all but a few columns
+    ro[3, ~keep.to(DEV)] = ninf
+    tr[4, -1] = ninf                                      # the last column only
+    for r in range(5):                                    # selected tokens stay finite
+        c = int(w.token_ids[r])
+        tr[r, c], ro[r, c] = w.train[r, c], w.rollout[r, c]
+    (lt, lr, d, et, er), met = score_entropy(w, tr, ro)
+    mask = w.action_mask.cpu().numpy()
+    ref_t, ref_r = oracle.entropy(to_oracle(tr), to_oracle(ro), mask)
+    for got, want in ((et, ref_t), (er, ref_r)):
+        gn = got.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(gn)) and np.max(np.abs(gn - want)) <= ENT_ATOL
+    plain = B.score(tr, ro, w.token_ids, w.action_mask, w.clip)
+    torch.cuda.synchronize()
+    for a, b in ((lt, plain.logp_train), (lr, plain.logp_rollout), (d, plain.dlogp)):
+        assert torch.equal(a, b)
+    (_, _, _, et0, er0), _ = score_entropy(w)
+    assert torch.equal(et[5:], et0[5:]) and torch.equal(er[5:], er0[5:])
+
+
 def test_entropy_closed_forms():
     vocab = 5000
     u = torch.full((40, vocab), 1.5, dtype=torch.bfloat16, device=DEV)
