@@ -25,8 +25,15 @@ namespace lpd {
 // changing them changes results (bitwise), but never makes them depend on the
 // batch.
 constexpr int kRowPlain = 0, kRowTransform = 1, kRowEntropy = 2, kRowScale = 3, kRowSoftcap = 4;
-__host__ __device__ constexpr int row_warps(int mode) { return mode == kRowTransform ? 16 : 20; }
-constexpr int kConsumerWarps = 20;               // the largest W: the workspace's warp-state stride
+// Consumer warps W of the single-segment row pass by mode: 23 (with the
+// producer, 24 warps: six per SM sub-partition, each at the 80 registers a
+// thread that its register file allows), 20 for the reduced soft-cap (no
+// faster at 23), 16 for the general transform chain (its larger body needs
+// more registers).
+__host__ __device__ constexpr int row_warps(int mode) {
+    return mode == kRowTransform ? 16 : mode == kRowSoftcap ? 20 : 23;
+}
+constexpr int kConsumerWarps = 23;               // the largest W: the workspace's warp-state stride
 constexpr int kColsPerThread = 16;
 constexpr int kMaxSegments = 16;                 // shards per side
 constexpr int kRingBytes = 200 * 1024;           // shared-memory staging ring

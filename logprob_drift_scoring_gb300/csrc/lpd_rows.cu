@@ -11,10 +11,10 @@
 // blockIdx.x, blockIdx.x + gridDim.x, ...  A producer thread streams each row
 // through a ring of shared-memory stages with 1-D bulk copies (TMA,
 // cp.async.bulk, completion on an mbarrier); every stage holds the same tile of
-// 16 * 32 W columns of both sides (W consumer warps: 20, so 10240 columns; 16
-// for the general transform chain; 19, 20 or 16 for the plain pass over
-// several vocab segments, whichever pads the segments' last tiles least, see
-// row_pass_warps).  The W warps read the
+// 16 * 32 W columns of both sides (W consumer warps: 23, so 11776 columns; 20
+// for the reduced soft-cap; 16 for the general transform chain; 23, 20, 19 or
+// 16 for the plain pass over several vocab segments, whichever pads the
+// segments' last tiles least, see row_pass_warps).  The W warps read the
 // stage, and thread t owns columns [G g + 4t, G g + 4t + 4), g = 0..3, G =
 // 128 W, of every tile.  Each thread keeps an online (max, sum exp) pair per
 // side in fp32 plus the sum of the two sides' term differences; at the end of
@@ -592,7 +592,7 @@ int row_pass_warps(const Segment *segs, int n_seg, int mode, bool use_tma) {
     // as much as real columns.  Ties keep the most warps.
     int best = row_warps(mode);
     int64_t best_cols = -1;
-    for (int w : {20, 19, 16}) {
+    for (int w : {23, 20, 19, 16}) {
         const int64_t tile = static_cast<int64_t>(kColsPerThread) * 32 * w;
         int64_t cols = 0;
         for (int k = 0; k < n_seg; ++k) cols += (segs[k].len + tile - 1) / tile * tile;
@@ -607,6 +607,7 @@ int row_pass_warps(const Segment *segs, int n_seg, int mode, bool use_tma) {
 cudaError_t launch_rows(const RowArgs &a, int dtype_t, int dtype_r, bool use_tma, int mode, int warps,
                         cudaStream_t stream) {
     if (mode == kRowPlain && use_tma && a.n_seg > 1) {
+        if (warps == 23) return dispatch<true, kRowPlain, 23, true>(a, dtype_t, dtype_r, stream);
         if (warps == 19) return dispatch<true, kRowPlain, 19, true>(a, dtype_t, dtype_r, stream);
         if (warps == 16) return dispatch<true, kRowPlain, 16, true>(a, dtype_t, dtype_r, stream);
         return dispatch<true, kRowPlain, 20, true>(a, dtype_t, dtype_r, stream);
