@@ -76,6 +76,7 @@ struct Ws {
     double *dval;
     uint32_t *keys;
     BlockPartial *blockpart;
+    uint32_t *hist;
 };
 
 Ws carve(void *base, int64_t n_rows, int n_seg) {
@@ -84,7 +85,7 @@ Ws carve(void *base, int64_t n_rows, int n_seg) {
     return Ws{reinterpret_cast<WsHeader *>(b + L.header),  reinterpret_cast<int2 *>(b + L.rowid),
               reinterpret_cast<float2 *>(b + L.pick),      reinterpret_cast<float4 *>(b + L.part),
               reinterpret_cast<double *>(b + L.dval),      reinterpret_cast<uint32_t *>(b + L.keys),
-              reinterpret_cast<BlockPartial *>(b + L.blockpart)};
+              reinterpret_cast<BlockPartial *>(b + L.blockpart), reinterpret_cast<uint32_t *>(b + L.hist)};
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LPD_OK : LPD_ERR_CUDA; }
@@ -207,7 +208,7 @@ int run_rows(const Segment *segs, int n_seg, int32_t dt, int32_t dr, bool tma, c
 // Stage 3: metric terms per block, then the merge and the percentile select.
 int run_metrics(int64_t n_rows, double clip_lo, double clip_hi, lpd_metrics *met, const Ws &w, cudaStream_t s) {
     return cuda_status(launch_metrics(n_rows, std::log(clip_lo), std::log(clip_hi), w.hdr, w.rowid, w.dval, w.keys,
-                                      w.blockpart, met, s));
+                                      w.blockpart, w.hist, met, s));
 }
 
 int validate_pair(const lpd_logits *train, const lpd_logits *rollout, int64_t n_rows, int64_t vocab) {

@@ -87,8 +87,12 @@ struct BlockPartial {  // one finalise block's share of the metrics
 };
 
 struct WsLayout {
-    size_t header, rowid, pick, part, dval, keys, blockpart, total;
+    size_t header, rowid, pick, part, dval, keys, blockpart, hist, total;
 };
+
+// Bins of the first digit of the |dlogp| radix select (11 bits of the fp32
+// pattern: the exponent and four mantissa bits).
+constexpr int kKeyHistBins = 2048;
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -103,6 +107,7 @@ constexpr WsLayout ws_layout(int64_t n_rows, int n_seg) {
     L.dval = off;      off += align256(R * sizeof(double));        // dlogp per active row
     L.keys = off;      off += align256(R * sizeof(uint32_t));      // |dlogp| as fp32 bits
     L.blockpart = off; off += align256(((R + kFinThreads - 1) / kFinThreads) * sizeof(BlockPartial));
+    L.hist = off;      off += align256(kKeyHistBins * sizeof(uint32_t));  // first-digit histogram of the keys
     L.total = off;
     return L;
 }
@@ -221,7 +226,7 @@ cudaError_t launch_dlogp_rows(int64_t n_rows, const float *dlogp, const WsHeader
                               double *dval, uint32_t *keys, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
                            const int2 *rowid, const double *dval, const uint32_t *keys,
-                           BlockPartial *bp, lpd_metrics *metrics, cudaStream_t stream);
+                           BlockPartial *bp, uint32_t *hist, lpd_metrics *metrics, cudaStream_t stream);
 
 cudaError_t launch_backward(const void *x, int x_dtype, int64_t x_stride_elems, void *out, int out_dtype,
                             int64_t out_stride_elems, int64_t n_rows, int64_t vocab, const int32_t *ids,

@@ -346,15 +346,25 @@ __global__ void __launch_bounds__(kFinalizeThreads) finalize_kernel(const __grid
 // active rows with a fixed tree: sum |d|, sum (exp(d) - 1 - d) evaluated as
 // expm1(d) - d, sum expm1(d) (ratio0 mean = 1 + that / A), the count of
 // ratio0 outside [lo, hi] (as d < ln lo or d > ln hi), and max |d| with the
-// lowest row index among ties.
+// lowest row index among ties.  Also the first pass of the percentile select:
+// the block's histogram of the keys' first digit (bits 30..20) in shared
+// memory, added to the zeroed global one bin by bin (integer counts, so the
+// order of the additions does not matter).
+constexpr int kKeyShift0 = 20;
+
 __global__ void __launch_bounds__(kFinThreads) terms_kernel(double ln_clip_lo, double ln_clip_hi,
                                                             const WsHeader *hdr, const int2 *rowid,
-                                                            const double *dval, BlockPartial *bp) {
+                                                            const double *dval, const uint32_t *keys,
+                                                            BlockPartial *bp, uint32_t *hist) {
     __shared__ Part sh[kFinThreads];
+    __shared__ uint32_t bh[kKeyHistBins];
     const int64_t n_active = hdr->n_active;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+    for (int b = threadIdx.x; b < kKeyHistBins; b += kFinThreads) bh[b] = 0;
     Part p = neutral_part();
+    __syncthreads();
     if (i < n_active) {
+        atomicAdd(&bh[(keys[i] >> kKeyShift0) & (kKeyHistBins - 1)], 1u);
         const double d = dval[i];
         const double em1 = expm1(d);
         p.sum_abs = fabs(d);
@@ -366,6 +376,8 @@ __global__ void __launch_bounds__(kFinThreads) terms_kernel(double ln_clip_lo, d
     }
     sh[threadIdx.x] = p;
     __syncthreads();
+    for (int b = threadIdx.x; b < kKeyHistBins; b += kFinThreads)
+        if (bh[b]) atomicAdd(&hist[b], bh[b]);
     block_tree<kFinThreads>(sh);
     if (threadIdx.x == 0) {
         BlockPartial &o = bp[blockIdx.x];
@@ -385,18 +397,24 @@ __global__ void __launch_bounds__(kFinThreads) terms_kernel(double ln_clip_lo, d
 // patterns of |dlogp| (monotone for non-negative floats; the sign bit is always
 // 0), in three passes of 11, 10 and 10 bits, both ranks in the same passes.
 // The first digit covers the exponent and four mantissa bits, so keys that
-// share an order of magnitude still spread over several histogram bins.  The
-// maximum comes exact from the partials.
-constexpr int kSelBins = 2048;
+// share an order of magnitude still spread over several histogram bins; its
+// histogram (one for both ranks) comes from the terms kernel's blocks, and
+// this CTA reads the keys only for the two narrower passes.  The maximum comes
+// exact from the partials.
+constexpr int kSelBins = kKeyHistBins;
+constexpr int kSelBatch = 8;
 
 __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, const WsHeader *hdr,
                                                               const uint32_t *keys, const BlockPartial *bp,
-                                                              lpd_metrics *out) {
+                                                              const uint32_t *hist0, lpd_metrics *out) {
     constexpr int kFold = 256;  // threads that fold block partials
     __shared__ Part sh[kFold];
     __shared__ uint32_t hist[2][kSelBins];
     __shared__ uint32_t prefix[2];
     __shared__ long long rank[2];
+    __shared__ uint32_t wsum[2][32];    // per-warp bin totals, then their exclusive scan
+    __shared__ uint32_t sel_bin[2];     // the bin holding each rank in this pass
+    __shared__ long long sel_rank[2];   // the rank within that bin
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t n_active = hdr->n_active;
 
@@ -421,48 +439,94 @@ __global__ void __launch_bounds__(kSelThreads) metrics_kernel(int64_t n_blocks, 
     block_tree<kFold>(sh);
 
     if (n_active > 0) {
-        const int shifts[3] = {20, 10, 0};
+        const int shifts[3] = {kKeyShift0, 10, 0};
         const int widths[3] = {11, 10, 10};
         for (int pass = 0; pass < 3; ++pass) {
             const int shift = shifts[pass];
             const uint32_t dmask = (1u << widths[pass]) - 1u;
             const int nbins = 1 << widths[pass];
             const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (shift + widths[pass]));
-            for (int b = tid; b < 2 * kSelBins; b += kSelThreads) (&hist[0][0])[b] = 0;
-            __syncthreads();
+            if (pass == 0) {
+                // the first digit's histogram, built by the terms kernel's
+                // blocks (one histogram serves both ranks: empty prefix)
+                for (int b = tid; b < kSelBins; b += kSelThreads) hist[0][b] = hist0[b];
+                __syncthreads();
+            } else {
+                for (int b = tid; b < 2 * kSelBins; b += kSelThreads) (&hist[0][0])[b] = 0;
+                __syncthreads();
+            }
             const uint32_t p0 = prefix[0], p1 = prefix[1];
-            for (int64_t i = tid; i < n_active; i += kSelThreads) {
-                const uint32_t key = keys[i];
-                const uint32_t dig = (key >> shift) & dmask;
-                if ((key & hi_mask) == p0) atomicAdd(&hist[0][dig], 1u);
-                if ((key & hi_mask) == p1) atomicAdd(&hist[1][dig], 1u);
+            // kSelBatch keys a thread in flight before their histogram updates
+            const int64_t step = static_cast<int64_t>(kSelThreads) * kSelBatch;
+            for (int64_t base = tid; pass > 0 && base < n_active; base += step) {
+                uint32_t key[kSelBatch];
+#pragma unroll
+                for (int j = 0; j < kSelBatch; ++j) {
+                    const int64_t i = base + static_cast<int64_t>(j) * kSelThreads;
+                    key[j] = i < n_active ? keys[i] : 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < kSelBatch; ++j) {
+                    if (base + static_cast<int64_t>(j) * kSelThreads >= n_active) break;
+                    const uint32_t dig = (key[j] >> shift) & dmask;
+                    if ((key[j] & hi_mask) == p0) atomicAdd(&hist[0][dig], 1u);
+                    if ((key[j] & hi_mask) == p1) atomicAdd(&hist[1][dig], 1u);
+                }
+            }
+            __syncthreads();
+            // Both ranks' bins at once, over the whole block: thread t owns
+            // bins [t per, (t + 1) per) of each histogram; counts are scanned
+            // within warps by shuffles, then across the 32 warp totals.
+            const int per = nbins / kSelThreads;
+            uint32_t tot[2], incl[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t *h = hist[pass == 0 ? 0 : r];
+                tot[r] = 0;
+                for (int b = 0; b < per; ++b) tot[r] += h[tid * per + b];
+                incl[r] = tot[r];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl[r], off);
+                    if (lane >= off) incl[r] += y;
+                }
+                if (lane == 31) wsum[r][warp] = incl[r];
             }
             __syncthreads();
             if (warp < 2) {
-                // lane l owns bins [l * per, (l + 1) * per)
-                const int per = nbins / 32;
-                uint32_t tot = 0;
-                for (int b = 0; b < per; ++b) tot += hist[warp][lane * per + b];
-                uint32_t incl = tot;
+                // exclusive scan of warp `warp`'s rank over the 32 warp totals
+                const uint32_t t = wsum[warp][lane];
+                uint32_t x = t;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += y;
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
                 }
-                const long long k = rank[warp];
-                const long long before = static_cast<long long>(incl - tot);
-                if (before < k && k <= static_cast<long long>(incl)) {
+                wsum[warp][lane] = x - t;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t *h = hist[pass == 0 ? 0 : r];
+                const long long k = rank[r];
+                const long long before = static_cast<long long>(wsum[r][warp]) + (incl[r] - tot[r]);
+                if (before < k && k <= before + static_cast<long long>(tot[r])) {
                     long long acc = before;
                     for (int b = 0; b < per; ++b) {
-                        const uint32_t c = hist[warp][lane * per + b];
+                        const uint32_t c = h[tid * per + b];
                         if (acc + c >= k) {
-                            prefix[warp] |= static_cast<uint32_t>(lane * per + b) << shift;
-                            rank[warp] = k - acc;
+                            sel_bin[r] = static_cast<uint32_t>(tid * per + b);
+                            sel_rank[r] = k - acc;
                             break;
                         }
                         acc += c;
                     }
                 }
+            }
+            __syncthreads();
+            if (tid < 2) {
+                prefix[tid] |= sel_bin[tid] << shift;
+                rank[tid] = sel_rank[tid];
             }
             __syncthreads();
         }
@@ -527,15 +591,16 @@ cudaError_t launch_finalize(const FinArgs &a, int64_t n_rows, cudaStream_t strea
 
 cudaError_t launch_metrics(int64_t n_rows, double ln_clip_lo, double ln_clip_hi, const WsHeader *hdr,
                            const int2 *rowid, const double *dval, const uint32_t *keys, BlockPartial *bp,
-                           lpd_metrics *metrics, cudaStream_t stream) {
+                           uint32_t *hist, lpd_metrics *metrics, cudaStream_t stream) {
     const int64_t blocks = (n_rows + kFinThreads - 1) / kFinThreads;
     if (blocks > 0) {
-        terms_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(ln_clip_lo, ln_clip_hi, hdr,
-                                                                               rowid, dval, bp);
-        const cudaError_t e = cudaGetLastError();
+        cudaError_t e = cudaMemsetAsync(hist, 0, kKeyHistBins * sizeof(uint32_t), stream);
         if (e != cudaSuccess) return e;
+        terms_kernel<<<static_cast<unsigned>(blocks), kFinThreads, 0, stream>>>(ln_clip_lo, ln_clip_hi, hdr,
+                                                                               rowid, dval, keys, bp, hist);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    metrics_kernel<<<1, kSelThreads, 0, stream>>>(blocks, hdr, keys, bp, metrics);
+    metrics_kernel<<<1, kSelThreads, 0, stream>>>(blocks, hdr, keys, bp, hist, metrics);
     return cudaGetLastError();
 }
 
