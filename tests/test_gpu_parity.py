@@ -81,6 +81,11 @@ CASES = {
     # 300 000 rows: many grid-stride passes per CTA and a percentile select
     # over ~270 000 keys
     "many_rows_vocab16": (300_000, 16, torch.bfloat16, torch.bfloat16, {}),
+    # around the plain pass's 11 776-column tile (23 consumer warps x 512):
+    # exactly one tile, one column past two tiles, one column short of a tile
+    "bf16_one_full_tile": (120, 11776, torch.bfloat16, torch.bfloat16, {}),
+    "bf16_two_tiles_plus_one": (120, 2 * 11776 + 1, torch.bfloat16, torch.bfloat16, {}),
+    "mixed_one_tile_minus_one": (100, 11775, torch.bfloat16, torch.float32, {}),
 }
 
 
@@ -301,6 +306,10 @@ def _small_sharded(bounds, rows=120, seed=20):
     [(a, b) for a, b in zip([0, 700, 701, 2000, 2100, 4097, 5000, 6000, 6001, 7000, 8192, 9000, 10001, 11000, 12000,
                              13000], [700, 701, 2000, 2100, 4097, 5000, 6000, 6001, 7000, 8192, 9000, 10001, 11000,
                                       12000, 13000, 14001])],
+    # segment lengths that make the multi-segment pass take 23 consumer warps:
+    # whole 11 776-column tiles, then ragged last tiles padded by -inf copies
+    [(0, 23552), (23552, 47104)],
+    [(0, 22776), (22776, 45552)],
 ])
 def test_sharded_vs_oracle(bounds):
     base, w = _small_sharded(bounds)

@@ -33,6 +33,7 @@ def score_entropy(w, train=None, rollout=None):
     (120, 9000, torch.float32, 0),
     (60, 151936, torch.bfloat16, 0),
     (80, 7, torch.bfloat16, 0),
+    (90, 11776 + 8, torch.float32, 0),   # one full tile and an 8-column ragged one
 ])
 def test_entropy_vs_oracle(rows, vocab, dr, pad):
     w = W.synthetic(rows, vocab, seed=rows + vocab, device=DEV, dtype_rollout=dr, row_pad=pad, spike_frac=0.1)
@@ -54,6 +55,7 @@ def test_entropy_vs_oracle(rows, vocab, dr, pad):
 
 @pytest.mark.parametrize("rows,vocab,dr,pad", [
     (24, 151936, torch.bfloat16, 0),     # bulk-copy path, ragged last tile
+    (24, 2 * 11776, torch.bfloat16, 0),  # whole tiles only: every column on the unclamped path
     (24, 12805, torch.float32, 3),       # unaligned rows: plain loads
 ])
 def test_entropy_with_neg_inf_logits(rows, vocab, dr, pad):
