@@ -57,8 +57,8 @@ std::mutex g_lock;
 typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// The driver's cuCtxGetCurrent and cuCtxGetId, fetched once through the
-// runtime (the library links only the CUDA runtime).
+// The CUDA driver API's cuCtxGetCurrent and cuCtxGetId, fetched once through
+// the runtime (the library links only the CUDA runtime).
 bool driver_ctx_fns(CtxGetCurrentFn *get_current, CtxGetIdFn *get_id) {
     static CtxGetCurrentFn s_cur = nullptr;
     static CtxGetIdFn s_id = nullptr;

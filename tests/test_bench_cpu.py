@@ -65,8 +65,8 @@ def test_launch_command():
 
 
 def test_reference_arm_under_two_ranks_prints_one_line():
-    # the reference arm as the driver launches it for N = 2 (torchrun, CPU
-    # only): rank 0 alone scores and prints; n_gpus is the world size
+    # the reference arm launched under torchrun for N = 2 (CPU only): rank 0
+    # alone scores and prints; n_gpus is the world size
     import json
 
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2", "--master-addr",
