@@ -570,7 +570,7 @@ int lpd_attn_merge_order_drift(const void *out_parts, int32_t parts_dtype, const
 /* ---- scoring without a caller-provided workspace -------------------------- */
 
 /* Largest n_rows lpd_score_noalloc accepts: its built-in scratch is sized for
- * this many rows (about 21.9 MB of device memory per GPU that loads the
+ * this many rows (about 25 MB of device memory per GPU that loads the
  * library, held until the process exits). */
 #define LPD_NOALLOC_MAX_ROWS 32768
 
