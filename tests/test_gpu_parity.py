@@ -422,3 +422,31 @@ def test_stalled_pipeline_times_out_cleanly(monkeypatch):
     assert res.metrics["status"] & B.LPD_STATUS_TIMEOUT
     monkeypatch.delenv("LPD_STALL_ROW_PASS")
     check_against_oracle(w)
+
+
+def test_drift_metrics_repeated_on_one_workspace():
+    """The staged calls, then the metrics stage twice more on the same
+    workspace (its select histogram is rebuilt each call) and once with other
+    clip bounds: the same record each time at the same bounds, and the oracle's
+    metrics at the others."""
+    w = W.synthetic(20000, 3000, seed=41, device=DEV, rollout_noise=0.3)
+    n = w.n_rows
+    lt, lr, d = (torch.empty(n, dtype=torch.float32, device=DEV) for _ in range(3))
+    met = torch.empty(B.METRICS_BYTES, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(B.lpd_workspace_size(B.LPD_KIND_SCORE, n), dtype=torch.uint8, device=DEV)
+    B.lpd_select_active(w.token_ids, w.action_mask, lt, lr, d, met, ws)
+    B.lpd_token_logp(w.train, w.rollout, lt, lr, d, met, ws)
+    B.lpd_drift_metrics(n, 0.8, 1.2, met, ws)
+    torch.cuda.synchronize()
+    first = B.read_metrics(met)
+    B.lpd_drift_metrics(n, 0.8, 1.2, met, ws)
+    B.lpd_drift_metrics(n, 0.8, 1.2, met, ws)
+    torch.cuda.synchronize()
+    assert B.read_metrics(met) == first
+    B.lpd_drift_metrics(n, 0.5, 1.5, met, ws)
+    torch.cuda.synchronize()
+    other = B.read_metrics(met)
+    mask = w.action_mask.cpu().numpy()
+    ref = oracle_score(w.train, w.rollout, w.token_ids, w.action_mask, clip=(0.5, 1.5))
+    assert_metrics_match(other, ref.metrics, ref.dlogp, mask, (0.5, 1.5))
+    assert other["p95_abs_dlogp"] == first["p95_abs_dlogp"] and other["clipfrac0"] < first["clipfrac0"]
