@@ -1038,7 +1038,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["lpd", "reference"], default="lpd")
     ap.add_argument("--config", choices=sorted(CONFIGS), default="qwen")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=16, help="reference arm: rows per host thread per step")
