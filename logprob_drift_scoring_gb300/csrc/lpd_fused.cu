@@ -26,9 +26,9 @@
 //      warps per row cut that wait to a quarter, each warp loads both sides'
 //      columns before one wait, and each frees its share as soon as its reads
 //      are done (the states travel to the row's lead warp through a separate
-//      shared-memory buffer).  Tiles are visited in groups of 8 row
-//      tiles so that the CTAs running together share their W tiles and hidden
-//      tiles in L2.
+//      shared-memory buffer).  Tiles are visited in groups of 16 row
+//      tiles (2048 tokens) so that the CTAs running together share their W
+//      tiles and hidden tiles in L2, and W is read from memory once a group.
 //   3. head_finalize_kernel: one warp per active row merges its vocab-tile
 //      partials in vocab order (fixed tree) and applies the same fp64 row
 //      arithmetic as the unfused path.
@@ -63,7 +63,7 @@ constexpr int kEpiSplit = 4;                   // epilogue warps per tensor-memo
 constexpr int kEpiWarps = 4 * kEpiSplit;
 constexpr int kEpiCols = kBN / kEpiSplit;      // accumulator columns per epilogue warp
 constexpr int kHeadThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
-constexpr int kGroupM = 8;                     // row tiles per raster group
+constexpr int kGroupM = 16;                    // row tiles per raster group
 constexpr uint32_t kTmemCols = 512;            // two 128 x 256 fp32 accumulators
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 constexpr uint32_t kWaitLimitIters = 1u << 30;
